@@ -1,0 +1,238 @@
+/*
+ * w4a16moe.h -- C ABI of the GB300 (sm_103a) W4A16 INT4 MoE expert GEMM pair.
+ *
+ * The operator is the Chord/Humming W4A16 MoE expert pair: gate_up, then
+ * down, over INT4 group-32 weights with BF16 scales and BF16 activations.
+ * Sources (page titles abbreviated):
+ *   [P-arex]   "vLLM 宣布 Humming 后端可运行 Novita 开源的 Chord 内核，称 H200 TP8
+ *              提速 1.33x、B300 EP8 decode 提速 2.15x" (arex-research)
+ *   [P-lens]   "vLLM と Novita AI が Chord をリリース：Kimi K2.x 用の高速 INT4 MoE
+ *              カーネル" (agentlenshq)
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Every pointer named *_d / a / out / packed / workspace is DEVICE memory
+ *   of the current CUDA device, allocated and owned by the caller. The
+ *   library allocates no memory and keeps no per-call state.
+ * - BF16 tensors are passed as uint16_t bit patterns.
+ * - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *   stream). Work is enqueued asynchronously; a call returns once it is
+ *   enqueued. Unless a flag says otherwise no call synchronises, so calls can
+ *   be captured in a CUDA graph (the over-allocated routing buffers make the
+ *   grid independent of the routing, [P-lens] "ランタイムの考慮事項").
+ * - Every call validates its arguments on the host before it enqueues
+ *   anything and returns a w4a16_status; nothing is enqueued on error.
+ *   A failed launch returns W4A16_ERR_CUDA.
+ * - All entry points are thread-safe.
+ */
+#ifndef W4A16MOE_H
+#define W4A16MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  W4A16_OK = 0,
+  W4A16_ERR_INVALID_ARG = 1,  /* null pointer, negative size, bad enum     */
+  W4A16_ERR_UNSUPPORTED = 2,  /* quantisation scheme or shape not handled:
+                                 reported at load, never a silent fallback
+                                 ([P-arex] "接入方式", [P-lens] "vLLM との統合") */
+  W4A16_ERR_ROUTING = 3,      /* routing tensors failed validation         */
+  W4A16_ERR_WORKSPACE = 4,    /* workspace missing or too small            */
+  W4A16_ERR_CUDA = 5,         /* a CUDA runtime call or launch failed      */
+  W4A16_ERR_TIMEOUT = 6       /* a device-side wait gave up (see
+                                 w4a16_read_device_status)                 */
+} w4a16_status;
+
+/* GEMM modes of the indexed family. */
+enum { W4A16_GATE_UP = 0, W4A16_DOWN = 1 };
+/* Grouped families. */
+enum { W4A16_GROUPED_CONTIGUOUS = 0, W4A16_GROUPED_MASKED = 1 };
+/* Call flags. */
+enum {
+  W4A16_FLAG_VALIDATE_ROUTING = 1, /* copy the routing tensors to the host and
+                                      check them before the launch; this
+                                      synchronises `stream` and is therefore
+                                      not graph-capturable ([P-lens]
+                                      "ランタイムの考慮事項": trusted routing
+                                      validation off = capturable)          */
+  W4A16_FLAG_ACCUMULATE = 2        /* DOWN: add into `out` instead of first
+                                      zeroing it                            */
+};
+/* Packed weight layouts (w4a16_prepack). One layout serves every family. */
+enum { W4A16_LAYOUT_KTILE64 = 0 };
+
+/* Static description of a status code. Never NULL. */
+const char* w4a16_status_string(int status);
+
+/* ABI version of this header (major * 100 + minor). */
+int w4a16_version(void);
+
+/*
+ * Schedule chosen from the shape and from tok_e, the routed rows per expert
+ * ([P-arex] "调度由每个专家收到的 token 数决定": tok_e, not the total token
+ * count, decides which schedule wins; [P-lens] "カーネルレベルの最適化").
+ */
+typedef struct {
+  int block_m;     /* routing block rows: the align block size and the
+                      largest MMA N of one work item (16..256, step 16)   */
+  int bn;          /* weight rows per tile (MMA M) = 128                  */
+  int bk;          /* K elements per pipeline step = 64                   */
+  int stages;      /* weight ring depth, in pairs of K steps (2..16)      */
+  int b_stages;    /* activation ring depth (2..16)                       */
+  int split_k;     /* 1 (no split of K)                                   */
+  int ctas_per_sm; /* 1 (persistent, one CTA per SM)                      */
+  int swap_ab;     /* 1: weights are the MMA M operand, tokens the N one  */
+  int layout;      /* W4A16_LAYOUT_KTILE64                                */
+  int grid;        /* CTAs to launch; 0 = number of SMs x ctas_per_sm     */
+} w4a16_plan_t;
+
+/*
+ * Fill *out for a GEMM with output width n and reduction length k over
+ * `tokens` tokens routed top-`topk` to `num_experts` local experts.
+ * tok_e_hint > 0 overrides the expected rows per expert (default
+ * tokens * topk / num_experts); it is known on the host without a sync.
+ * Host only. Errors: INVALID_ARG on non-positive sizes or a NULL out.
+ */
+w4a16_status w4a16_plan(int tokens, int topk, int num_experts, int n, int k,
+                        float tok_e_hint, w4a16_plan_t* out);
+
+/*
+ * Rows to allocate for sorted_ids so that any routing of `numel` rows over
+ * `num_experts` experts fits after padding every expert to block_m:
+ * roundup(numel + min(num_experts, numel) * (block_m - 1), block_m).
+ * expert_ids needs capacity / block_m entries. Host only; 0 on bad input.
+ */
+size_t w4a16_align_capacity(int numel, int num_experts, int block_m);
+
+/*
+ * moe_align_block_size ([P-arex] "调度由每个专家收到的 token 数决定": the
+ * indexed kernel consumes sorted_ids / expert_ids / num_tokens_padded).
+ *   topk_ids   int32 [tokens, topk] device: local expert id of each routed
+ *              row, any value outside [0, num_experts) = not local (skipped).
+ *   sorted_ids int32 [capacity] device out: for e ascending, the flattened
+ *              rows i = t*topk + k with topk_ids.flat[i] == e in ascending i,
+ *              padded with the sentinel tokens*topk to a multiple of block_m;
+ *              entries past the padded total also hold the sentinel.
+ *   expert_ids int32 [capacity/block_m] device out: expert of each block,
+ *              -1 past the padded total.
+ *   num_tokens_padded int32 [1] device out: the padded total.
+ * capacity must be a multiple of block_m and at least
+ * w4a16_align_capacity(tokens*topk, num_experts, block_m), so the output
+ * always fits. block_m in [1, 1024]; num_experts in [1, 1024].
+ * Deterministic: the result is unique and bit-exact.
+ */
+w4a16_status w4a16_moe_align_block_size(const int32_t* topk_ids, int tokens, int topk,
+                                        int num_experts, int block_m, int capacity,
+                                        int32_t* sorted_ids, int32_t* expert_ids,
+                                        int32_t* num_tokens_padded, void* stream);
+
+/*
+ * Bytes of the packed weights of `num_experts` experts of shape [n, k].
+ * Schema ([P-arex] "接入方式"): uint4, group 32, BF16 scales. group must be
+ * 32 and k a positive multiple of 32, else W4A16_ERR_UNSUPPORTED; layout
+ * must be W4A16_LAYOUT_KTILE64. Host only.
+ */
+w4a16_status w4a16_prepack_size(int num_experts, int n, int k, int group, int layout,
+                                size_t* bytes);
+
+/*
+ * Repack checkpoint weights into the kernel layout (once, at load; the layout
+ * is fixed at load, [P-arex] "调度由每个专家收到的 token 数决定").
+ *   q       uint8 [num_experts, n, k/2] device: uint4 codes, even k in the
+ *           low nibble; the weight is (q - 8) * scale.
+ *   scales  BF16 [num_experts, n, k/32] device: one scale per 32 k.
+ *   packed  device out, packed_bytes >= w4a16_prepack_size(...), 16-byte
+ *           aligned. Opaque: 128-row tiles x 64-k steps, contiguous along k
+ *           inside a tile; rows past n and k past k hold zero weights.
+ */
+w4a16_status w4a16_prepack(const uint8_t* q, const uint16_t* scales, int num_experts, int n,
+                           int k, int group, int layout, void* packed, size_t packed_bytes,
+                           void* stream);
+
+/* Inverse of w4a16_prepack (for checking a packed blob byte for byte). */
+w4a16_status w4a16_unpack(const void* packed, int num_experts, int n, int k, uint8_t* q,
+                          uint16_t* scales, void* stream);
+
+/*
+ * Device workspace bytes for a GEMM call under `plan` (at least 256: the
+ * device status words). The caller zero-fills a new workspace once; the
+ * library keeps it zero except when a device-side wait gives up.
+ */
+size_t w4a16_workspace_size(const w4a16_plan_t* plan, int rows, int n);
+
+/*
+ * Indexed W4A16 MoE GEMM ([P-arex] "调度由每个专家收到的 token 数决定",
+ * "六个场景的逐层测量与限定条件"; [P-lens] "コア貢献").
+ * Weights: `packed` from w4a16_prepack with [num_experts, n, k].
+ * For each block b < num_tokens_padded / plan->block_m with expert
+ * e = expert_ids[b] in [0, num_experts) and each row i = sorted_ids[...] of
+ * the block with i < tokens*topk:
+ *   GATE_UP: a = x BF16 [tokens, k]; out BF16 [tokens*topk, n]:
+ *            out[i, :] = bf16( x[i / topk, :] . W_e^T ), fp32 accumulation.
+ *            Rows of out not routed to a local expert are left untouched.
+ *   DOWN:    a = activation BF16 [tokens*topk, k] (rows by flattened id);
+ *            topk_weights fp32 [tokens, topk]; out fp32 [tokens, n]:
+ *            out[i / topk, :] += topk_weights.flat[i] * ( a[i, :] . W_e^T ).
+ *            `out` is zeroed first unless W4A16_FLAG_ACCUMULATE. Summation
+ *            order across the top-k rows of a token is not fixed.
+ * The routing buffers may be over-allocated (capacity rows); the grid does
+ * not depend on their contents. Blocks with expert -1 and sentinel rows are
+ * skipped; ids out of range are ignored, never dereferenced.
+ * Requires: k % 32 == 0, n >= 1, plan from w4a16_plan (block_m equal to the
+ * align block size, 16..256 step 16), workspace >= w4a16_workspace_size,
+ * a, out 16-byte aligned.
+ */
+w4a16_status w4a16_moe_indexed_gemm(int mode, const void* packed, int num_experts, int n, int k,
+                                    const uint16_t* a, int tokens, int topk,
+                                    const int32_t* sorted_ids, const int32_t* expert_ids,
+                                    const int32_t* num_tokens_padded, int capacity,
+                                    const float* topk_weights, void* out, int flags,
+                                    const w4a16_plan_t* plan, void* workspace, size_t ws_bytes,
+                                    void* stream);
+
+/*
+ * Grouped W4A16 MoE GEMM ([P-lens] "グループ化 SM90 カーネル技術").
+ *   CONTIGUOUS: a BF16 [m, k] with each expert's rows padded to a multiple
+ *     of 128 rows; layout = m_expert int32 [m], the expert of every row or
+ *     -1 for padding; every aligned 128-row block holds rows of one expert.
+ *     out BF16 [m, n]: out[r] = bf16(a[r] . W_{m_expert[r]}^T) for valid r.
+ *     m must be a multiple of plan->block_m, which must divide 128.
+ *   MASKED: a BF16 [num_experts, m, k] (m = the fixed row budget max_m);
+ *     layout = masked_m int32 [num_experts]; out BF16 [num_experts, m, n]:
+ *     rows r < masked_m[e] of expert e get bf16(a[e, r] . W_e^T).
+ * Padding rows of out are left untouched. expected_m is the expected rows
+ * per expert (schedule hint only).
+ */
+w4a16_status w4a16_moe_grouped_gemm(int kind, const void* packed, int num_experts, int n, int k,
+                                    const uint16_t* a, int m, const int32_t* layout,
+                                    int expected_m, uint16_t* out, int flags,
+                                    const w4a16_plan_t* plan, void* workspace, size_t ws_bytes,
+                                    void* stream);
+
+/*
+ * Activation between gate_up and down (the pages leave it out of the timed
+ * pair, [P-arex] "六个场景的逐层测量与限定条件"; its form is this library's
+ * reading): in BF16 [rows, 2*inter] = [gate | up]; out BF16 [rows, inter]
+ * = bf16(silu(gate) * up), computed in fp32. inter % 8 == 0.
+ */
+w4a16_status w4a16_silu_and_mul(const uint16_t* in, int rows, int inter, uint16_t* out,
+                                void* stream);
+
+/*
+ * Synchronise `stream`, read the device status word of `workspace`, reset it
+ * to zero, and return W4A16_OK or W4A16_ERR_TIMEOUT (a device-side wait of a
+ * GEMM gave up after about a second; the kernel then ended early and its
+ * output is incomplete). *detail (optional) receives the raw word.
+ */
+w4a16_status w4a16_read_device_status(void* workspace, int* detail, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4A16MOE_H */

@@ -1,0 +1,149 @@
+"""Host-side checks of the C ABI: the library builds and loads, exports every
+symbol the header declares, and its host-only entry points (scheduler,
+capacity, sizes, argument validation) behave as documented. No GPU needed:
+no call here reaches a kernel."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from w4a16_int4_moe_gb300 import ops
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                      "include", "w4a16moe.h")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(w4a16_[a-z_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = _declared_functions()
+    assert len(names) >= 13
+    for name in names:
+        assert hasattr(lib, name), name
+    assert set(names) == set(ops.EXPORTED)
+
+
+def test_status_strings(lib):
+    for st in range(7):
+        assert ops.status_string(st)
+    assert ops.status_string(99) == "unknown status"
+    assert ops.w4a16_version() == 100
+
+
+def test_align_capacity_closed_form(lib):
+    # roundup(numel + min(E, numel) * (bm - 1), bm)
+    assert ops.w4a16_align_capacity(576 * 8, 48, 16) == ((4608 + 48 * 15 + 15) // 16) * 16
+    assert ops.w4a16_align_capacity(6, 3, 4) == 16
+    assert ops.w4a16_align_capacity(2, 384, 16) == 32      # min(E, numel) = 2
+    assert ops.w4a16_align_capacity(0, 8, 16) == 0
+    assert ops.w4a16_align_capacity(-1, 8, 16) == 0
+
+
+def test_plan_follows_tok_e(lib):
+    # decode, 9-15 rows/expert: one block per expert with headroom
+    p = ops.w4a16_plan(576, 8, 384, 4096, 7168, 12.0)
+    assert p.block_m == 32 and p.bn == 128 and p.bk == 64 and p.swap_ab == 1
+    # TP8 T=16: a third of a row per expert
+    assert ops.w4a16_plan(16, 8, 384, 512, 7168).block_m == 16
+    # prefill above the ~80 rows/expert switch
+    assert ops.w4a16_plan(8192, 8, 384, 4096, 7168, 81.3).block_m == 128
+    assert ops.w4a16_plan(8192, 8, 48, 4096, 7168, 600.0).block_m == 256
+    for tok_e in (0.3, 5, 12, 40, 80, 81, 150, 400):
+        p = ops.w4a16_plan(1024, 8, 48, 4096, 7168, float(tok_e))
+        assert 16 <= p.block_m <= 256 and p.block_m % 16 == 0
+        assert 2 <= p.stages <= 16 and p.b_stages % 2 == 0 and p.split_k == 1
+
+
+def test_plan_rejects_bad_sizes(lib):
+    p = ops.Plan()
+    assert lib.w4a16_plan(0, 8, 0, 1, 1, 0.0, ctypes.byref(p)) == ops.W4A16_ERR_INVALID_ARG
+    assert lib.w4a16_plan(4, 8, 4, 1, 1, 0.0, None) == ops.W4A16_ERR_INVALID_ARG
+
+
+def test_prepack_size_and_unsupported_schemes(lib):
+    assert ops.w4a16_prepack_size(48, 4096, 7168) == 48 * 32 * 112 * 4608
+    # ragged n pads to whole 128-row tiles, k = 32 mod 64 to a whole k step
+    assert ops.w4a16_prepack_size(2, 130, 96) == 2 * 2 * 2 * 4608
+    out = ctypes.c_size_t(0)
+    # group != 32, k not a multiple of 32, unknown layout: refused at load
+    assert lib.w4a16_prepack_size(1, 128, 128, 64, 0, ctypes.byref(out)) == ops.W4A16_ERR_UNSUPPORTED
+    assert lib.w4a16_prepack_size(1, 128, 100, 32, 0, ctypes.byref(out)) == ops.W4A16_ERR_UNSUPPORTED
+    assert lib.w4a16_prepack_size(1, 128, 128, 32, 7, ctypes.byref(out)) == ops.W4A16_ERR_UNSUPPORTED
+    assert lib.w4a16_prepack(None, None, 1, 128, 128, 16, 0, None, 0, None) == ops.W4A16_ERR_UNSUPPORTED
+    assert lib.w4a16_prepack(None, None, 1, 128, 128, 32, 0, None, 0, None) == ops.W4A16_ERR_INVALID_ARG
+
+
+def test_gemm_argument_checks_before_any_launch(lib):
+    plan = ops.w4a16_plan(64, 2, 8, 1024, 512)
+    fake = ctypes.c_void_p(1 << 20)   # never dereferenced: checks fail first
+    args = dict(mode=ops.W4A16_GATE_UP, packed=fake, E=8, n=1024, k=512, a=fake, tokens=64,
+                topk=2, sid=fake, eid=fake, ntp=fake, cap=256, w=None, out=fake, flags=0,
+                ws=fake, wsb=256)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return lib.w4a16_moe_indexed_gemm(a["mode"], a["packed"], a["E"], a["n"], a["k"], a["a"],
+                                          a["tokens"], a["topk"], a["sid"], a["eid"], a["ntp"],
+                                          a["cap"], a["w"], a["out"], a["flags"], ctypes.byref(plan),
+                                          a["ws"], a["wsb"], None)
+    assert call(mode=7) == ops.W4A16_ERR_INVALID_ARG
+    assert call(k=500) == ops.W4A16_ERR_UNSUPPORTED           # k % 32 != 0
+    assert call(mode=ops.W4A16_DOWN) == ops.W4A16_ERR_INVALID_ARG  # no top-k weights
+    assert call(ws=None) == ops.W4A16_ERR_WORKSPACE
+    assert call(wsb=16) == ops.W4A16_ERR_WORKSPACE
+    assert call(cap=250) == ops.W4A16_ERR_INVALID_ARG          # not a multiple of block_m
+    assert call(flags=64) == ops.W4A16_ERR_INVALID_ARG
+    assert call(out=ctypes.c_void_p((1 << 20) + 2)) == ops.W4A16_ERR_INVALID_ARG  # misaligned
+    bad = ops.Plan.from_buffer_copy(plan)
+    bad.block_m = 24
+    assert lib.w4a16_moe_indexed_gemm(0, fake, 8, 1024, 512, fake, 64, 2, fake, fake, fake, 240,
+                                      None, fake, 0, ctypes.byref(bad), fake, 256, None) \
+        == ops.W4A16_ERR_INVALID_ARG
+    bad = ops.Plan.from_buffer_copy(plan)
+    bad.split_k = 2
+    assert lib.w4a16_moe_indexed_gemm(0, fake, 8, 1024, 512, fake, 64, 2, fake, fake, fake, 256,
+                                      None, fake, 0, ctypes.byref(bad), fake, 256, None) \
+        == ops.W4A16_ERR_INVALID_ARG
+
+
+def test_grouped_and_align_argument_checks(lib):
+    fake = ctypes.c_void_p(1 << 20)
+    plan = ops.w4a16_plan(32, 1, 1, 256, 256, 32.0)
+    assert lib.w4a16_moe_grouped_gemm(5, fake, 4, 256, 256, fake, 128, fake, 16, fake, 0,
+                                      ctypes.byref(plan), fake, 256, None) == ops.W4A16_ERR_INVALID_ARG
+    bad = ops.Plan.from_buffer_copy(plan)
+    bad.block_m = 48   # does not divide the 128-row expert alignment
+    assert lib.w4a16_moe_grouped_gemm(0, fake, 4, 256, 256, fake, 144, fake, 16, fake, 0,
+                                      ctypes.byref(bad), fake, 256, None) == ops.W4A16_ERR_INVALID_ARG
+    # align: capacity too small, not a multiple of block_m, too many experts
+    assert lib.w4a16_moe_align_block_size(fake, 64, 2, 8, 16, 64, fake, fake, fake, None) \
+        == ops.W4A16_ERR_INVALID_ARG
+    assert lib.w4a16_moe_align_block_size(fake, 64, 2, 8, 16, 250, fake, fake, fake, None) \
+        == ops.W4A16_ERR_INVALID_ARG
+    assert lib.w4a16_moe_align_block_size(fake, 64, 2, 2000, 16, 1 << 16, fake, fake, fake, None) \
+        == ops.W4A16_ERR_UNSUPPORTED
+    assert lib.w4a16_silu_and_mul(fake, 4, 12, fake, None) == ops.W4A16_ERR_INVALID_ARG
+
+
+def test_product_path_has_no_cpu_fallback():
+    # The package never imports the oracle; a missing library is an error.
+    import w4a16_int4_moe_gb300 as pkg
+    root = os.path.dirname(pkg.__file__)
+    for dirpath, _, files in os.walk(root):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f), encoding="utf-8").read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+    saved = ops._lib
+    ops._lib = None
+    try:
+        with pytest.raises(RuntimeError):
+            ops.load_library("/nonexistent/libw4a16moe.so")
+    finally:
+        ops._lib = saved

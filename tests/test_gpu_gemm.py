@@ -1,0 +1,341 @@
+"""Parity of the tcgen05 W4A16 MoE GEMMs with the float64 oracle.
+
+Every comparison goes through the C ABI (ctypes binding). Stages are compared
+one at a time: the GPU's down pass is checked on the GPU's own BF16
+activation fed to the oracle, so errors do not compound across stages.
+Small shapes are compared element by element over every routed row; the
+full-size shard shapes are compared on sampled output columns (the oracle
+evaluates the plain definition only there) or sampled rows.
+"""
+
+import functools
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from w4a16_int4_moe_gb300 import moe as moe_mod
+from w4a16_int4_moe_gb300 import ops
+from w4a16_int4_moe_gb300 import workloads as wl
+from helpers import assert_close, bf16_bits, bf16_tensor, dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _pack(q, s, device):
+    return ops.w4a16_prepack(dev(q, device), dev(s.view(np.int16), device))
+
+
+def _routing(ids, experts, bm, device):
+    t = dev(ids, device)
+    cap = ops.w4a16_align_capacity(t.numel(), experts, bm)
+    return ops.w4a16_moe_align_block_size(t, experts, bm, cap)
+
+
+def _plan(bm, n, k, stages=None, b_stages=None, grid=0):
+    p = ops.w4a16_plan(64, 1, 1, n, k, float(bm))
+    p.block_m = bm
+    p.b_stages = b_stages or (8 if bm <= 32 else (6 if bm <= 64 else 4))
+    p.stages = stages or min(p.stages, 8)
+    p.grid = grid
+    return p
+
+
+def _gate_up(p, packed, routing, plan, device):
+    sid, eid, ntp = routing
+    ws = ops.new_workspace(plan, device)
+    x = bf16_tensor(p.x, device)
+    out = torch.full((p.numel, 2 * p.inter), float("nan"), dtype=torch.bfloat16, device=device)
+    ops.w4a16_moe_indexed_gemm(ops.W4A16_GATE_UP, packed, p.num_experts, 2 * p.inter, p.hidden,
+                               x, p.tokens, p.topk, sid, eid, ntp, plan, ws, out=out)
+    st, word = ops.w4a16_read_device_status(ws)
+    assert st == ops.W4A16_OK, hex(word)
+    return out
+
+
+def _down(p, packed, routing, plan, act_bits, device):
+    sid, eid, ntp = routing
+    ws = ops.new_workspace(plan, device)
+    a = bf16_tensor(act_bits, device)
+    w = dev(p.topk_weights, device)
+    out = torch.full((p.tokens, p.hidden), float("nan"), dtype=torch.float32, device=device)
+    ops.w4a16_moe_indexed_gemm(ops.W4A16_DOWN, packed, p.num_experts, p.hidden, p.inter, a,
+                               p.tokens, p.topk, sid, eid, ntp, plan, ws, topk_weights=w, out=out)
+    st, word = ops.w4a16_read_device_status(ws)
+    assert st == ops.W4A16_OK, hex(word)
+    return out
+
+
+def _routed(p):
+    flat = p.topk_ids.reshape(-1)
+    return (flat >= 0) & (flat < p.num_experts)
+
+
+def _check_pair(p, device, bm, cols_gu=None, cols_dn=None, what=""):
+    """gate_up vs oracle, then down (on the GPU's activation) vs oracle."""
+    pk_gu = _pack(p.q_gu, p.s_gu, device)
+    pk_dn = _pack(p.q_dn, p.s_dn, device)
+    routing = _routing(p.topk_ids, p.num_experts, bm, device)
+    g = _gate_up(p, pk_gu, routing, _plan(bm, 2 * p.inter, p.hidden), device)
+    g_bits = bf16_bits(g)
+    routed = _routed(p)
+    g_ref = oracle.indexed_gate_up(p.x, p.topk_ids, p.q_gu, p.s_gu, cols=cols_gu)
+    g_got = oracle.bf16_bits_to_f64(g_bits)
+    if cols_gu is not None:
+        g_got = g_got[:, cols_gu]
+    e1 = assert_close(g_got[routed], g_ref[routed], f"{what} gate_up")
+    # activation (untimed glue) on the GPU's own gate_up output
+    act = ops.w4a16_silu_and_mul(g)
+    a_bits = bf16_bits(act)
+    a_ref = oracle.bf16_bits_to_f64(oracle.silu_and_mul(g_bits[routed]))
+    assert_close(oracle.bf16_bits_to_f64(a_bits[routed]), a_ref, f"{what} silu_and_mul",
+                 rel_l2=4e-3, max_abs_frac=1e-2)
+    a_bits_clean = a_bits.copy()
+    a_bits_clean[~routed] = 0
+    y = _down(p, pk_dn, routing, _plan(bm, p.hidden, p.inter), a_bits_clean, device)
+    y_ref = oracle.indexed_down(a_bits_clean, p.topk_ids, p.topk_weights, p.q_dn, p.s_dn,
+                                cols=cols_dn)
+    y_got = y.cpu().numpy()
+    if cols_dn is not None:
+        y_got = y_got[:, cols_dn]
+    e2 = assert_close(y_got, y_ref, f"{what} down")
+    print(f"{what}: gate_up rel-L2 {e1[0]:.2e} max-abs {e1[1]:.2e}; "
+          f"down rel-L2 {e2[0]:.2e} max-abs {e2[1]:.2e}")
+    return g_bits
+
+
+# ------------------------------------------------------------ small shapes --
+
+@pytest.mark.parametrize("bm", [16, 32, 64, 128, 256])
+def test_tiny_all_block_sizes(cuda_dev, bm):
+    _check_pair(wl.tiny(), cuda_dev, bm, what=f"tiny bm={bm}")
+
+
+@pytest.mark.parametrize("tokens,hidden,inter,experts,topk,bm", [
+    (37, 96, 96, 5, 3, 16),      # k = 32 mod 64 on both GEMMs, ragged n (192 / 96 rows)
+    (200, 320, 224, 6, 2, 64),   # ragged n tiles (448 / 320 rows), k = 32 mod 64 on down
+    (5, 64, 32, 40, 4, 16),      # far more experts than rows: many empty experts
+    (130, 256, 160, 3, 1, 128),  # top-1, rows above one block per expert
+])
+def test_ragged_shapes(cuda_dev, tokens, hidden, inter, experts, topk, bm):
+    p = wl.uniform_problem(tokens, hidden, inter, experts, topk, seed=tokens)
+    _check_pair(p, cuda_dev, bm, what=f"ragged {tokens}x{hidden}x{inter}")
+
+
+def test_nonlocal_and_degenerate_routing(cuda_dev):
+    p = wl.uniform_problem(48, 128, 64, 6, 2, seed=21)
+    p.topk_ids[::3, 0] = -1          # non-local experts
+    p.topk_ids[1::5, 1] = 9          # ids >= E are not local either
+    _check_pair(p, cuda_dev, 16, what="non-local")
+
+
+def test_all_zero_point_weights_give_zero(cuda_dev):
+    p = wl.tiny(seed=4)
+    p.q_gu[:] = 0x88
+    pk = _pack(p.q_gu, p.s_gu, cuda_dev)
+    routing = _routing(p.topk_ids, p.num_experts, 32, cuda_dev)
+    g = _gate_up(p, pk, routing, _plan(32, 2 * p.inter, p.hidden), cuda_dev)
+    routed = _routed(p)
+    assert torch.all(g[torch.from_numpy(routed).to(cuda_dev)] == 0)
+
+
+def test_no_routed_rows_leaves_output_untouched(cuda_dev):
+    p = wl.tiny(seed=5)
+    p.topk_ids[:] = -1
+    pk = _pack(p.q_gu, p.s_gu, cuda_dev)
+    routing = _routing(p.topk_ids, p.num_experts, 16, cuda_dev)
+    g = _gate_up(p, pk, routing, _plan(16, 2 * p.inter, p.hidden), cuda_dev)
+    assert torch.all(torch.isnan(g))
+
+
+def test_schedules_are_bitwise_identical(cuda_dev):
+    # Pipelining and scheduling choices do not change any gate_up output bit
+    # (every row's K reduction runs in the same order): block size, ring
+    # depths and grid size.
+    p = wl.uniform_problem(96, 512, 256, 8, 2, seed=8)
+    pk = _pack(p.q_gu, p.s_gu, cuda_dev)
+    ref = None
+    for bm, st, bst, grid in [(16, 8, 8, 0), (32, 4, 4, 0), (64, 16, 6, 3), (128, 2, 4, 1),
+                              (256, 6, 4, 0), (48, 5, 10, 7)]:
+        routing = _routing(p.topk_ids, p.num_experts, bm, cuda_dev)
+        g = _gate_up(p, pk, routing, _plan(bm, 2 * p.inter, p.hidden, st, bst, grid), cuda_dev)
+        bits = bf16_bits(g)[_routed(p)]
+        if ref is None:
+            ref = bits
+        else:
+            np.testing.assert_array_equal(bits, ref, err_msg=f"bm={bm} stages={st}")
+
+
+def test_over_allocated_routing_and_validation(cuda_dev):
+    p = wl.tiny(seed=6)
+    pk = _pack(p.q_gu, p.s_gu, cuda_dev)
+    t = dev(p.topk_ids, cuda_dev)
+    cap = ops.w4a16_align_capacity(t.numel(), 8, 32) + 32 * 8   # extra unused blocks
+    sid, eid, ntp = ops.w4a16_moe_align_block_size(t, 8, 32, cap)
+    plan = _plan(32, 2 * p.inter, p.hidden)
+    ws = ops.new_workspace(plan, cuda_dev)
+    out = torch.empty((p.numel, 2 * p.inter), dtype=torch.bfloat16, device=cuda_dev)
+    ops.w4a16_moe_indexed_gemm(ops.W4A16_GATE_UP, pk, 8, 2 * p.inter, p.hidden,
+                               bf16_tensor(p.x, cuda_dev), p.tokens, p.topk, sid, eid, ntp, plan,
+                               ws, out=out, flags=ops.W4A16_FLAG_VALIDATE_ROUTING)
+    g_ref = oracle.indexed_gate_up(p.x, p.topk_ids, p.q_gu, p.s_gu)
+    assert_close(oracle.bf16_bits_to_f64(bf16_bits(out)), g_ref, "over-allocated")
+    # corrupt routing is refused when validation is on
+    eid[0] = 99
+    with pytest.raises(ops.W4A16Error) as ei:
+        ops.w4a16_moe_indexed_gemm(ops.W4A16_GATE_UP, pk, 8, 2 * p.inter, p.hidden,
+                                   bf16_tensor(p.x, cuda_dev), p.tokens, p.topk, sid, eid, ntp,
+                                   plan, ws, out=out, flags=ops.W4A16_FLAG_VALIDATE_ROUTING)
+    assert ei.value.status == ops.W4A16_ERR_ROUTING
+    # ... and is ignored (never dereferenced) when validation is off
+    ops.w4a16_moe_indexed_gemm(ops.W4A16_GATE_UP, pk, 8, 2 * p.inter, p.hidden,
+                               bf16_tensor(p.x, cuda_dev), p.tokens, p.topk, sid, eid, ntp, plan,
+                               ws, out=out)
+    assert ops.w4a16_read_device_status(ws)[0] == ops.W4A16_OK
+
+
+def test_down_accumulate_flag(cuda_dev):
+    p = wl.tiny(seed=7)
+    pk = _pack(p.q_dn, p.s_dn, cuda_dev)
+    routing = _routing(p.topk_ids, 8, 32, cuda_dev)
+    plan = _plan(32, p.hidden, p.inter)
+    rng = np.random.default_rng(1)
+    a_bits = wl.random_activations(rng, p.numel, p.inter)
+    y = _down(p, pk, routing, plan, a_bits, cuda_dev)
+    ws = ops.new_workspace(plan, cuda_dev)
+    sid, eid, ntp = routing
+    y2 = y.clone()
+    ops.w4a16_moe_indexed_gemm(ops.W4A16_DOWN, pk, 8, p.hidden, p.inter,
+                               bf16_tensor(a_bits, cuda_dev), p.tokens, p.topk, sid, eid, ntp,
+                               plan, ws, topk_weights=dev(p.topk_weights, cuda_dev), out=y2,
+                               flags=ops.W4A16_FLAG_ACCUMULATE)
+    assert_close(y2.cpu().numpy(), 2.0 * y.cpu().numpy(), "accumulate", rel_l2=1e-6,
+                 max_abs_frac=1e-6)
+
+
+def test_layer_forward_and_graph_capture(cuda_dev):
+    p = wl.tiny(seed=9)
+    gu = moe_mod.PackedExperts.from_checkpoint(dev(p.q_gu, cuda_dev),
+                                               dev(p.s_gu.view(np.int16), cuda_dev))
+    dn = moe_mod.PackedExperts.from_checkpoint(dev(p.q_dn, cuda_dev),
+                                               dev(p.s_dn.view(np.int16), cuda_dev))
+    layer = moe_mod.W4A16MoE(gu, dn, p.topk, p.tokens)
+    x = bf16_tensor(p.x, cuda_dev)
+    ids = dev(p.topk_ids, cuda_dev)
+    w = dev(p.topk_weights, cuda_dev)
+    y = layer.forward(x, ids, w)
+    torch.cuda.synchronize()
+    g, g_bits, a_bits, y_ref = oracle.moe_layer(p.x, p.topk_ids, p.topk_weights, p.q_gu, p.s_gu,
+                                                p.q_dn, p.s_dn)
+    assert_close(y.cpu().numpy(), y_ref, "layer forward")
+    # the whole pair captured in one CUDA graph (routing validation off)
+    s = torch.cuda.Stream()
+    out = torch.zeros_like(y)
+    with torch.cuda.stream(s):
+        layer.forward(x, ids, w, out=out)
+    torch.cuda.synchronize()
+    out.fill_(float("nan"))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        layer.forward(x, ids, w, out=out)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert_close(out.cpu().numpy(), y_ref, "graph replay")
+
+
+# ---------------------------------------------------------- grouped GEMMs --
+
+def _grouped(gp, device, plan=None):
+    pk = _pack(gp.q, gp.s, device)
+    ws = ops.new_workspace(plan or ops.w4a16_plan(16, 1, 1, gp.n, gp.k, 16.0), device)
+    a = bf16_tensor(gp.a, device)
+    lay = dev(gp.layout, device)
+    kind = ops.W4A16_GROUPED_CONTIGUOUS if gp.kind == "contiguous" else ops.W4A16_GROUPED_MASKED
+    m = gp.a.shape[0] if gp.kind == "contiguous" else gp.a.shape[1]
+    out = ops.w4a16_moe_grouped_gemm(kind, pk, gp.num_experts, gp.n, gp.k, a, m, lay, ws,
+                                     plan=plan, expected_m=gp.expected_m)
+    st, word = ops.w4a16_read_device_status(ws)
+    assert st == ops.W4A16_OK, hex(word)
+    return oracle.bf16_bits_to_f64(bf16_bits(out))
+
+
+@pytest.mark.parametrize("bm", [32, 64, 128])
+def test_grouped_contiguous_small(cuda_dev, bm):
+    gp = wl.grouped_contiguous_problem([5, 128, 0, 77], num_experts=4, n=200, k=96, seed=bm)
+    got = _grouped(gp, cuda_dev, _plan(bm, gp.n, gp.k))
+    ref = oracle.grouped_contiguous(gp.a, gp.layout, gp.q, gp.s)
+    valid = gp.layout >= 0
+    assert_close(got[valid], ref[valid], f"contiguous bm={bm}")
+
+
+@pytest.mark.parametrize("bm", [16, 32])
+def test_grouped_masked_small(cuda_dev, bm):
+    gp = wl.grouped_masked_problem(num_experts=6, max_m=32, n=256, k=160, seed=bm)
+    gp.layout[2] = 0      # an expert with no rows
+    gp.layout[3] = 32     # a full budget
+    got = _grouped(gp, cuda_dev, _plan(bm, gp.n, gp.k))
+    ref = oracle.grouped_masked(gp.a, gp.layout, gp.q, gp.s)
+    valid = ~np.isnan(ref[..., 0])
+    assert_close(got[valid], ref[valid], f"masked bm={bm}")
+
+
+# ------------------------------------------------- full-size shard shapes --
+
+@functools.lru_cache(maxsize=1)
+def _ep8_decode():
+    return wl.ep8_decode()
+
+
+def _sample_cols(n, count, seed):
+    rng = np.random.default_rng(seed)
+    return np.sort(rng.choice(n, size=min(n, count), replace=False))
+
+
+@pytest.mark.slow
+def test_ep8_decode_full_size(cuda_dev):
+    p = _ep8_decode()
+    plan_bm = ops.w4a16_plan(p.tokens, p.topk, p.num_experts, 2 * p.inter, p.hidden,
+                             p.tok_e_hint()).block_m
+    _check_pair(p, cuda_dev, plan_bm, cols_gu=_sample_cols(4096, 384, 1),
+                cols_dn=_sample_cols(7168, 384, 2), what="EP8 decode")
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("tokens", [16, 64, 256])
+def test_tp8_full_size(cuda_dev, tokens):
+    p = wl.tp8(tokens)
+    bm = ops.w4a16_plan(p.tokens, p.topk, p.num_experts, 2 * p.inter, p.hidden).block_m
+    _check_pair(p, cuda_dev, bm, cols_gu=_sample_cols(512, 128, 3),
+                cols_dn=_sample_cols(7168, 256, 4), what=f"TP8 T={tokens}")
+
+
+@pytest.mark.slow
+def test_ep8_prefill_full_size(cuda_dev):
+    p = wl.ep8_prefill()
+    bm = ops.w4a16_plan(p.tokens, p.topk, p.num_experts, 2 * p.inter, p.hidden,
+                        p.tok_e_hint()).block_m
+    _check_pair(p, cuda_dev, bm, cols_gu=_sample_cols(4096, 128, 5),
+                cols_dn=_sample_cols(7168, 128, 6), what="EP8 prefill")
+
+
+@pytest.mark.slow
+def test_grouped_masked_full_size(cuda_dev):
+    gp = wl.grouped_masked_problem()
+    got = _grouped(gp, cuda_dev)
+    cols = _sample_cols(gp.n, 256, 7)
+    ref = oracle.grouped_masked(gp.a, gp.layout, gp.q, gp.s, cols=cols)
+    valid = ~np.isnan(ref[..., 0])
+    assert_close(got[..., cols][valid], ref[valid], "masked full size")
+
+
+@pytest.mark.slow
+def test_grouped_contiguous_full_size_ragged(cuda_dev):
+    rng = np.random.default_rng(11)
+    gp = wl.grouped_contiguous_problem(rng.integers(128, 1025, size=48), seed=11)
+    got = _grouped(gp, cuda_dev, _plan(128, gp.n, gp.k))
+    rows = np.sort(rng.choice(gp.a.shape[0], size=384, replace=False))
+    cols = _sample_cols(gp.n, 128, 12)
+    ref = oracle.grouped_contiguous(gp.a[rows], gp.layout[rows], gp.q, gp.s, cols=cols)
+    valid = gp.layout[rows] >= 0
+    assert_close(got[rows][:, cols][valid], ref[valid], "contiguous full size")

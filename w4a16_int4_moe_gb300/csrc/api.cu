@@ -1,0 +1,400 @@
+// api.cu -- the extern "C" entry points declared in include/w4a16moe.h:
+// host-side argument checks, the tok_e scheduler, and the launches.
+
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <vector>
+
+#include "internal.h"
+
+using namespace w4a16;
+
+namespace {
+
+constexpr int kMaxDynSmem = 232448;  // 227 KB per CTA on sm_103a
+constexpr long long kDefaultTimeoutCycles = 2000000000LL;  // about a second
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+w4a16_status cuda_status(cudaError_t e) { return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA; }
+
+long long wait_timeout_cycles() {
+  const char* s = std::getenv("W4A16_WAIT_TIMEOUT_CYCLES");
+  if (s != nullptr) {
+    const long long v = std::atoll(s);
+    if (v > 0) return v;
+  }
+  return kDefaultTimeoutCycles;
+}
+
+int round_up(int x, int m) { return (x + m - 1) / m * m; }
+
+// Shared-memory-driven pipeline depths for a block_m; stages as given when
+// the plan sets them.
+bool plan_pipeline(const w4a16_plan_t& p, int* w_stages, int* b_stages, size_t* smem) {
+  if (p.block_m < 16 || p.block_m > 256 || p.block_m % 16 != 0) return false;
+  if (p.bn != kTileRows || p.bk != kKStep || p.split_k != 1 || p.layout != W4A16_LAYOUT_KTILE64)
+    return false;
+  if (p.stages < 2 || p.stages > 16 || p.b_stages < 4 || p.b_stages > 16 || p.b_stages % 2 != 0)
+    return false;
+  const size_t bytes = gemm_smem_bytes(p.block_m, p.stages, p.b_stages);
+  if (bytes > static_cast<size_t>(kMaxDynSmem)) return false;
+  *w_stages = p.stages;
+  *b_stages = p.b_stages;
+  *smem = bytes;
+  return true;
+}
+
+int current_sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  return device_sm_count(dev);
+}
+
+void fill_tmem_slots(int block_m, GemmArgs* a) {
+  const int dcols = round_up(block_m, 32);
+  a->d_cols = dcols;
+  a->d_slots = (128 + 2 * dcols <= 512) ? 2 : 1;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* w4a16_status_string(int status) {
+  switch (status) {
+    case W4A16_OK: return "ok";
+    case W4A16_ERR_INVALID_ARG: return "invalid argument";
+    case W4A16_ERR_UNSUPPORTED: return "unsupported quantisation scheme or shape";
+    case W4A16_ERR_ROUTING: return "routing tensors failed validation";
+    case W4A16_ERR_WORKSPACE: return "workspace missing or too small";
+    case W4A16_ERR_CUDA: return "CUDA error";
+    case W4A16_ERR_TIMEOUT: return "a device-side wait gave up";
+    default: return "unknown status";
+  }
+}
+
+int w4a16_version(void) { return 100; }
+
+w4a16_status w4a16_plan(int tokens, int topk, int num_experts, int n, int k, float tok_e_hint,
+                        w4a16_plan_t* out) {
+  if (out == nullptr || tokens < 0 || topk <= 0 || num_experts <= 0 || n <= 0 || k <= 0)
+    return W4A16_ERR_INVALID_ARG;
+  double tok_e = tok_e_hint > 0.f ? static_cast<double>(tok_e_hint)
+                                  : static_cast<double>(tokens) * topk / num_experts;
+  // tok_e decides the schedule (page "vLLM 宣布 Humming 后端可运行 … Chord 内核 …",
+  // section "调度由每个专家收到的 token 数决定"; switch near 80 rows/expert).
+  // Below the switch the block holds the expected rows of an expert with
+  // headroom for the spread, so each weight tile streams once per expert;
+  // above it the block is sized by padded expert rows. The MMA N of a block
+  // is its real row count rounded to 16, so padding costs no tensor time.
+  int block_m;
+  if (tok_e <= 80.0) {
+    block_m = round_up(std::max(16, static_cast<int>(std::ceil(1.5 * tok_e))), 16);
+    block_m = std::min(block_m, 128);
+  } else {
+    block_m = tok_e <= 192.0 ? 128 : 256;
+  }
+  w4a16_plan_t p;
+  std::memset(&p, 0, sizeof(p));
+  p.block_m = block_m;
+  p.bn = kTileRows;
+  p.bk = kKStep;
+  p.b_stages = block_m <= 32 ? 8 : (block_m <= 64 ? 6 : 4);
+  // weight ring: as deep as shared memory allows (up to 16 stages of 9 KB)
+  int ws = 16;
+  while (ws > 2 && gemm_smem_bytes(block_m, ws, p.b_stages) > static_cast<size_t>(kMaxDynSmem))
+    --ws;
+  p.stages = ws;
+  p.split_k = 1;
+  p.ctas_per_sm = 1;
+  p.swap_ab = 1;
+  p.layout = W4A16_LAYOUT_KTILE64;
+  p.grid = 0;
+  *out = p;
+  return W4A16_OK;
+}
+
+size_t w4a16_align_capacity(int numel, int num_experts, int block_m) {
+  if (numel < 0 || num_experts <= 0 || block_m <= 0) return 0;
+  const long long pad = static_cast<long long>(std::min(num_experts, numel)) * (block_m - 1);
+  const long long cap = (static_cast<long long>(numel) + pad + block_m - 1) / block_m * block_m;
+  return static_cast<size_t>(cap);
+}
+
+w4a16_status w4a16_moe_align_block_size(const int32_t* topk_ids, int tokens, int topk,
+                                        int num_experts, int block_m, int capacity,
+                                        int32_t* sorted_ids, int32_t* expert_ids,
+                                        int32_t* num_tokens_padded, void* stream) {
+  if (tokens < 0 || topk <= 0 || num_experts <= 0 || block_m <= 0 || capacity < 0)
+    return W4A16_ERR_INVALID_ARG;
+  if (sorted_ids == nullptr || expert_ids == nullptr || num_tokens_padded == nullptr)
+    return W4A16_ERR_INVALID_ARG;
+  const long long numel = static_cast<long long>(tokens) * topk;
+  if (numel > 0 && topk_ids == nullptr) return W4A16_ERR_INVALID_ARG;
+  if (numel >= (1LL << 30)) return W4A16_ERR_UNSUPPORTED;
+  if (num_experts > 1024 || block_m > 1024) return W4A16_ERR_UNSUPPORTED;
+  if (capacity % block_m != 0) return W4A16_ERR_INVALID_ARG;
+  if (static_cast<size_t>(capacity) <
+      w4a16_align_capacity(static_cast<int>(numel), num_experts, block_m))
+    return W4A16_ERR_INVALID_ARG;
+  return cuda_status(launch_align(topk_ids, static_cast<int>(numel), num_experts, block_m,
+                                  capacity, sorted_ids, expert_ids, num_tokens_padded,
+                                  static_cast<cudaStream_t>(stream)));
+}
+
+w4a16_status w4a16_prepack_size(int num_experts, int n, int k, int group, int layout,
+                                size_t* bytes) {
+  if (bytes == nullptr || num_experts <= 0 || n <= 0 || k <= 0) return W4A16_ERR_INVALID_ARG;
+  if (group != kGroup || k % kGroup != 0 || layout != W4A16_LAYOUT_KTILE64)
+    return W4A16_ERR_UNSUPPORTED;
+  *bytes = static_cast<size_t>(num_experts) * packed_expert_bytes(n, k);
+  return W4A16_OK;
+}
+
+w4a16_status w4a16_prepack(const uint8_t* q, const uint16_t* scales, int num_experts, int n,
+                           int k, int group, int layout, void* packed, size_t packed_bytes,
+                           void* stream) {
+  size_t need = 0;
+  const w4a16_status st = w4a16_prepack_size(num_experts, n, k, group, layout, &need);
+  if (st != W4A16_OK) return st;
+  if (q == nullptr || scales == nullptr || packed == nullptr) return W4A16_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(packed) || (reinterpret_cast<uintptr_t>(scales) & 1u))
+    return W4A16_ERR_INVALID_ARG;
+  if (packed_bytes < need) return W4A16_ERR_INVALID_ARG;
+  return cuda_status(launch_prepack(q, scales, num_experts, n, k, static_cast<uint8_t*>(packed),
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+w4a16_status w4a16_unpack(const void* packed, int num_experts, int n, int k, uint8_t* q,
+                          uint16_t* scales, void* stream) {
+  if (packed == nullptr || q == nullptr || scales == nullptr || num_experts <= 0 || n <= 0 ||
+      k <= 0)
+    return W4A16_ERR_INVALID_ARG;
+  if (k % kGroup != 0) return W4A16_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(packed) || (reinterpret_cast<uintptr_t>(scales) & 1u))
+    return W4A16_ERR_INVALID_ARG;
+  return cuda_status(launch_unpack(static_cast<const uint8_t*>(packed), num_experts, n, k, q,
+                                   scales, static_cast<cudaStream_t>(stream)));
+}
+
+size_t w4a16_workspace_size(const w4a16_plan_t* plan, int rows, int n) {
+  (void)plan;
+  (void)rows;
+  (void)n;
+  return kStatusBytes;
+}
+
+w4a16_status w4a16_moe_indexed_gemm(int mode, const void* packed, int num_experts, int n, int k,
+                                    const uint16_t* a, int tokens, int topk,
+                                    const int32_t* sorted_ids, const int32_t* expert_ids,
+                                    const int32_t* num_tokens_padded, int capacity,
+                                    const float* topk_weights, void* out, int flags,
+                                    const w4a16_plan_t* plan, void* workspace, size_t ws_bytes,
+                                    void* stream) {
+  if (mode != W4A16_GATE_UP && mode != W4A16_DOWN) return W4A16_ERR_INVALID_ARG;
+  if (num_experts <= 0 || n <= 0 || k <= 0 || tokens < 0 || topk <= 0 || capacity < 0)
+    return W4A16_ERR_INVALID_ARG;
+  if (k % kGroup != 0) return W4A16_ERR_UNSUPPORTED;
+  if (plan == nullptr || packed == nullptr || out == nullptr || sorted_ids == nullptr ||
+      expert_ids == nullptr || num_tokens_padded == nullptr)
+    return W4A16_ERR_INVALID_ARG;
+  if (tokens > 0 && a == nullptr) return W4A16_ERR_INVALID_ARG;
+  if (mode == W4A16_DOWN && tokens > 0 && topk_weights == nullptr) return W4A16_ERR_INVALID_ARG;
+  if ((flags & ~(W4A16_FLAG_VALIDATE_ROUTING | W4A16_FLAG_ACCUMULATE)) != 0)
+    return W4A16_ERR_INVALID_ARG;
+  if (!aligned16(packed) || !aligned16(out) || (a != nullptr && !aligned16(a)))
+    return W4A16_ERR_INVALID_ARG;
+  if (workspace == nullptr || ws_bytes < w4a16_workspace_size(plan, tokens * topk, n))
+    return W4A16_ERR_WORKSPACE;
+  int w_stages = 0, b_stages = 0;
+  size_t smem = 0;
+  if (!plan_pipeline(*plan, &w_stages, &b_stages, &smem)) return W4A16_ERR_INVALID_ARG;
+  const int bm = plan->block_m;
+  if (capacity % bm != 0) return W4A16_ERR_INVALID_ARG;
+  const long long numel = static_cast<long long>(tokens) * topk;
+  if (numel >= (1LL << 30)) return W4A16_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  if (flags & W4A16_FLAG_VALIDATE_ROUTING) {
+    // Trusted-routing validation off keeps the call capturable; on, the
+    // routing is copied back and checked here.
+    if (cudaStreamSynchronize(s) != cudaSuccess) return W4A16_ERR_CUDA;
+    int ntp = 0;
+    if (cudaMemcpy(&ntp, num_tokens_padded, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+      return W4A16_ERR_CUDA;
+    if (ntp < 0 || ntp > capacity || ntp % bm != 0) return W4A16_ERR_ROUTING;
+    std::vector<int32_t> eid(ntp / bm), sid(ntp);
+    if (ntp > 0) {
+      if (cudaMemcpy(eid.data(), expert_ids, eid.size() * 4, cudaMemcpyDeviceToHost) !=
+              cudaSuccess ||
+          cudaMemcpy(sid.data(), sorted_ids, sid.size() * 4, cudaMemcpyDeviceToHost) !=
+              cudaSuccess)
+        return W4A16_ERR_CUDA;
+    }
+    for (size_t b = 0; b < eid.size(); ++b) {
+      if (eid[b] < -1 || eid[b] >= num_experts) return W4A16_ERR_ROUTING;
+      for (int j = 0; j < bm; ++j) {
+        const int id = sid[b * bm + j];
+        if (id < 0 || id > numel) return W4A16_ERR_ROUTING;
+      }
+    }
+  }
+
+  if (mode == W4A16_DOWN && !(flags & W4A16_FLAG_ACCUMULATE) && tokens > 0) {
+    const cudaError_t e =
+        cudaMemsetAsync(out, 0, static_cast<size_t>(tokens) * n * sizeof(float), s);
+    if (e != cudaSuccess) return W4A16_ERR_CUDA;
+  }
+  if (numel == 0 || capacity == 0) return W4A16_OK;
+
+  GemmArgs g;
+  std::memset(&g, 0, sizeof(g));
+  g.wpack = static_cast<const uint8_t*>(packed);
+  g.expert_bytes = static_cast<long long>(packed_expert_bytes(n, k));
+  g.num_experts = num_experts;
+  g.n = n;
+  g.k = k;
+  g.n_tiles = packed_tiles(n);
+  g.k_steps = packed_ksteps(k);
+  g.act = a;
+  g.family = kIndexed;
+  g.out_mode = mode == W4A16_DOWN ? kOutF32WeightedAdd : kOutBf16;
+  g.sorted_ids = sorted_ids;
+  g.expert_ids = expert_ids;
+  g.num_tokens_padded = num_tokens_padded;
+  g.capacity = capacity;
+  g.numel = static_cast<int>(numel);
+  g.a_div = mode == W4A16_DOWN ? 1 : topk;
+  g.o_div = mode == W4A16_DOWN ? topk : 1;
+  g.topk_weights = topk_weights;
+  g.block_m = bm;
+  g.out = out;
+  g.status = static_cast<int*>(workspace);
+  g.w_stages = w_stages;
+  g.b_stages = b_stages;
+  fill_tmem_slots(bm, &g);
+  g.timeout_cycles = wait_timeout_cycles();
+  const int sms = current_sm_count();
+  if (sms <= 0) return W4A16_ERR_CUDA;
+  long long grid = plan->grid > 0 ? plan->grid : static_cast<long long>(sms) * plan->ctas_per_sm;
+  const long long max_items = static_cast<long long>(capacity / bm) * g.n_tiles;
+  grid = std::max<long long>(1, std::min(grid, max_items));
+  (void)smem;
+  return cuda_status(launch_moe_gemm(g, static_cast<int>(grid), s));
+}
+
+w4a16_status w4a16_moe_grouped_gemm(int kind, const void* packed, int num_experts, int n, int k,
+                                    const uint16_t* a, int m, const int32_t* layout,
+                                    int expected_m, uint16_t* out, int flags,
+                                    const w4a16_plan_t* plan, void* workspace, size_t ws_bytes,
+                                    void* stream) {
+  if (kind != W4A16_GROUPED_CONTIGUOUS && kind != W4A16_GROUPED_MASKED)
+    return W4A16_ERR_INVALID_ARG;
+  if (num_experts <= 0 || n <= 0 || k <= 0 || m < 0) return W4A16_ERR_INVALID_ARG;
+  if (k % kGroup != 0) return W4A16_ERR_UNSUPPORTED;
+  if (packed == nullptr || out == nullptr || layout == nullptr) return W4A16_ERR_INVALID_ARG;
+  if (m > 0 && a == nullptr) return W4A16_ERR_INVALID_ARG;
+  if ((flags & ~W4A16_FLAG_VALIDATE_ROUTING) != 0) return W4A16_ERR_INVALID_ARG;
+  if (!aligned16(packed) || !aligned16(out) || (a != nullptr && !aligned16(a)))
+    return W4A16_ERR_INVALID_ARG;
+  w4a16_plan_t local;
+  if (plan == nullptr) {
+    const int rows = expected_m > 0 ? expected_m : std::max(1, m);
+    w4a16_plan(rows, 1, 1, n, k, static_cast<float>(rows), &local);
+    if (kind == W4A16_GROUPED_CONTIGUOUS) local.block_m = std::min(local.block_m, 128);
+    plan = &local;
+  }
+  if (workspace == nullptr || ws_bytes < w4a16_workspace_size(plan, m, n))
+    return W4A16_ERR_WORKSPACE;
+  int w_stages = 0, b_stages = 0;
+  size_t smem = 0;
+  if (!plan_pipeline(*plan, &w_stages, &b_stages, &smem)) return W4A16_ERR_INVALID_ARG;
+  const int bm = plan->block_m;
+  const long long rows_total =
+      kind == W4A16_GROUPED_MASKED ? static_cast<long long>(num_experts) * m : m;
+  if (rows_total >= (1LL << 30)) return W4A16_ERR_UNSUPPORTED;
+  if (kind == W4A16_GROUPED_CONTIGUOUS && (128 % bm != 0 || m % bm != 0))
+    return W4A16_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  if (flags & W4A16_FLAG_VALIDATE_ROUTING) {
+    if (cudaStreamSynchronize(s) != cudaSuccess) return W4A16_ERR_CUDA;
+    const int cnt = kind == W4A16_GROUPED_CONTIGUOUS ? m : num_experts;
+    std::vector<int32_t> lay(cnt);
+    if (cnt > 0 &&
+        cudaMemcpy(lay.data(), layout, cnt * 4, cudaMemcpyDeviceToHost) != cudaSuccess)
+      return W4A16_ERR_CUDA;
+    if (kind == W4A16_GROUPED_CONTIGUOUS) {
+      for (int b0 = 0; b0 < m; b0 += 128) {
+        const int head = lay[b0];
+        for (int r = b0; r < std::min(m, b0 + 128); ++r) {
+          if (lay[r] < -1 || lay[r] >= num_experts) return W4A16_ERR_ROUTING;
+          if (lay[r] >= 0 && lay[r] != head) return W4A16_ERR_ROUTING;
+        }
+      }
+    } else {
+      for (int e = 0; e < num_experts; ++e)
+        if (lay[e] < 0 || lay[e] > m) return W4A16_ERR_ROUTING;
+    }
+  }
+  if (rows_total == 0) return W4A16_OK;
+
+  GemmArgs g;
+  std::memset(&g, 0, sizeof(g));
+  g.wpack = static_cast<const uint8_t*>(packed);
+  g.expert_bytes = static_cast<long long>(packed_expert_bytes(n, k));
+  g.num_experts = num_experts;
+  g.n = n;
+  g.k = k;
+  g.n_tiles = packed_tiles(n);
+  g.k_steps = packed_ksteps(k);
+  g.act = a;
+  g.family = kind == W4A16_GROUPED_CONTIGUOUS ? kContiguous : kMasked;
+  g.out_mode = kOutBf16;
+  g.layout = layout;
+  g.m = m;
+  g.block_m = bm;
+  g.out = out;
+  g.status = static_cast<int*>(workspace);
+  g.w_stages = w_stages;
+  g.b_stages = b_stages;
+  fill_tmem_slots(bm, &g);
+  g.timeout_cycles = wait_timeout_cycles();
+  const int sms = current_sm_count();
+  if (sms <= 0) return W4A16_ERR_CUDA;
+  const long long blocks = kind == W4A16_GROUPED_CONTIGUOUS
+                               ? m / bm
+                               : static_cast<long long>(num_experts) * ((m + bm - 1) / bm);
+  long long grid = plan->grid > 0 ? plan->grid : static_cast<long long>(sms) * plan->ctas_per_sm;
+  grid = std::max<long long>(1, std::min(grid, blocks * g.n_tiles));
+  (void)smem;
+  return cuda_status(launch_moe_gemm(g, static_cast<int>(grid), s));
+}
+
+w4a16_status w4a16_silu_and_mul(const uint16_t* in, int rows, int inter, uint16_t* out,
+                                void* stream) {
+  if (rows < 0 || inter <= 0 || inter % 8 != 0) return W4A16_ERR_INVALID_ARG;
+  if (rows > 0 && (in == nullptr || out == nullptr)) return W4A16_ERR_INVALID_ARG;
+  if (rows > 0 && (!aligned16(in) || !aligned16(out))) return W4A16_ERR_INVALID_ARG;
+  return cuda_status(launch_silu_and_mul(in, rows, inter, out, static_cast<cudaStream_t>(stream)));
+}
+
+w4a16_status w4a16_read_device_status(void* workspace, int* detail, void* stream) {
+  if (workspace == nullptr) return W4A16_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return W4A16_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpy(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return W4A16_ERR_CUDA;
+  if (detail != nullptr) *detail = word;
+  if (word == 0) return W4A16_OK;
+  if (cudaMemset(workspace, 0, sizeof(int)) != cudaSuccess) return W4A16_ERR_CUDA;
+  return W4A16_ERR_TIMEOUT;
+}
+
+}  // extern "C"

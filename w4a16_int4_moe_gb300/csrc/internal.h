@@ -1,0 +1,83 @@
+// internal.h -- host-side declarations shared by the library's translation
+// units (not part of the public ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/w4a16moe.h"
+
+namespace w4a16 {
+
+// Packed weight layout (W4A16_LAYOUT_KTILE64): for every expert, 128-row
+// tiles; inside a tile, 64-k steps back to back; one step holds
+//   q      [2 groups][128 rows][16 bytes]  (32 codes of one group per row)
+//   scales [2 groups][128 rows] BF16
+// so a whole tile's k range is one contiguous run of bytes.
+constexpr int kTileRows = 128;
+constexpr int kKStep = 64;
+constexpr int kGroup = 32;
+constexpr int kStepQBytes = 2 * kTileRows * 16;        // 4096
+constexpr int kStepBytes = kStepQBytes + 2 * kTileRows * 2;  // 4608
+constexpr int kStatusBytes = 256;
+
+inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+inline long long ceil_div_ll(long long a, long long b) { return (a + b - 1) / b; }
+
+inline int packed_tiles(int n) { return ceil_div(n, kTileRows); }
+inline int packed_ksteps(int k) { return ceil_div(k, kKStep); }
+inline size_t packed_expert_bytes(int n, int k) {
+  return static_cast<size_t>(packed_tiles(n)) * packed_ksteps(k) * kStepBytes;
+}
+
+enum Family { kIndexed = 0, kContiguous = 1, kMasked = 2 };
+enum OutMode { kOutBf16 = 0, kOutF32WeightedAdd = 1 };
+
+struct GemmArgs {
+  const uint8_t* wpack;
+  long long expert_bytes;
+  int num_experts, n, k, n_tiles, k_steps;
+  const uint16_t* act;  // BF16 rows of length k
+  int family;
+  int out_mode;
+  // indexed routing
+  const int32_t* sorted_ids;
+  const int32_t* expert_ids;
+  const int32_t* num_tokens_padded;
+  int capacity;
+  int numel;     // tokens * topk (sentinel)
+  int a_div;     // activation row = id / a_div
+  int o_div;     // output row = id / o_div
+  const float* topk_weights;
+  // grouped layouts
+  const int32_t* layout;  // m_expert [m] or masked_m [E]
+  int m;                  // rows (contiguous) or per-expert budget (masked)
+  // common
+  int block_m;
+  void* out;
+  int* status;
+  // pipeline configuration (derived from the plan)
+  int w_stages, b_stages, d_slots, d_cols;
+  long long timeout_cycles;
+};
+
+int device_sm_count(int device);
+size_t gemm_smem_bytes(int block_m, int w_stages, int b_stages);
+cudaError_t launch_moe_gemm(const GemmArgs& args, int grid, cudaStream_t stream);
+
+cudaError_t launch_align(const int32_t* topk_ids, int numel, int num_experts, int block_m,
+                         int capacity, int32_t* sorted_ids, int32_t* expert_ids,
+                         int32_t* num_tokens_padded, cudaStream_t stream);
+size_t align_smem_bytes(int num_experts);
+
+cudaError_t launch_prepack(const uint8_t* q, const uint16_t* scales, int num_experts, int n,
+                           int k, uint8_t* packed, cudaStream_t stream);
+cudaError_t launch_unpack(const uint8_t* packed, int num_experts, int n, int k, uint8_t* q,
+                          uint16_t* scales, cudaStream_t stream);
+
+cudaError_t launch_silu_and_mul(const uint16_t* in, int rows, int inter, uint16_t* out,
+                                cudaStream_t stream);
+
+}  // namespace w4a16

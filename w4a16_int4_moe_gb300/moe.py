@@ -1,0 +1,105 @@
+"""The layer-level call a user makes: prepacked weights resident on the GPU,
+then gate_up -> silu_and_mul -> down per batch of routed tokens.
+
+Every step is a call into the C-ABI library (``ops``); this module only
+allocates buffers (torch device memory) and sequences the calls on one
+stream.
+"""
+
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import ops
+
+
+@dataclass
+class PackedExperts:
+    """Prepacked expert weights of one projection: [num_experts, n, k]."""
+    packed: torch.Tensor
+    num_experts: int
+    n: int
+    k: int
+
+    @classmethod
+    def from_checkpoint(cls, q: torch.Tensor, scales: torch.Tensor, group: int = 32):
+        e, n, kh = q.shape
+        return cls(ops.w4a16_prepack(q, scales, group), e, n, kh * 2)
+
+
+class W4A16MoE:
+    """One MoE layer's expert pair on one GPU (gate_up [E, 2I, H], down [E, H, I])."""
+
+    def __init__(self, gate_up: PackedExperts, down: PackedExperts, topk: int,
+                 max_tokens: int, tok_e_hint: float = 0.0, device=None):
+        assert gate_up.num_experts == down.num_experts
+        assert gate_up.n == 2 * down.k and gate_up.k == down.n
+        self.gate_up, self.down = gate_up, down
+        self.num_experts = gate_up.num_experts
+        self.hidden, self.inter = gate_up.k, down.k
+        self.topk = topk
+        self.device = device or gate_up.packed.device
+        self.max_tokens = max_tokens
+        self.tok_e_hint = tok_e_hint
+        self._plan_for(max_tokens)
+
+    def _plan_for(self, tokens: int):
+        hint = self.tok_e_hint
+        self.plan_gu = ops.w4a16_plan(tokens, self.topk, self.num_experts, self.gate_up.n,
+                                      self.gate_up.k, hint)
+        self.plan_dn = ops.w4a16_plan(tokens, self.topk, self.num_experts, self.down.n,
+                                      self.down.k, hint)
+        # both GEMMs read the same routing blocks
+        self.plan_dn.block_m = self.plan_gu.block_m
+        self.block_m = self.plan_gu.block_m
+        numel = self.max_tokens * self.topk
+        self.capacity = ops.w4a16_align_capacity(numel, self.num_experts, self.block_m)
+        dev = self.device
+        self.sorted_ids = torch.empty(self.capacity, dtype=torch.int32, device=dev)
+        self.expert_ids = torch.empty(self.capacity // self.block_m, dtype=torch.int32, device=dev)
+        self.ntp = torch.empty(1, dtype=torch.int32, device=dev)
+        self.inter_buf = torch.empty((numel, 2 * self.inter), dtype=torch.bfloat16, device=dev)
+        self.act_buf = torch.empty((numel, self.inter), dtype=torch.bfloat16, device=dev)
+        self.workspace = ops.new_workspace(self.plan_gu, dev)
+
+    def align(self, topk_ids: torch.Tensor, stream=None):
+        return ops.w4a16_moe_align_block_size(
+            topk_ids, self.num_experts, self.block_m, self.capacity,
+            out=(self.sorted_ids, self.expert_ids, self.ntp), stream=stream)
+
+    def gate_up_gemm(self, x: torch.Tensor, tokens: int, stream=None):
+        numel = tokens * self.topk
+        return ops.w4a16_moe_indexed_gemm(
+            ops.W4A16_GATE_UP, self.gate_up.packed, self.num_experts, self.gate_up.n,
+            self.gate_up.k, x, tokens, self.topk, self.sorted_ids, self.expert_ids, self.ntp,
+            self.plan_gu, self.workspace, out=self.inter_buf[:numel], stream=stream)
+
+    def activation(self, tokens: int, stream=None):
+        numel = tokens * self.topk
+        return ops.w4a16_silu_and_mul(self.inter_buf[:numel], out=self.act_buf[:numel],
+                                      stream=stream)
+
+    def down_gemm(self, tokens: int, topk_weights: torch.Tensor, out: torch.Tensor, stream=None):
+        numel = tokens * self.topk
+        return ops.w4a16_moe_indexed_gemm(
+            ops.W4A16_DOWN, self.down.packed, self.num_experts, self.down.n, self.down.k,
+            self.act_buf[:numel], tokens, self.topk, self.sorted_ids, self.expert_ids, self.ntp,
+            self.plan_dn, self.workspace, topk_weights=topk_weights, out=out, stream=stream)
+
+    def forward(self, x: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor,
+                out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+        """x BF16 [T, H], topk_ids int32 [T, topk], topk_weights fp32 [T, topk]
+        -> fp32 [T, H] (this GPU's experts' share of the top-k weighted sum)."""
+        tokens = x.shape[0]
+        if tokens > self.max_tokens:
+            raise ValueError("more tokens than the layer was planned for")
+        if out is None:
+            out = torch.empty((tokens, self.hidden), dtype=torch.float32, device=x.device)
+        self.align(topk_ids, stream)
+        self.gate_up_gemm(x, tokens, stream)
+        self.activation(tokens, stream)
+        self.down_gemm(tokens, topk_weights, out, stream)
+        return out

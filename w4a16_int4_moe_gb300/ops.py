@@ -1,0 +1,252 @@
+"""Thin ctypes binding of ``libw4a16moe.so`` (declared in include/w4a16moe.h).
+
+Names follow the C entry points. Every function only marshals arguments:
+tensors become ``data_ptr()`` values, the stream is torch's current CUDA
+stream. All computation happens in the library's CUDA kernels; a missing or
+unloadable library raises ``RuntimeError`` (there is no CPU fallback).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+W4A16_OK = 0
+W4A16_ERR_INVALID_ARG = 1
+W4A16_ERR_UNSUPPORTED = 2
+W4A16_ERR_ROUTING = 3
+W4A16_ERR_WORKSPACE = 4
+W4A16_ERR_CUDA = 5
+W4A16_ERR_TIMEOUT = 6
+
+W4A16_GATE_UP = 0
+W4A16_DOWN = 1
+W4A16_GROUPED_CONTIGUOUS = 0
+W4A16_GROUPED_MASKED = 1
+W4A16_FLAG_VALIDATE_ROUTING = 1
+W4A16_FLAG_ACCUMULATE = 2
+W4A16_LAYOUT_KTILE64 = 0
+
+# Every symbol include/w4a16moe.h declares.
+EXPORTED = (
+    "w4a16_status_string", "w4a16_version", "w4a16_plan", "w4a16_align_capacity",
+    "w4a16_moe_align_block_size", "w4a16_prepack_size", "w4a16_prepack", "w4a16_unpack",
+    "w4a16_workspace_size", "w4a16_moe_indexed_gemm", "w4a16_moe_grouped_gemm",
+    "w4a16_silu_and_mul", "w4a16_read_device_status",
+)
+
+
+class Plan(ctypes.Structure):
+    """Mirror of w4a16_plan_t."""
+    _fields_ = [(name, ctypes.c_int) for name in (
+        "block_m", "bn", "bk", "stages", "b_stages", "split_k", "ctas_per_sm", "swap_ab",
+        "layout", "grid")]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+class W4A16Error(RuntimeError):
+    def __init__(self, fn, status, msg):
+        super().__init__(f"{fn} failed: status {status} ({msg})")
+        self.status = status
+
+
+_lib = None
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_Z = ctypes.c_size_t
+
+
+def load_library(path: Optional[str] = None):
+    """Load the library (building it first when it is missing or stale)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if path is None:
+        path = _build.LIB
+        if _build.is_stale():
+            _build.build_library()
+    if not os.path.exists(path):
+        raise RuntimeError(f"W4A16 MoE CUDA library not found at {path}")
+    lib = ctypes.CDLL(path)
+    sig = {
+        "w4a16_status_string": (ctypes.c_char_p, [_I]),
+        "w4a16_version": (_I, []),
+        "w4a16_plan": (_I, [_I, _I, _I, _I, _I, ctypes.c_float, ctypes.POINTER(Plan)]),
+        "w4a16_align_capacity": (_Z, [_I, _I, _I]),
+        "w4a16_moe_align_block_size": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
+        "w4a16_prepack_size": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(_Z)]),
+        "w4a16_prepack": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _Z, _P]),
+        "w4a16_unpack": (_I, [_P, _I, _I, _I, _P, _P, _P]),
+        "w4a16_workspace_size": (_Z, [ctypes.POINTER(Plan), _I, _I]),
+        "w4a16_moe_indexed_gemm": (_I, [_I, _P, _I, _I, _I, _P, _I, _I, _P, _P, _P, _I, _P, _P,
+                                        _I, ctypes.POINTER(Plan), _P, _Z, _P]),
+        "w4a16_moe_grouped_gemm": (_I, [_I, _P, _I, _I, _I, _P, _I, _P, _I, _P, _I,
+                                        ctypes.POINTER(Plan), _P, _Z, _P]),
+        "w4a16_silu_and_mul": (_I, [_P, _I, _I, _P, _P]),
+        "w4a16_read_device_status": (_I, [_P, ctypes.POINTER(_I), _P]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().w4a16_status_string(int(status)).decode()
+
+
+def _check(fn: str, status: int):
+    if status != W4A16_OK:
+        raise W4A16Error(fn, status, status_string(status))
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+# ------------------------------------------------------------- host only --
+
+def w4a16_version() -> int:
+    return load_library().w4a16_version()
+
+
+def w4a16_plan(tokens: int, topk: int, num_experts: int, n: int, k: int,
+               tok_e_hint: float = 0.0) -> Plan:
+    p = Plan()
+    _check("w4a16_plan", load_library().w4a16_plan(tokens, topk, num_experts, n, k,
+                                                    float(tok_e_hint), ctypes.byref(p)))
+    return p
+
+
+def w4a16_align_capacity(numel: int, num_experts: int, block_m: int) -> int:
+    return int(load_library().w4a16_align_capacity(numel, num_experts, block_m))
+
+
+def w4a16_prepack_size(num_experts: int, n: int, k: int, group: int = 32,
+                       layout: int = W4A16_LAYOUT_KTILE64) -> int:
+    out = _Z(0)
+    _check("w4a16_prepack_size", load_library().w4a16_prepack_size(
+        num_experts, n, k, group, layout, ctypes.byref(out)))
+    return int(out.value)
+
+
+def w4a16_workspace_size(plan: Plan, rows: int = 0, n: int = 0) -> int:
+    return int(load_library().w4a16_workspace_size(ctypes.byref(plan), rows, n))
+
+
+# ---------------------------------------------------------------- device --
+
+def w4a16_moe_align_block_size(topk_ids: torch.Tensor, num_experts: int, block_m: int,
+                               capacity: Optional[int] = None, out=None, stream=None):
+    """Returns (sorted_ids, expert_ids, num_tokens_padded) int32 device tensors."""
+    tokens, topk = topk_ids.shape
+    numel = tokens * topk
+    if capacity is None:
+        capacity = w4a16_align_capacity(numel, num_experts, block_m)
+    dev = topk_ids.device
+    if out is None:
+        out = (torch.empty(capacity, dtype=torch.int32, device=dev),
+               torch.empty(capacity // block_m, dtype=torch.int32, device=dev),
+               torch.empty(1, dtype=torch.int32, device=dev))
+    sorted_ids, expert_ids, ntp = out
+    _check("w4a16_moe_align_block_size", load_library().w4a16_moe_align_block_size(
+        _ptr(topk_ids), tokens, topk, num_experts, block_m, capacity,
+        _ptr(sorted_ids), _ptr(expert_ids), _ptr(ntp), _stream(stream)))
+    return sorted_ids, expert_ids, ntp
+
+
+def w4a16_prepack(q: torch.Tensor, scales: torch.Tensor, group: int = 32,
+                  layout: int = W4A16_LAYOUT_KTILE64, out: Optional[torch.Tensor] = None,
+                  stream=None) -> torch.Tensor:
+    """q uint8 [E, n, k/2], scales BF16 [E, n, k/32] -> packed uint8 blob."""
+    e, n, kh = q.shape
+    k = kh * 2
+    size = w4a16_prepack_size(e, n, k, group, layout)
+    if out is None:
+        out = torch.empty(size, dtype=torch.uint8, device=q.device)
+    _check("w4a16_prepack", load_library().w4a16_prepack(
+        _ptr(q), _ptr(scales), e, n, k, group, layout, _ptr(out), out.numel(), _stream(stream)))
+    return out
+
+
+def w4a16_unpack(packed: torch.Tensor, num_experts: int, n: int, k: int, stream=None):
+    q = torch.empty((num_experts, n, k // 2), dtype=torch.uint8, device=packed.device)
+    s = torch.empty((num_experts, n, k // 32), dtype=torch.int16, device=packed.device)
+    _check("w4a16_unpack", load_library().w4a16_unpack(
+        _ptr(packed), num_experts, n, k, _ptr(q), _ptr(s), _stream(stream)))
+    return q, s
+
+
+def new_workspace(plan: Plan, device, rows: int = 0, n: int = 0) -> torch.Tensor:
+    return torch.zeros(w4a16_workspace_size(plan, rows, n), dtype=torch.uint8, device=device)
+
+
+def w4a16_moe_indexed_gemm(mode: int, packed: torch.Tensor, num_experts: int, n: int, k: int,
+                           a: torch.Tensor, tokens: int, topk: int, sorted_ids: torch.Tensor,
+                           expert_ids: torch.Tensor, num_tokens_padded: torch.Tensor,
+                           plan: Plan, workspace: torch.Tensor,
+                           topk_weights: Optional[torch.Tensor] = None,
+                           out: Optional[torch.Tensor] = None, flags: int = 0, stream=None):
+    """GATE_UP: out BF16 [tokens*topk, n]; DOWN: out FP32 [tokens, n]."""
+    if out is None:
+        if mode == W4A16_GATE_UP:
+            out = torch.empty((tokens * topk, n), dtype=torch.bfloat16, device=a.device)
+        else:
+            out = torch.empty((tokens, n), dtype=torch.float32, device=a.device)
+    _check("w4a16_moe_indexed_gemm", load_library().w4a16_moe_indexed_gemm(
+        mode, _ptr(packed), num_experts, n, k, _ptr(a), tokens, topk, _ptr(sorted_ids),
+        _ptr(expert_ids), _ptr(num_tokens_padded), sorted_ids.numel(), _ptr(topk_weights),
+        _ptr(out), flags, ctypes.byref(plan), _ptr(workspace), workspace.numel(),
+        _stream(stream)))
+    return out
+
+
+def w4a16_moe_grouped_gemm(kind: int, packed: torch.Tensor, num_experts: int, n: int, k: int,
+                           a: torch.Tensor, m: int, layout: torch.Tensor, workspace: torch.Tensor,
+                           plan: Optional[Plan] = None, expected_m: int = 0,
+                           out: Optional[torch.Tensor] = None, flags: int = 0, stream=None):
+    """CONTIGUOUS: a [m, k] -> out [m, n]; MASKED: a [E, m, k] -> out [E, m, n] (BF16)."""
+    if out is None:
+        shape = (m, n) if kind == W4A16_GROUPED_CONTIGUOUS else (num_experts, m, n)
+        out = torch.empty(shape, dtype=torch.bfloat16, device=a.device)
+    _check("w4a16_moe_grouped_gemm", load_library().w4a16_moe_grouped_gemm(
+        kind, _ptr(packed), num_experts, n, k, _ptr(a), m, _ptr(layout), expected_m, _ptr(out),
+        flags, None if plan is None else ctypes.byref(plan), _ptr(workspace), workspace.numel(),
+        _stream(stream)))
+    return out
+
+
+def w4a16_silu_and_mul(x: torch.Tensor, out: Optional[torch.Tensor] = None, stream=None):
+    rows, two_i = x.shape
+    inter = two_i // 2
+    if out is None:
+        out = torch.empty((rows, inter), dtype=torch.bfloat16, device=x.device)
+    _check("w4a16_silu_and_mul", load_library().w4a16_silu_and_mul(
+        _ptr(x), rows, inter, _ptr(out), _stream(stream)))
+    return out
+
+
+def w4a16_read_device_status(workspace: torch.Tensor, stream=None):
+    """(status, raw word): W4A16_OK, or W4A16_ERR_TIMEOUT when a wait gave up."""
+    detail = _I(0)
+    st = load_library().w4a16_read_device_status(_ptr(workspace), ctypes.byref(detail),
+                                                 _stream(stream))
+    if st not in (W4A16_OK, W4A16_ERR_TIMEOUT):
+        _check("w4a16_read_device_status", st)
+    return st, int(detail.value)
