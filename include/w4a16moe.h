@@ -231,6 +231,40 @@ w4a16_status w4a16_silu_and_mul(const uint16_t* in, int rows, int inter, uint16_
  */
 w4a16_status w4a16_read_device_status(void* workspace, int* detail, void* stream);
 
+/*
+ * No-allocation variant of w4a16_moe_indexed_gemm. The pages have no
+ * counterpart of this call; it exists for callers that cannot allocate
+ * device memory when they call the operator: a host whose caching allocator
+ * owns all device memory and hands out no raw buffers, code that must not
+ * allocate after start-up (cudaMalloc/cudaFree may synchronise the device
+ * and take a global lock), or a plugin interface that passes only the
+ * operation's tensors.
+ * Same arguments and results as w4a16_moe_indexed_gemm, without the
+ * workspace: the library uses a fixed 64 KiB array of device memory compiled
+ * into it, which every GPU that loads the library holds until the process
+ * exits. The call allocates nothing. The caller still provides every input
+ * and output buffer.
+ * - Returns W4A16_ERR_WORKSPACE if w4a16_workspace_size(plan, ...) exceeds
+ *   64 KiB.
+ * - The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current); make that first call
+ *   before any stream capture begins.
+ * - Every call on a device shares the array and the call clears its status
+ *   word on `stream` first, so calls that overlap on the GPU (different
+ *   streams without ordering) race on it: order them, or use
+ *   w4a16_moe_indexed_gemm with one workspace per stream.
+ * - flags: those of w4a16_moe_indexed_gemm, plus W4A16_FLAG_SYNC_STATUS to
+ *   synchronise `stream` after the launch and return W4A16_ERR_TIMEOUT if a
+ *   device-side wait gave up (without it such a failure is not reported).
+ */
+enum { W4A16_FLAG_SYNC_STATUS = 4 };
+w4a16_status w4a16_moe_indexed_gemm_noalloc(int mode, const void* packed, int num_experts, int n,
+                                            int k, const uint16_t* a, int tokens, int topk,
+                                            const int32_t* sorted_ids, const int32_t* expert_ids,
+                                            const int32_t* num_tokens_padded, int capacity,
+                                            const float* topk_weights, void* out, int flags,
+                                            const w4a16_plan_t* plan, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

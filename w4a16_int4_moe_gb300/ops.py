@@ -31,13 +31,14 @@ W4A16_GROUPED_MASKED = 1
 W4A16_FLAG_VALIDATE_ROUTING = 1
 W4A16_FLAG_ACCUMULATE = 2
 W4A16_LAYOUT_KTILE64 = 0
+W4A16_FLAG_SYNC_STATUS = 4
 
 # Every symbol include/w4a16moe.h declares.
 EXPORTED = (
     "w4a16_status_string", "w4a16_version", "w4a16_plan", "w4a16_align_capacity",
     "w4a16_moe_align_block_size", "w4a16_prepack_size", "w4a16_prepack", "w4a16_unpack",
     "w4a16_workspace_size", "w4a16_moe_indexed_gemm", "w4a16_moe_grouped_gemm",
-    "w4a16_silu_and_mul", "w4a16_read_device_status",
+    "w4a16_silu_and_mul", "w4a16_read_device_status", "w4a16_moe_indexed_gemm_noalloc",
 )
 
 
@@ -92,6 +93,8 @@ def load_library(path: Optional[str] = None):
                                         ctypes.POINTER(Plan), _P, _Z, _P]),
         "w4a16_silu_and_mul": (_I, [_P, _I, _I, _P, _P]),
         "w4a16_read_device_status": (_I, [_P, ctypes.POINTER(_I), _P]),
+        "w4a16_moe_indexed_gemm_noalloc": (_I, [_I, _P, _I, _I, _I, _P, _I, _I, _P, _P, _P, _I,
+                                                _P, _P, _I, ctypes.POINTER(Plan), _P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -250,3 +253,26 @@ def w4a16_read_device_status(workspace: torch.Tensor, stream=None):
     if st not in (W4A16_OK, W4A16_ERR_TIMEOUT):
         _check("w4a16_read_device_status", st)
     return st, int(detail.value)
+
+
+def w4a16_moe_indexed_gemm_noalloc(mode: int, packed: torch.Tensor, num_experts: int, n: int,
+                                   k: int, a: torch.Tensor, tokens: int, topk: int,
+                                   sorted_ids: torch.Tensor, expert_ids: torch.Tensor,
+                                   num_tokens_padded: torch.Tensor, plan: Plan,
+                                   topk_weights: Optional[torch.Tensor] = None,
+                                   out: Optional[torch.Tensor] = None, flags: int = 0,
+                                   stream=None):
+    """w4a16_moe_indexed_gemm for callers that cannot allocate device memory:
+    no workspace argument; the library's built-in 64 KiB device array serves
+    as the workspace. Only ``out`` is allocated here when the caller passes
+    none (a caller that cannot allocate passes its own)."""
+    if out is None:
+        if mode == W4A16_GATE_UP:
+            out = torch.empty((tokens * topk, n), dtype=torch.bfloat16, device=a.device)
+        else:
+            out = torch.empty((tokens, n), dtype=torch.float32, device=a.device)
+    _check("w4a16_moe_indexed_gemm_noalloc", load_library().w4a16_moe_indexed_gemm_noalloc(
+        mode, _ptr(packed), num_experts, n, k, _ptr(a), tokens, topk, _ptr(sorted_ids),
+        _ptr(expert_ids), _ptr(num_tokens_padded), sorted_ids.numel(), _ptr(topk_weights),
+        _ptr(out), flags, ctypes.byref(plan), _stream(stream)))
+    return out
