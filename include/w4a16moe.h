@@ -79,7 +79,7 @@ int w4a16_version(void);
  */
 typedef struct {
   int block_m;     /* routing block rows: the align block size and the
-                      largest MMA N of one work item (16..256, step 16)   */
+                      largest MMA N of one work item (16..128, step 16)   */
   int bn;          /* weight rows per tile (MMA M) = 128                  */
   int bk;          /* K elements per pipeline step = 64                   */
   int stages;      /* weight ring depth, in pairs of K steps (2..16)      */
@@ -184,7 +184,7 @@ size_t w4a16_workspace_size(const w4a16_plan_t* plan, int rows, int n);
  * not depend on their contents. Blocks with expert -1 and sentinel rows are
  * skipped; ids out of range are ignored, never dereferenced.
  * Requires: k % 32 == 0, n >= 1, plan from w4a16_plan (block_m equal to the
- * align block size, 16..256 step 16), workspace >= w4a16_workspace_size,
+ * align block size, 16..128 step 16), workspace >= w4a16_workspace_size,
  * a, out 16-byte aligned.
  */
 w4a16_status w4a16_moe_indexed_gemm(int mode, const void* packed, int num_experts, int n, int k,

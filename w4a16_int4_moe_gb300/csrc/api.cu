@@ -36,7 +36,7 @@ int round_up(int x, int m) { return (x + m - 1) / m * m; }
 // Shared-memory-driven pipeline depths for a block_m; stages as given when
 // the plan sets them.
 bool plan_pipeline(const w4a16_plan_t& p, int* w_stages, int* b_stages, size_t* smem) {
-  if (p.block_m < 16 || p.block_m > 256 || p.block_m % 16 != 0) return false;
+  if (p.block_m < 16 || p.block_m > 128 || p.block_m % 16 != 0) return false;
   if (p.bn != kTileRows || p.bk != kKStep || p.split_k != 1 || p.layout != W4A16_LAYOUT_KTILE64)
     return false;
   if (p.stages < 2 || p.stages > 16 || p.b_stages < 4 || p.b_stages > 16 || p.b_stages % 2 != 0)
@@ -55,10 +55,22 @@ int current_sm_count() {
   return device_sm_count(dev);
 }
 
+// TMEM (512 columns): 2 * a_slots A slots of 32 columns (64 BF16 of K per
+// lane), then d_slots accumulator slots, each holding the two partial
+// accumulators (even / odd k steps) of d_cols columns. Two accumulator slots
+// let the epilogue of one item overlap the next item's MMAs; the remaining
+// columns deepen the A ring (up to 6 slots per dequant warpgroup).
 void fill_tmem_slots(int block_m, GemmArgs* a) {
   const int dcols = round_up(block_m, 32);
   a->d_cols = dcols;
-  a->d_slots = (128 + 2 * dcols <= 512) ? 2 : 1;
+  a->d_slots = (2 * 64 + 2 * 2 * dcols <= 512) ? 2 : 1;
+  int sa = 6;
+  while (sa > 2 && 64 * sa + a->d_slots * 2 * dcols > 512) --sa;
+  if (const char* e = std::getenv("W4A16_TUNE_A_SLOTS")) {
+    const int v = std::atoi(e);
+    if (v >= 2 && v <= 8 && 64 * v + a->d_slots * 2 * dcols <= 512) sa = v;
+  }
+  a->a_slots = sa;
 }
 
 }  // namespace
@@ -97,7 +109,7 @@ w4a16_status w4a16_plan(int tokens, int topk, int num_experts, int n, int k, flo
     block_m = round_up(std::max(16, static_cast<int>(std::ceil(1.5 * tok_e))), 16);
     block_m = std::min(block_m, 128);
   } else {
-    block_m = tok_e <= 192.0 ? 128 : 256;
+    block_m = 128;
   }
   w4a16_plan_t p;
   std::memset(&p, 0, sizeof(p));

@@ -59,7 +59,7 @@ struct GemmArgs {
   void* out;
   int* status;
   // pipeline configuration (derived from the plan)
-  int w_stages, b_stages, d_slots, d_cols;
+  int w_stages, b_stages, d_slots, d_cols, a_slots;
   long long timeout_cycles;
 };
 

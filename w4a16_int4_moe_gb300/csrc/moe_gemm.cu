@@ -39,20 +39,21 @@ namespace w4a16 {
 
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 576;
 constexpr int kWStageBytes = 2 * kStepBytes;  // one weight stage = 2 k steps
-constexpr int kASlots = 4;                    // 2 per dequant warpgroup
+constexpr int kMaxASlots = 16;                // A slots over both dequant warpgroups
 constexpr int kAColsPerSlot = 32;             // 64 BF16 of K per TMEM lane
-constexpr int kDColBase = kASlots * kAColsPerSlot;
 constexpr int kTmemCols = 512;
 constexpr int kGatherLag = 2;
 
-// warp roles
+// warp roles (warp 3 idles; the warpgroups start at multiples of 4 warps so
+// that warp % 4 selects the TMEM lane quarter each warp may access)
 constexpr int kWarpProducer = 0;
-constexpr int kWarpMma = 1;
-constexpr int kWarpGather0 = 2;   // 2 warps
-constexpr int kWarpDequant0 = 4;  // 8 warps (2 warpgroups)
+constexpr int kWarpMma0 = 1;        // MMA issuer of the even k steps (+ TMEM allocation)
+constexpr int kWarpMma1 = 2;        // MMA issuer of the odd k steps
+constexpr int kWarpDequant0 = 4;    // 8 warps (2 warpgroups)
 constexpr int kWarpEpilogue0 = 12;  // 4 warps
+constexpr int kWarpGather0 = 16;    // 2 warps
 
 // where codes recorded in the status word when a wait gives up
 enum Where {
@@ -93,7 +94,7 @@ __device__ __forceinline__ size_t align_up(size_t x, size_t a) { return (x + a -
 
 // Bounded wait: true when the phase of parity `parity` has completed; false
 // when the CTA is aborting or this wait ran out (then it starts the abort).
-__device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                         int* status, int where, long long timeout) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
@@ -224,7 +225,8 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_moe_gemm_kernel(const GemmA
   off = align_up(off, 8);
   sm.bars = reinterpret_cast<uint64_t*>(base + off);
   const int WS = args.w_stages, BS = args.b_stages;
-  const int n_bars = 2 * WS + 2 * kASlots + 2 * BS + 2 + 2 + 2 + 2 + 1;
+  const int SA = args.a_slots;  // A slots per dequant warpgroup
+  const int n_bars = 2 * WS + 4 * SA + 2 * BS + 2 + 2 + 2 + 2 + 2;
   off += n_bars * 8;
   sm.tmem_base = reinterpret_cast<uint32_t*>(base + off);
   off += 4;
@@ -238,9 +240,9 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_moe_gemm_kernel(const GemmA
     B.w_empty = b0;
     b0 += 8 * WS;
     B.a_full = b0;
-    b0 += 8 * kASlots;
+    b0 += 8 * 2 * SA;
     B.a_empty = b0;
-    b0 += 8 * kASlots;
+    b0 += 8 * 2 * SA;
     B.b_full = b0;
     b0 += 8 * BS;
     B.b_empty = b0;
@@ -263,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_moe_gemm_kernel(const GemmA
       mbar_init(B.wf(i), 1);
       mbar_init(B.we(i), 8);  // every dequant warp releases every stage
     }
-    for (int i = 0; i < kASlots; ++i) {
+    for (int i = 0; i < 2 * SA; ++i) {
       mbar_init(B.af(i), 4);  // the 4 warps of the owning warpgroup
       mbar_init(B.ae(i), 1);  // tcgen05.commit
     }
@@ -274,15 +276,16 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_moe_gemm_kernel(const GemmA
     for (int i = 0; i < 2; ++i) {
       mbar_init(B.itf(i), 2);  // lane 0 of each gather warp
       mbar_init(B.ite(i), 4);
-      mbar_init(B.accf(i), 1);
+      mbar_init(B.accf(i), 2);  // one tcgen05.commit per MMA issuer
       mbar_init(B.acce(i), 4);
     }
     mbar_init(B.final_bar, 1);
+    mbar_init(B.final_bar + 8, 1);
     *sm.abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
   }
-  if (warp == kWarpMma) {
+  if (warp == kWarpMma0) {
     tmem_alloc(smem_u32(sm.tmem_base), kTmemCols);
     tmem_relinquish();
   }
@@ -304,6 +307,9 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_moe_gemm_kernel(const GemmA
     num_blocks = args.num_experts * bpe;
   }
   const int items = num_blocks * args.n_tiles;
+  // TMEM columns: A slots first, then per accumulator slot the two partial
+  // accumulators (even / odd k steps) of d_cols columns each.
+  const int d_col_base = 2 * SA * kAColsPerSlot;
   const int n_wst = (args.k_steps + 1) / 2;
   const long long tmo = args.timeout_cycles;
   volatile int* abort_flag = sm.abort_flag;
@@ -346,12 +352,17 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_moe_gemm_kernel(const GemmA
         }
       }
     }
-  } else if (warp == kWarpMma) {
-    // ======================= MMA issuer =====================================
+  } else if (warp == kWarpMma0 || warp == kWarpMma1) {
+    // ======================= MMA issuers ====================================
+    // Issuer g owns the k steps with ks % 2 == g: it consumes dequant
+    // warpgroup g's A slots and gather warp g's B stages, and accumulates into
+    // its own FP32 partial accumulator; the epilogue adds the two partials in
+    // a fixed order. At small N one issuing thread, not the tensor core, sets
+    // the pace (each tcgen05.mma blocks its issuer for tens of cycles), so two
+    // independent issuers double the MMA rate.
+    const int g = warp - kWarpMma0;
     if (lane == 0) {
-      uint32_t acnt[2] = {0, 0};
-      uint32_t bcnt[2] = {0, 0};
-      uint32_t icnt = 0, dcnt = 0;
+      uint32_t acnt = 0, bcnt = 0, icnt = 0, dcnt = 0;
       const int bhalf = BS / 2;
       bool ok = true;
       for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
@@ -371,14 +382,12 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_moe_gemm_kernel(const GemmA
         }
         tc_fence_after();
         const uint32_t idesc = idesc_bf16_m128(static_cast<uint32_t>(n16));
-        const uint32_t d_tmem = tmem + kDColBase + dslot * args.d_cols;
-        for (int ks = 0; ks < args.k_steps; ++ks) {
-          const int g = ks & 1;
-          const int aslot = 2 * g + (acnt[g] & 1);
-          const int bslot = 2 * (bcnt[g] % bhalf) + g;
-          if (!wait_phase(B.af(aslot), (acnt[g] >> 1) & 1, abort_flag, status, kWhereMmaA, tmo) ||
-              !wait_phase(B.bf(bslot), (bcnt[g] / bhalf) & 1, abort_flag, status, kWhereMmaB,
-                          tmo)) {
+        const uint32_t d_tmem = tmem + d_col_base + (dslot * 2 + g) * args.d_cols;
+        for (int ks = g; ks < args.k_steps; ks += 2) {
+          const int aslot = g * SA + static_cast<int>(acnt % SA);
+          const int bslot = 2 * static_cast<int>(bcnt % bhalf) + g;
+          if (!wait_phase(B.af(aslot), (acnt / SA) & 1, abort_flag, status, kWhereMmaA, tmo) ||
+              !wait_phase(B.bf(bslot), (bcnt / bhalf) & 1, abort_flag, status, kWhereMmaB, tmo)) {
             ok = false;
             break;
           }
@@ -388,25 +397,25 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_moe_gemm_kernel(const GemmA
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             mma_bf16_ts(d_tmem, a_tmem + kk * 8, smem_desc_sw128_kmajor(b_addr + kk * 32), idesc,
-                        (ks | kk) != 0 ? 1u : 0u);
+                        (ks != g || kk != 0) ? 1u : 0u);
           }
           tc_commit(B.ae(aslot));
           tc_commit(B.be(bslot));
-          ++acnt[g];
-          ++bcnt[g];
+          ++acnt;
+          ++bcnt;
         }
         if (!ok) break;
         tc_commit(B.accf(dslot));
         ++icnt;
         ++dcnt;
       }
-      // every MMA issued by this thread has finished once final_bar flips
-      tc_commit(B.final_bar);
+      // every MMA issued by this thread has finished once its final barrier flips
+      tc_commit(B.final_bar + 8 * g);
       const long long t0 = clock64();
-      while (!mbar_try_wait(B.final_bar, 0) && clock64() - t0 < tmo) {
+      while (!mbar_try_wait(B.final_bar + 8 * g, 0) && clock64() - t0 < tmo) {
       }
     }
-  } else if (warp < kWarpDequant0) {
+  } else if (warp >= kWarpGather0) {
     // ======================= token gather (cp.async) ========================
     // Gather warp gw fills the B stages of the k steps with ks % 2 == gw into
     // its own half of the ring, and keeps its own copy of the block's row
@@ -485,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_moe_gemm_kernel(const GemmA
       ++icnt;
     }
     cp_async_wait<0>();
-  } else if (warp < kWarpEpilogue0) {
+  } else if (warp >= kWarpDequant0 && warp < kWarpEpilogue0) {
     // ======================= dequantisation into TMEM =======================
     // Warpgroup g dequantises the k steps with ks % 2 == g; thread r of the
     // warpgroup owns weight row r of the tile, i.e. TMEM lane r.
@@ -519,8 +528,8 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_moe_gemm_kernel(const GemmA
         uint32_t v[32];
         dequant_group(q0, s0, v);
         dequant_group(q1, s1, v + 16);
-        const int aslot = 2 * g + (acnt & 1);
-        ok = __all_sync(0xffffffffu, wait_phase(B.ae(aslot), ((acnt >> 1) & 1) ^ 1, abort_flag,
+        const int aslot = g * SA + static_cast<int>(acnt % SA);
+        ok = __all_sync(0xffffffffu, wait_phase(B.ae(aslot), ((acnt / SA) & 1) ^ 1, abort_flag,
                                                  status, kWhereDequantA, tmo));
         if (!ok) break;
         tc_fence_after();
@@ -532,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_moe_gemm_kernel(const GemmA
         ++acnt;
       }
     }
-  } else {
+  } else if (warp >= kWarpEpilogue0) {
     // ======================= epilogue =======================================
     // Thread r owns weight row r of the tile (TMEM lane r): it reads the
     // block's token columns and writes output column tile*128 + r.
@@ -555,17 +564,21 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_moe_gemm_kernel(const GemmA
       const float* iwt = sm.info_wt + islot * bm;
       const int ng = d.tile * kTileRows + r;
       const bool row_ok = ng < args.n;
-      const uint32_t dcol = tmem + lane_base + kDColBase + dslot * args.d_cols;
+      const uint32_t dcol0 = tmem + lane_base + d_col_base + (dslot * 2) * args.d_cols;
+      const uint32_t dcol1 = dcol0 + args.d_cols;
+      const bool odd_steps = args.k_steps > 1;  // the odd-k accumulator holds data
       for (int j0 = 0; j0 < n16; j0 += 16) {
-        uint32_t v[16];
-        tmem_ld_32x32b_x16(dcol + j0, v);
+        uint32_t v[16], w[16];
+        tmem_ld_32x32b_x16(dcol0 + j0, v);
+        if (odd_steps) tmem_ld_32x32b_x16(dcol1 + j0, w);
         tmem_ld_wait();
         if (!row_ok) continue;
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) {
           const int dr = idst[j0 + jj];
           if (dr < 0) continue;
-          const float x = __uint_as_float(v[jj]);
+          const float x = odd_steps ? __uint_as_float(v[jj]) + __uint_as_float(w[jj])
+                                    : __uint_as_float(v[jj]);
           if (args.out_mode == kOutF32WeightedAdd) {
             float* o = static_cast<float*>(args.out) + static_cast<long long>(dr) * args.n + ng;
             atomicAdd(o, iwt[j0 + jj] * x);
@@ -591,7 +604,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_moe_gemm_kernel(const GemmA
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (warp == kWarpMma) {
+  if (warp == kWarpMma0) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -603,7 +616,7 @@ size_t gemm_smem_bytes(int block_m, int w_stages, int b_stages) {
   off += static_cast<size_t>(w_stages) * kWStageBytes;
   off += 3 * 4 * static_cast<size_t>(block_m) * 4 + 4 * 4;
   off = (off + 7) / 8 * 8;
-  off += (2 * w_stages + 2 * kASlots + 2 * b_stages + 9) * 8;
+  off += (2 * w_stages + 2 * kMaxASlots + 2 * b_stages + 10) * 8;
   off += 8;
   return off;
 }
