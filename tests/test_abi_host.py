@@ -52,11 +52,11 @@ def test_plan_follows_tok_e(lib):
     # TP8 T=16: a third of a row per expert
     assert ops.w4a16_plan(16, 8, 384, 512, 7168).block_m == 16
     # prefill above the ~80 rows/expert switch
-    assert ops.w4a16_plan(8192, 8, 384, 4096, 7168, 81.3).block_m == 128
-    assert ops.w4a16_plan(8192, 8, 48, 4096, 7168, 600.0).block_m == 128
+    assert ops.w4a16_plan(8192, 8, 384, 4096, 7168, 81.3).block_m == 64
+    assert ops.w4a16_plan(8192, 8, 48, 4096, 7168, 600.0).block_m == 64
     for tok_e in (0.3, 5, 12, 40, 80, 81, 150, 400):
         p = ops.w4a16_plan(1024, 8, 48, 4096, 7168, float(tok_e))
-        assert 16 <= p.block_m <= 128 and p.block_m % 16 == 0
+        assert 16 <= p.block_m <= 64 and p.block_m % 16 == 0
         assert 2 <= p.stages <= 16 and p.b_stages % 2 == 0 and p.split_k == 1
 
 
@@ -103,6 +103,11 @@ def test_gemm_argument_checks_before_any_launch(lib):
     bad = ops.Plan.from_buffer_copy(plan)
     bad.block_m = 24
     assert lib.w4a16_moe_indexed_gemm(0, fake, 8, 1024, 512, fake, 64, 2, fake, fake, fake, 240,
+                                      None, fake, 0, ctypes.byref(bad), fake, 256, None) \
+        == ops.W4A16_ERR_INVALID_ARG
+    bad = ops.Plan.from_buffer_copy(plan)
+    bad.block_m = 128   # gathered rows: at most 64 rows per block (half-filled 8-row atoms)
+    assert lib.w4a16_moe_indexed_gemm(0, fake, 8, 1024, 512, fake, 64, 2, fake, fake, fake, 256,
                                       None, fake, 0, ctypes.byref(bad), fake, 256, None) \
         == ops.W4A16_ERR_INVALID_ARG
     bad = ops.Plan.from_buffer_copy(plan)

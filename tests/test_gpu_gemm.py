@@ -107,7 +107,7 @@ def _check_pair(p, device, bm, cols_gu=None, cols_dn=None, what=""):
 
 # ------------------------------------------------------------ small shapes --
 
-@pytest.mark.parametrize("bm", [16, 32, 64, 112, 128])
+@pytest.mark.parametrize("bm", [16, 32, 48, 64])
 def test_tiny_all_block_sizes(cuda_dev, bm):
     _check_pair(wl.tiny(), cuda_dev, bm, what=f"tiny bm={bm}")
 
@@ -116,7 +116,7 @@ def test_tiny_all_block_sizes(cuda_dev, bm):
     (37, 96, 96, 5, 3, 16),      # k = 32 mod 64 on both GEMMs, ragged n (192 / 96 rows)
     (200, 320, 224, 6, 2, 64),   # ragged n tiles (448 / 320 rows), k = 32 mod 64 on down
     (5, 64, 32, 40, 4, 16),      # far more experts than rows: many empty experts
-    (130, 256, 160, 3, 1, 128),  # top-1, rows above one block per expert
+    (130, 256, 160, 3, 1, 64),   # top-1, several blocks per expert
 ])
 def test_ragged_shapes(cuda_dev, tokens, hidden, inter, experts, topk, bm):
     p = wl.uniform_problem(tokens, hidden, inter, experts, topk, seed=tokens)
@@ -156,8 +156,8 @@ def test_schedules_are_bitwise_identical(cuda_dev):
     p = wl.uniform_problem(96, 512, 256, 8, 2, seed=8)
     pk = _pack(p.q_gu, p.s_gu, cuda_dev)
     ref = None
-    for bm, st, bst, grid in [(16, 8, 8, 0), (32, 4, 4, 0), (64, 16, 6, 3), (128, 2, 4, 1),
-                              (112, 6, 4, 0), (48, 5, 10, 7)]:
+    for bm, st, bst, grid in [(16, 8, 8, 0), (32, 4, 4, 0), (64, 8, 6, 3), (64, 2, 4, 1),
+                              (16, 3, 12, 5), (48, 5, 10, 7)]:
         routing = _routing(p.topk_ids, p.num_experts, bm, cuda_dev)
         g = _gate_up(p, pk, routing, _plan(bm, 2 * p.inter, p.hidden, st, bst, grid), cuda_dev)
         bits = bf16_bits(g)[_routed(p)]

@@ -33,44 +33,61 @@ long long wait_timeout_cycles() {
 
 int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
-// Shared-memory-driven pipeline depths for a block_m; stages as given when
-// the plan sets them.
-bool plan_pipeline(const w4a16_plan_t& p, int* w_stages, int* b_stages, size_t* smem) {
-  if (p.block_m < 16 || p.block_m > 128 || p.block_m % 16 != 0) return false;
+// TMEM (512 columns): the operand ring's 2 * S A slots of 32 columns (64
+// BF16 of K per lane), then d_slots accumulator slots, each holding the two
+// partial accumulators (even / odd k steps) of d_cols columns. Two
+// accumulator slots let the epilogue of one item overlap the next item's
+// MMAs; the remaining columns deepen the ring (up to 6 slots per parity).
+int tmem_ring_slots(int block_m, bool gather, int* d_cols, int* d_slots) {
+  const int dcols = round_up(max_mma_n(block_m, gather), 32);
+  const int dsl = (2 * 64 + 2 * 2 * dcols <= 512) ? 2 : 1;
+  int s = 6;
+  while (s > 2 && 64 * s + dsl * 2 * dcols > 512) --s;
+  if (d_cols) *d_cols = dcols;
+  if (d_slots) *d_slots = dsl;
+  return s;
+}
+
+struct Pipeline {
+  int w_stages, ring_slots, d_cols, d_slots;
+  size_t smem;
+};
+
+// Validate a plan and derive the pipeline: the operand ring depth is the
+// smaller of what TMEM allows and plan.b_stages / 2. Gathered rows (indexed
+// family) use half of every 8-row atom, so their block is at most 64 rows.
+bool plan_pipeline(const w4a16_plan_t& p, bool gather, Pipeline* out) {
+  if (p.block_m < 16 || p.block_m > (gather ? 64 : 128) || p.block_m % 16 != 0) return false;
   if (p.bn != kTileRows || p.bk != kKStep || p.split_k != 1 || p.layout != W4A16_LAYOUT_KTILE64)
     return false;
   if (p.stages < 2 || p.stages > 16 || p.b_stages < 4 || p.b_stages > 16 || p.b_stages % 2 != 0)
     return false;
-  const size_t bytes = gemm_smem_bytes(p.block_m, p.stages, p.b_stages);
-  if (bytes > static_cast<size_t>(kMaxDynSmem)) return false;
-  *w_stages = p.stages;
-  *b_stages = p.b_stages;
-  *smem = bytes;
+  Pipeline pl;
+  int s = tmem_ring_slots(p.block_m, gather, &pl.d_cols, &pl.d_slots);
+  if (const char* e = std::getenv("W4A16_TUNE_A_SLOTS")) {
+    const int v = std::atoi(e);
+    if (v >= 2 && v < s) s = v;
+  }
+  pl.ring_slots = std::min(s, p.b_stages / 2);
+  pl.w_stages = p.stages;
+  pl.smem = gemm_smem_bytes(p.block_m, gather, pl.w_stages, pl.ring_slots);
+  if (pl.smem > static_cast<size_t>(kMaxDynSmem)) return false;
+  *out = pl;
   return true;
+}
+
+void fill_pipeline(const Pipeline& pl, GemmArgs* g) {
+  g->w_stages = pl.w_stages;
+  g->b_stages = 2 * pl.ring_slots;
+  g->a_slots = pl.ring_slots;
+  g->d_cols = pl.d_cols;
+  g->d_slots = pl.d_slots;
 }
 
 int current_sm_count() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   return device_sm_count(dev);
-}
-
-// TMEM (512 columns): 2 * a_slots A slots of 32 columns (64 BF16 of K per
-// lane), then d_slots accumulator slots, each holding the two partial
-// accumulators (even / odd k steps) of d_cols columns. Two accumulator slots
-// let the epilogue of one item overlap the next item's MMAs; the remaining
-// columns deepen the A ring (up to 6 slots per dequant warpgroup).
-void fill_tmem_slots(int block_m, GemmArgs* a) {
-  const int dcols = round_up(block_m, 32);
-  a->d_cols = dcols;
-  a->d_slots = (2 * 64 + 2 * 2 * dcols <= 512) ? 2 : 1;
-  int sa = 6;
-  while (sa > 2 && 64 * sa + a->d_slots * 2 * dcols > 512) --sa;
-  if (const char* e = std::getenv("W4A16_TUNE_A_SLOTS")) {
-    const int v = std::atoi(e);
-    if (v >= 2 && v <= 8 && 64 * v + a->d_slots * 2 * dcols <= 512) sa = v;
-  }
-  a->a_slots = sa;
 }
 
 }  // namespace
@@ -107,19 +124,20 @@ w4a16_status w4a16_plan(int tokens, int topk, int num_experts, int n, int k, flo
   int block_m;
   if (tok_e <= 80.0) {
     block_m = round_up(std::max(16, static_cast<int>(std::ceil(1.5 * tok_e))), 16);
-    block_m = std::min(block_m, 128);
+    block_m = std::min(block_m, 64);
   } else {
-    block_m = 128;
+    block_m = 64;
   }
   w4a16_plan_t p;
   std::memset(&p, 0, sizeof(p));
   p.block_m = block_m;
   p.bn = kTileRows;
   p.bk = kKStep;
-  p.b_stages = block_m <= 32 ? 8 : (block_m <= 64 ? 6 : 4);
+  const int ring = tmem_ring_slots(block_m, true, nullptr, nullptr);
+  p.b_stages = 2 * ring;
   // weight ring: as deep as shared memory allows (up to 16 stages of 9 KB)
   int ws = 16;
-  while (ws > 2 && gemm_smem_bytes(block_m, ws, p.b_stages) > static_cast<size_t>(kMaxDynSmem))
+  while (ws > 2 && gemm_smem_bytes(block_m, true, ws, ring) > static_cast<size_t>(kMaxDynSmem))
     --ws;
   p.stages = ws;
   p.split_k = 1;
@@ -223,9 +241,8 @@ w4a16_status w4a16_moe_indexed_gemm(int mode, const void* packed, int num_expert
     return W4A16_ERR_INVALID_ARG;
   if (workspace == nullptr || ws_bytes < w4a16_workspace_size(plan, tokens * topk, n))
     return W4A16_ERR_WORKSPACE;
-  int w_stages = 0, b_stages = 0;
-  size_t smem = 0;
-  if (!plan_pipeline(*plan, &w_stages, &b_stages, &smem)) return W4A16_ERR_INVALID_ARG;
+  Pipeline pl;
+  if (!plan_pipeline(*plan, true, &pl)) return W4A16_ERR_INVALID_ARG;
   const int bm = plan->block_m;
   if (capacity % bm != 0) return W4A16_ERR_INVALID_ARG;
   const long long numel = static_cast<long long>(tokens) * topk;
@@ -274,6 +291,9 @@ w4a16_status w4a16_moe_indexed_gemm(int mode, const void* packed, int num_expert
   g.n_tiles = packed_tiles(n);
   g.k_steps = packed_ksteps(k);
   g.act = a;
+  g.gather_rows = 1;
+  g.act_rows = static_cast<int>(mode == W4A16_DOWN ? numel : tokens);
+  if (!encode_act_tmap(&g.tmap, a, g.act_rows, k, 1)) return W4A16_ERR_CUDA;
   g.family = kIndexed;
   g.out_mode = mode == W4A16_DOWN ? kOutF32WeightedAdd : kOutBf16;
   g.sorted_ids = sorted_ids;
@@ -287,16 +307,13 @@ w4a16_status w4a16_moe_indexed_gemm(int mode, const void* packed, int num_expert
   g.block_m = bm;
   g.out = out;
   g.status = static_cast<int*>(workspace);
-  g.w_stages = w_stages;
-  g.b_stages = b_stages;
-  fill_tmem_slots(bm, &g);
+  fill_pipeline(pl, &g);
   g.timeout_cycles = wait_timeout_cycles();
   const int sms = current_sm_count();
   if (sms <= 0) return W4A16_ERR_CUDA;
   long long grid = plan->grid > 0 ? plan->grid : static_cast<long long>(sms) * plan->ctas_per_sm;
   const long long max_items = static_cast<long long>(capacity / bm) * g.n_tiles;
   grid = std::max<long long>(1, std::min(grid, max_items));
-  (void)smem;
   return cuda_status(launch_moe_gemm(g, static_cast<int>(grid), s));
 }
 
@@ -318,14 +335,13 @@ w4a16_status w4a16_moe_grouped_gemm(int kind, const void* packed, int num_expert
   if (plan == nullptr) {
     const int rows = expected_m > 0 ? expected_m : std::max(1, m);
     w4a16_plan(rows, 1, 1, n, k, static_cast<float>(rows), &local);
-    if (kind == W4A16_GROUPED_CONTIGUOUS) local.block_m = std::min(local.block_m, 128);
+    if (rows > 80) local.block_m = 128;  // consecutive rows fill whole atoms
     plan = &local;
   }
   if (workspace == nullptr || ws_bytes < w4a16_workspace_size(plan, m, n))
     return W4A16_ERR_WORKSPACE;
-  int w_stages = 0, b_stages = 0;
-  size_t smem = 0;
-  if (!plan_pipeline(*plan, &w_stages, &b_stages, &smem)) return W4A16_ERR_INVALID_ARG;
+  Pipeline pl;
+  if (!plan_pipeline(*plan, false, &pl)) return W4A16_ERR_INVALID_ARG;
   const int bm = plan->block_m;
   const long long rows_total =
       kind == W4A16_GROUPED_MASKED ? static_cast<long long>(num_experts) * m : m;
@@ -366,6 +382,9 @@ w4a16_status w4a16_moe_grouped_gemm(int kind, const void* packed, int num_expert
   g.n_tiles = packed_tiles(n);
   g.k_steps = packed_ksteps(k);
   g.act = a;
+  g.gather_rows = 0;
+  g.act_rows = static_cast<int>(rows_total);
+  if (!encode_act_tmap(&g.tmap, a, rows_total, k, 8)) return W4A16_ERR_CUDA;
   g.family = kind == W4A16_GROUPED_CONTIGUOUS ? kContiguous : kMasked;
   g.out_mode = kOutBf16;
   g.layout = layout;
@@ -373,9 +392,7 @@ w4a16_status w4a16_moe_grouped_gemm(int kind, const void* packed, int num_expert
   g.block_m = bm;
   g.out = out;
   g.status = static_cast<int*>(workspace);
-  g.w_stages = w_stages;
-  g.b_stages = b_stages;
-  fill_tmem_slots(bm, &g);
+  fill_pipeline(pl, &g);
   g.timeout_cycles = wait_timeout_cycles();
   const int sms = current_sm_count();
   if (sms <= 0) return W4A16_ERR_CUDA;
@@ -384,7 +401,6 @@ w4a16_status w4a16_moe_grouped_gemm(int kind, const void* packed, int num_expert
                                : static_cast<long long>(num_experts) * ((m + bm - 1) / bm);
   long long grid = plan->grid > 0 ? plan->grid : static_cast<long long>(sms) * plan->ctas_per_sm;
   grid = std::max<long long>(1, std::min(grid, blocks * g.n_tiles));
-  (void)smem;
   return cuda_status(launch_moe_gemm(g, static_cast<int>(grid), s));
 }
 

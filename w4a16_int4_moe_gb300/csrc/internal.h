@@ -2,6 +2,7 @@
 // units (not part of the public ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstddef>
@@ -36,6 +37,12 @@ enum Family { kIndexed = 0, kContiguous = 1, kMasked = 2 };
 enum OutMode { kOutBf16 = 0, kOutF32WeightedAdd = 1 };
 
 struct GemmArgs {
+  // Activation tensor map (BF16 [act_rows, k], 128-byte swizzle, box 64 x
+  // box_rows): box_rows 1 for the row gather (tile::gather4), 8 for
+  // consecutive rows.
+  CUtensorMap tmap;
+  int act_rows;
+  int gather_rows;  // 1: rows gathered four at a time, 4 real rows per 8-row atom
   const uint8_t* wpack;
   long long expert_bytes;
   int num_experts, n, k, n_tiles, k_steps;
@@ -64,7 +71,12 @@ struct GemmArgs {
 };
 
 int device_sm_count(int device);
-size_t gemm_smem_bytes(int block_m, int w_stages, int b_stages);
+// Largest MMA N of a block: gathered rows fill half of every 8-row atom.
+__host__ __device__ inline int max_mma_n(int block_m, bool gather) {
+  return gather ? 2 * block_m : block_m;
+}
+size_t gemm_smem_bytes(int block_m, bool gather, int w_stages, int ring_slots);
+bool encode_act_tmap(CUtensorMap* map, const void* act, long long rows, int k, int box_rows);
 cudaError_t launch_moe_gemm(const GemmArgs& args, int grid, cudaStream_t stream);
 
 cudaError_t launch_align(const int32_t* topk_ids, int numel, int num_experts, int block_m,

@@ -30,6 +30,8 @@
 
 #include <cuda_bf16.h>
 
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "internal.h"
@@ -41,10 +43,8 @@ namespace {
 
 constexpr int kThreads = 576;
 constexpr int kWStageBytes = 2 * kStepBytes;  // one weight stage = 2 k steps
-constexpr int kMaxASlots = 16;                // A slots over both dequant warpgroups
 constexpr int kAColsPerSlot = 32;             // 64 BF16 of K per TMEM lane
 constexpr int kTmemCols = 512;
-constexpr int kGatherLag = 2;
 
 // warp roles (warp 3 idles; the warpgroups start at multiples of 4 warps so
 // that warp % 4 selects the TMEM lane quarter each warp may access)
@@ -63,31 +63,31 @@ enum Where {
 };
 
 struct Smem {
-  uint8_t* b_ring;
-  uint8_t* w_ring;
-  int* info_src;   // [2 gather warps][2 item slots][block_m]
-  int* info_dst;   // [2][2][block_m]
-  float* info_wt;  // [2][2][block_m]
-  int* info_n16;   // [2][2]
+  uint8_t* b_ring;      // [2 parities][S slots][block_m rows][128 B], 128-byte swizzle
+  uint8_t* w_ring;      // [WS stages][2 k steps][kStepBytes]
+  int* info_row;        // [2 gather warps][2 item slots][block_m]: activation row, -1 = none
+  int* info_dst;        // [2][2][block_m]: output row, -1 = not a real row
+  float* info_wt;       // [2][2][block_m]: top-k weight (down pass)
+  int* info_n16;        // [2][2]: MMA N of the item
   uint64_t* bars;
   uint32_t* tmem_base;
   volatile int* abort_flag;
 };
 
+// mbarrier addresses (shared-window offsets, 8 bytes each)
 struct Bars {
-  uint32_t w_full, w_empty, a_full, a_empty, b_full, b_empty, item_full, item_empty, acc_full,
-      acc_empty, final_bar;
-  int ws, bs;
+  uint32_t w_full, w_empty, a_full, b_full, ab_empty, item_full, item_empty, acc_full, acc_empty,
+      final_bar;
   __device__ uint32_t wf(int i) const { return w_full + 8u * i; }
   __device__ uint32_t we(int i) const { return w_empty + 8u * i; }
   __device__ uint32_t af(int i) const { return a_full + 8u * i; }
-  __device__ uint32_t ae(int i) const { return a_empty + 8u * i; }
   __device__ uint32_t bf(int i) const { return b_full + 8u * i; }
-  __device__ uint32_t be(int i) const { return b_empty + 8u * i; }
+  __device__ uint32_t abe(int i) const { return ab_empty + 8u * i; }
   __device__ uint32_t itf(int i) const { return item_full + 8u * i; }
   __device__ uint32_t ite(int i) const { return item_empty + 8u * i; }
   __device__ uint32_t accf(int i) const { return acc_full + 8u * i; }
   __device__ uint32_t acce(int i) const { return acc_empty + 8u * i; }
+  __device__ uint32_t fin(int i) const { return final_bar + 8u * i; }
 };
 
 __device__ __forceinline__ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -199,7 +199,8 @@ __device__ __forceinline__ void dequant_group(const uint4 q, uint32_t scale_bits
 
 }  // namespace
 
-__global__ void __launch_bounds__(kThreads, 1) w4a16_moe_gemm_kernel(const GemmArgs args) {
+__global__ void __launch_bounds__(kThreads, 1)
+    w4a16_moe_gemm_kernel(const __grid_constant__ GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -207,14 +208,18 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_moe_gemm_kernel(const GemmA
   // ---- shared-memory carve-up (base aligned to 1024 for the swizzle) ----
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* base = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  const int bm = args.block_m;
+  const int S = args.a_slots;  // operand ring slots per k-step parity
+  const int WS = args.w_stages;
+  const bool gather = args.gather_rows != 0;
+  const uint32_t b_slot_bytes = static_cast<uint32_t>(max_mma_n(bm, gather)) * 128u;
   Smem sm;
   size_t off = 0;
-  const int bm = args.block_m;
-  sm.b_ring = base + off;
-  off += static_cast<size_t>(args.b_stages) * bm * 128;
+  sm.b_ring = base;
+  off += static_cast<size_t>(2 * S) * b_slot_bytes;
   sm.w_ring = base + off;
-  off += static_cast<size_t>(args.w_stages) * kWStageBytes;
-  sm.info_src = reinterpret_cast<int*>(base + off);
+  off += static_cast<size_t>(WS) * kWStageBytes;
+  sm.info_row = reinterpret_cast<int*>(base + off);
   off += 4 * bm * sizeof(int);
   sm.info_dst = reinterpret_cast<int*>(base + off);
   off += 4 * bm * sizeof(int);
@@ -224,10 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_moe_gemm_kernel(const GemmA
   off += 4 * sizeof(int);
   off = align_up(off, 8);
   sm.bars = reinterpret_cast<uint64_t*>(base + off);
-  const int WS = args.w_stages, BS = args.b_stages;
-  const int SA = args.a_slots;  // A slots per dequant warpgroup
-  const int n_bars = 2 * WS + 4 * SA + 2 * BS + 2 + 2 + 2 + 2 + 2;
-  off += n_bars * 8;
+  off += (2 * WS + 6 * S + 10) * 8;
   sm.tmem_base = reinterpret_cast<uint32_t*>(base + off);
   off += 4;
   sm.abort_flag = reinterpret_cast<volatile int*>(base + off);
@@ -240,13 +242,11 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_moe_gemm_kernel(const GemmA
     B.w_empty = b0;
     b0 += 8 * WS;
     B.a_full = b0;
-    b0 += 8 * 2 * SA;
-    B.a_empty = b0;
-    b0 += 8 * 2 * SA;
+    b0 += 8 * 2 * S;
     B.b_full = b0;
-    b0 += 8 * BS;
-    B.b_empty = b0;
-    b0 += 8 * BS;
+    b0 += 8 * 2 * S;
+    B.ab_empty = b0;
+    b0 += 8 * 2 * S;
     B.item_full = b0;
     b0 += 16;
     B.item_empty = b0;
@@ -256,8 +256,6 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_moe_gemm_kernel(const GemmA
     B.acc_empty = b0;
     b0 += 16;
     B.final_bar = b0;
-    B.ws = WS;
-    B.bs = BS;
   }
 
   if (threadIdx.x == 0) {
@@ -265,22 +263,18 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_moe_gemm_kernel(const GemmA
       mbar_init(B.wf(i), 1);
       mbar_init(B.we(i), 8);  // every dequant warp releases every stage
     }
-    for (int i = 0; i < 2 * SA; ++i) {
-      mbar_init(B.af(i), 4);  // the 4 warps of the owning warpgroup
-      mbar_init(B.ae(i), 1);  // tcgen05.commit
-    }
-    for (int i = 0; i < BS; ++i) {
-      mbar_init(B.bf(i), 32);  // every lane of the owning gather warp
-      mbar_init(B.be(i), 1);   // tcgen05.commit
+    for (int i = 0; i < 2 * S; ++i) {
+      mbar_init(B.af(i), 4);   // the 4 warps of the dequant warpgroup
+      mbar_init(B.bf(i), 1);   // the gather warp's expect_tx (plus the copies' bytes)
+      mbar_init(B.abe(i), 1);  // one tcgen05.commit of the MMA issuer
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(B.itf(i), 2);  // lane 0 of each gather warp
-      mbar_init(B.ite(i), 4);
+      mbar_init(B.itf(i), 2);   // lane 0 of each gather warp
+      mbar_init(B.ite(i), 4);   // the 4 epilogue warps
       mbar_init(B.accf(i), 2);  // one tcgen05.commit per MMA issuer
       mbar_init(B.acce(i), 4);
+      mbar_init(B.fin(i), 1);
     }
-    mbar_init(B.final_bar, 1);
-    mbar_init(B.final_bar + 8, 1);
     *sm.abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -307,13 +301,18 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_moe_gemm_kernel(const GemmA
     num_blocks = args.num_experts * bpe;
   }
   const int items = num_blocks * args.n_tiles;
-  // TMEM columns: A slots first, then per accumulator slot the two partial
-  // accumulators (even / odd k steps) of d_cols columns each.
-  const int d_col_base = 2 * SA * kAColsPerSlot;
+  // TMEM columns: the 2*S A slots (32 columns each), then per accumulator
+  // slot the two partial accumulators (even / odd k steps), d_cols each.
+  const int d_col_base = 2 * S * kAColsPerSlot;
   const int n_wst = (args.k_steps + 1) / 2;
   const long long tmo = args.timeout_cycles;
   volatile int* abort_flag = sm.abort_flag;
   int* status = args.status;
+
+  // The k steps of one parity g form one pipeline: dequant warpgroup g fills
+  // the A slot (TMEM), gather warp g the B slot (shared memory) of ring slot
+  // g*S + c % S, where c counts that parity's k steps over all items; MMA
+  // issuer g consumes both and frees the slot with one tcgen05.commit.
 
   if (warp == kWarpProducer) {
     // ======================= weight producer (bulk copies) ==================
@@ -354,16 +353,14 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_moe_gemm_kernel(const GemmA
     }
   } else if (warp == kWarpMma0 || warp == kWarpMma1) {
     // ======================= MMA issuers ====================================
-    // Issuer g owns the k steps with ks % 2 == g: it consumes dequant
-    // warpgroup g's A slots and gather warp g's B stages, and accumulates into
-    // its own FP32 partial accumulator; the epilogue adds the two partials in
-    // a fixed order. At small N one issuing thread, not the tensor core, sets
-    // the pace (each tcgen05.mma blocks its issuer for tens of cycles), so two
+    // Issuer g owns the k steps with ks % 2 == g and accumulates into its own
+    // FP32 partial accumulator; the epilogue adds the two partials in a fixed
+    // order. At small N one issuing thread, not the tensor core, sets the
+    // pace (each tcgen05.mma blocks its issuer for tens of cycles), so two
     // independent issuers double the MMA rate.
     const int g = warp - kWarpMma0;
     if (lane == 0) {
-      uint32_t acnt = 0, bcnt = 0, icnt = 0, dcnt = 0;
-      const int bhalf = BS / 2;
+      uint32_t cnt = 0, icnt = 0, dcnt = 0;
       bool ok = true;
       for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
         const ItemDesc d = decode_item(args, it, num_blocks, bpe);
@@ -383,26 +380,23 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_moe_gemm_kernel(const GemmA
         tc_fence_after();
         const uint32_t idesc = idesc_bf16_m128(static_cast<uint32_t>(n16));
         const uint32_t d_tmem = tmem + d_col_base + (dslot * 2 + g) * args.d_cols;
-        for (int ks = g; ks < args.k_steps; ks += 2) {
-          const int aslot = g * SA + static_cast<int>(acnt % SA);
-          const int bslot = 2 * static_cast<int>(bcnt % bhalf) + g;
-          if (!wait_phase(B.af(aslot), (acnt / SA) & 1, abort_flag, status, kWhereMmaA, tmo) ||
-              !wait_phase(B.bf(bslot), (bcnt / bhalf) & 1, abort_flag, status, kWhereMmaB, tmo)) {
+        for (int ks = g; ks < args.k_steps; ks += 2, ++cnt) {
+          const int slot = g * S + static_cast<int>(cnt % S);
+          const uint32_t ph = (cnt / S) & 1;
+          if (!wait_phase(B.af(slot), ph, abort_flag, status, kWhereMmaA, tmo) ||
+              !wait_phase(B.bf(slot), ph, abort_flag, status, kWhereMmaB, tmo)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t b_addr = smem_u32(sm.b_ring + static_cast<size_t>(bslot) * bm * 128);
-          const uint32_t a_tmem = tmem + aslot * kAColsPerSlot;
+          const uint32_t b_addr = smem_u32(sm.b_ring + static_cast<size_t>(slot) * b_slot_bytes);
+          const uint32_t a_tmem = tmem + slot * kAColsPerSlot;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             mma_bf16_ts(d_tmem, a_tmem + kk * 8, smem_desc_sw128_kmajor(b_addr + kk * 32), idesc,
                         (ks != g || kk != 0) ? 1u : 0u);
           }
-          tc_commit(B.ae(aslot));
-          tc_commit(B.be(bslot));
-          ++acnt;
-          ++bcnt;
+          tc_commit(B.abe(slot));
         }
         if (!ok) break;
         tc_commit(B.accf(dslot));
@@ -410,21 +404,24 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_moe_gemm_kernel(const GemmA
         ++dcnt;
       }
       // every MMA issued by this thread has finished once its final barrier flips
-      tc_commit(B.final_bar + 8 * g);
+      tc_commit(B.fin(g));
       const long long t0 = clock64();
-      while (!mbar_try_wait(B.final_bar + 8 * g, 0) && clock64() - t0 < tmo) {
+      while (!mbar_try_wait(B.fin(g), 0) && clock64() - t0 < tmo) {
       }
     }
   } else if (warp >= kWarpGather0) {
-    // ======================= token gather (cp.async) ========================
-    // Gather warp gw fills the B stages of the k steps with ks % 2 == gw into
-    // its own half of the ring, and keeps its own copy of the block's row
-    // information, so the two warps never wait on each other.
-    const int gw = warp - kWarpGather0;
-    const int half = BS / 2;
-    const int lag = half > 2 ? kGatherLag : 1;
-    uint32_t bcnt = 0, icnt = 0;
-    int npend = 0;
+    // ======================= activation loads (TMA) =========================
+    // Gather warp g fills the B slots of parity g with tensor copies that
+    // write the 128-byte-swizzled K-major layout the MMA descriptor expects
+    // and count their bytes on the slot's mbarrier.
+    //  - gathered rows (indexed family): tile::gather4 puts 4 routed rows at
+    //    the start of an 8-row swizzle atom (rows 4..7 of the atom are not
+    //    used), so every copy starts 1024-byte aligned; the MMA N covers 8
+    //    columns per 4 rows and the epilogue skips the unused columns;
+    //  - consecutive rows (grouped families): one 64 x 8 box per atom.
+    const int g = warp - kWarpGather0;
+    const void* map = &args.tmap;
+    uint32_t cnt = 0, icnt = 0;
     bool ok = true;
     for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
       const ItemDesc d = decode_item(args, it, num_blocks, bpe);
@@ -433,8 +430,8 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_moe_gemm_kernel(const GemmA
       ok = __all_sync(0xffffffffu, wait_phase(B.ite(islot), ((icnt >> 1) & 1) ^ 1, abort_flag,
                                                status, kWhereGatherItem, tmo));
       if (!ok) break;
-      const int copy = gw * 2 + islot;
-      int* isrc = sm.info_src + copy * bm;
+      const int copy = g * 2 + islot;
+      int* irow = sm.info_row + copy * bm;
       int* idst = sm.info_dst + copy * bm;
       float* iwt = sm.info_wt + copy * bm;
       int maxj = -1;
@@ -442,58 +439,56 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_moe_gemm_kernel(const GemmA
         int s, dd;
         float w;
         row_info(args, d, j, s, dd, w);
-        isrc[j] = s;
+        irow[j] = s;
         idst[j] = dd;
         iwt[j] = w;
         if (dd >= 0) maxj = j;
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) maxj = max(maxj, __shfl_xor_sync(0xffffffffu, maxj, o));
-      int n16 = (maxj + 1 + 15) & ~15;
-      if (n16 == 0) n16 = 16;  // a block with no real row still runs a valid MMA
-      if (lane == 0) sm.info_n16[copy] = n16;
+      // atoms to load and the MMA N (a multiple of 16 columns)
+      const int rows_needed = max(maxj + 1, 1);
+      const int n_copies = gather ? (rows_needed + 3) / 4 : (rows_needed + 7) / 8;
+      const int n_mma = ((n_copies * 8) + 15) & ~15;
+      if (lane == 0) sm.info_n16[copy] = n_mma;
       __syncwarp();
       if (lane == 0) mbar_arrive(B.itf(islot));
-      const int chunks = n16 * 8;
-      for (int ks = gw; ks < args.k_steps; ks += 2, ++bcnt) {
-        const int bslot = 2 * (bcnt % half) + gw;
-        ok = __all_sync(0xffffffffu, wait_phase(B.be(bslot), ((bcnt / half) & 1) ^ 1, abort_flag,
-                                                 status, kWhereGatherB, tmo));
-        if (!ok) break;
-        const uint32_t stage = smem_u32(sm.b_ring + static_cast<size_t>(bslot) * bm * 128);
-        for (int idx = lane; idx < chunks; idx += 32) {
-          const int j = idx >> 3, c = idx & 7;
-          const int srow = isrc[j];
-          const int kidx = ks * kKStep + c * 8;
-          const uint32_t dst = stage + (j >> 3) * 1024 + (j & 7) * 128 + ((c ^ (j & 7)) << 4);
-          if (srow >= 0 && kidx < args.k) {
-            cp_async_16(dst, args.act + static_cast<long long>(srow) * args.k + kidx, 16);
-          } else {
-            cp_async_16(dst, args.act, 0);
-          }
-        }
-        cp_async_commit();
-        ++npend;
-        if (npend > lag) {
-          if (lag == 2) cp_async_wait<2>(); else cp_async_wait<1>();
-          fence_proxy_async_smem();
-          const uint32_t u = bcnt - lag;
-          mbar_arrive(B.bf(2 * (u % half) + gw));
-          --npend;
+      // per-lane copy coordinates, fixed for the item
+      int r0 = args.act_rows, r1 = args.act_rows, r2 = args.act_rows, r3 = args.act_rows;
+      if (lane < n_copies) {
+        if (gather) {
+          const int j = 4 * lane;
+          r0 = irow[j] >= 0 ? irow[j] : args.act_rows;
+          r1 = (j + 1 < bm && irow[j + 1] >= 0) ? irow[j + 1] : args.act_rows;
+          r2 = (j + 2 < bm && irow[j + 2] >= 0) ? irow[j + 2] : args.act_rows;
+          r3 = (j + 3 < bm && irow[j + 3] >= 0) ? irow[j + 3] : args.act_rows;
+        } else {
+          // first row of this atom in the activation tensor (consecutive rows)
+          r0 = (args.family == kContiguous) ? d.blk * bm + 8 * lane
+                                            : d.e * args.m + (d.blk - d.e * bpe) * bm + 8 * lane;
         }
       }
-      // Flush at the end of every item: the next item's stages may wait on
-      // this item's epilogue, which waits on these stages.
-      cp_async_wait<0>();
-      fence_proxy_async_smem();
-      for (; npend > 0; --npend) {
-        const uint32_t u = bcnt - npend;
-        mbar_arrive(B.bf(2 * (u % half) + gw));
+      const uint32_t copy_bytes = gather ? 512u : 1024u;
+      for (int ks = g; ks < args.k_steps; ks += 2, ++cnt) {
+        const int slot = g * S + static_cast<int>(cnt % S);
+        ok = __all_sync(0xffffffffu, wait_phase(B.abe(slot), ((cnt / S) & 1) ^ 1, abort_flag,
+                                                 status, kWhereGatherB, tmo));
+        if (!ok) break;
+        if (lane == 0) mbar_arrive_expect_tx(B.bf(slot), n_copies * copy_bytes);
+        __syncwarp();
+        if (lane < n_copies) {
+          const uint32_t dst =
+              smem_u32(sm.b_ring + static_cast<size_t>(slot) * b_slot_bytes) + lane * 1024u;
+          if (gather) {
+            tma_gather4(dst, map, ks * kKStep, r0, r1, r2, r3, B.bf(slot));
+          } else {
+            tma_load_2d(dst, map, ks * kKStep, r0, B.bf(slot));
+          }
+        }
       }
       if (!ok) break;
       ++icnt;
     }
-    cp_async_wait<0>();
   } else if (warp >= kWarpDequant0 && warp < kWarpEpilogue0) {
     // ======================= dequantisation into TMEM =======================
     // Warpgroup g dequantises the k steps with ks % 2 == g; thread r of the
@@ -502,49 +497,50 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_moe_gemm_kernel(const GemmA
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    uint32_t wcnt = 0, acnt = 0;
+    uint32_t wcnt = 0, cnt = 0;
     bool ok = true;
     for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
       const ItemDesc d = decode_item(args, it, num_blocks, bpe);
       if (d.e < 0) continue;
       for (int st = 0; st < n_wst; ++st, ++wcnt) {
-        const int slot = wcnt % WS;
-        ok = __all_sync(0xffffffffu, wait_phase(B.wf(slot), (wcnt / WS) & 1, abort_flag, status,
+        const int wslot = wcnt % WS;
+        ok = __all_sync(0xffffffffu, wait_phase(B.wf(wslot), (wcnt / WS) & 1, abort_flag, status,
                                                  kWhereDequantW, tmo));
         if (!ok) break;
         const int ks = 2 * st + g;
         if (ks >= args.k_steps) {
           __syncwarp();
-          if (lane == 0) mbar_arrive(B.we(slot));
+          if (lane == 0) mbar_arrive(B.we(wslot));
           continue;
         }
-        const uint8_t* stp = sm.w_ring + static_cast<size_t>(slot) * kWStageBytes + g * kStepBytes;
+        const uint8_t* stp = sm.w_ring + static_cast<size_t>(wslot) * kWStageBytes + g * kStepBytes;
         const uint4 q0 = *reinterpret_cast<const uint4*>(stp + r * 16);
         const uint4 q1 = *reinterpret_cast<const uint4*>(stp + 2048 + r * 16);
         const uint32_t s0 = *reinterpret_cast<const uint16_t*>(stp + kStepQBytes + r * 2);
         const uint32_t s1 = *reinterpret_cast<const uint16_t*>(stp + kStepQBytes + 256 + r * 2);
         __syncwarp();
-        if (lane == 0) mbar_arrive(B.we(slot));
+        if (lane == 0) mbar_arrive(B.we(wslot));
         uint32_t v[32];
         dequant_group(q0, s0, v);
         dequant_group(q1, s1, v + 16);
-        const int aslot = g * SA + static_cast<int>(acnt % SA);
-        ok = __all_sync(0xffffffffu, wait_phase(B.ae(aslot), ((acnt / SA) & 1) ^ 1, abort_flag,
+        const int slot = g * S + static_cast<int>(cnt % S);
+        ok = __all_sync(0xffffffffu, wait_phase(B.abe(slot), ((cnt / S) & 1) ^ 1, abort_flag,
                                                  status, kWhereDequantA, tmo));
         if (!ok) break;
         tc_fence_after();
-        tmem_st_32x32b_x32(tmem + lane_base + aslot * kAColsPerSlot, v);
+        tmem_st_32x32b_x32(tmem + lane_base + slot * kAColsPerSlot, v);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(B.af(aslot));
-        ++acnt;
+        if (lane == 0) mbar_arrive(B.af(slot));
+        ++cnt;
       }
     }
   } else if (warp >= kWarpEpilogue0) {
     // ======================= epilogue =======================================
     // Thread r owns weight row r of the tile (TMEM lane r): it reads the
-    // block's token columns and writes output column tile*128 + r.
+    // block's token columns of both partial accumulators and writes output
+    // column tile*128 + r.
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
@@ -575,13 +571,21 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_moe_gemm_kernel(const GemmA
         if (!row_ok) continue;
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) {
-          const int dr = idst[j0 + jj];
+          // MMA column -> block row (gathered rows use 4 of every 8 columns)
+          const int c = j0 + jj;
+          int j = c;
+          if (gather) {
+            if ((c & 7) >= 4) continue;
+            j = (c >> 3) * 4 + (c & 3);
+          }
+          if (j >= bm) continue;
+          const int dr = idst[j];
           if (dr < 0) continue;
           const float x = odd_steps ? __uint_as_float(v[jj]) + __uint_as_float(w[jj])
                                     : __uint_as_float(v[jj]);
           if (args.out_mode == kOutF32WeightedAdd) {
             float* o = static_cast<float*>(args.out) + static_cast<long long>(dr) * args.n + ng;
-            atomicAdd(o, iwt[j0 + jj] * x);
+            atomicAdd(o, iwt[j] * x);
           } else {
             __nv_bfloat16* o =
                 static_cast<__nv_bfloat16*>(args.out) + static_cast<long long>(dr) * args.n + ng;
@@ -610,15 +614,38 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_moe_gemm_kernel(const GemmA
   }
 }
 
-size_t gemm_smem_bytes(int block_m, int w_stages, int b_stages) {
+size_t gemm_smem_bytes(int block_m, bool gather, int w_stages, int ring_slots) {
   size_t off = 1024;  // alignment slack
-  off += static_cast<size_t>(b_stages) * block_m * 128;
+  off += static_cast<size_t>(2 * ring_slots) * max_mma_n(block_m, gather) * 128;
   off += static_cast<size_t>(w_stages) * kWStageBytes;
-  off += 3 * 4 * static_cast<size_t>(block_m) * 4 + 4 * 4;
+  off += 4 * static_cast<size_t>(block_m) * (4 + 4 + 4) + 4 * 4;
   off = (off + 7) / 8 * 8;
-  off += (2 * w_stages + 2 * kMaxASlots + 2 * b_stages + 10) * 8;
+  off += (2 * w_stages + 6 * ring_slots + 10) * 8;
   off += 8;
   return off;
+}
+
+bool encode_act_tmap(CUtensorMap* map, const void* act, long long rows, int k, int box_rows) {
+  using EncodeFn = PFN_cuTensorMapEncodeTiled_v12000;
+  static EncodeFn encode = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      encode = reinterpret_cast<EncodeFn>(fn);
+  });
+  if (encode == nullptr || rows <= 0 || rows > (1LL << 31) || k <= 0) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(k) * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kKStep), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(act), dims, strides,
+                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
 }
 
 int device_sm_count(int device) {
@@ -637,7 +664,7 @@ int device_sm_count(int device) {
 cudaError_t launch_moe_gemm(const GemmArgs& args, int grid, cudaStream_t stream) {
   // At least 118 KB so that two CTAs never share an SM: each CTA allocates
   // all 512 TMEM columns.
-  size_t smem = gemm_smem_bytes(args.block_m, args.w_stages, args.b_stages);
+  size_t smem = gemm_smem_bytes(args.block_m, args.gather_rows != 0, args.w_stages, args.a_slots);
   if (smem < 118 * 1024) smem = 118 * 1024;
   cudaError_t err = cudaFuncSetAttribute(w4a16_moe_gemm_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -63,6 +63,31 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
+// ------------------------------------------------ tensor copies (TMA) ---
+
+// Four rows (given by their row coordinates) of a 2-D tensor map whose box
+// is one row high, written as four consecutive rows at `dst` with the map's
+// swizzle; completion counted in bytes on `bar`. Out-of-range rows read the
+// fill value (zero).
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* map, int col, int r0, int r1,
+                                            int r2, int r3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(map), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
+      : "memory");
+}
+
+// One box of a 2-D tensor map at (col, row).
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* map, int col, int row,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(map), "r"(col), "r"(row), "r"(bar)
+      : "memory");
+}
+
 // ---------------------------------------------------- cp.async (gather) ---
 
 // 16-byte copy; src_bytes == 0 writes 16 zero bytes and reads nothing.
