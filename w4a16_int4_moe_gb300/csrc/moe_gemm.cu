@@ -96,10 +96,11 @@ __device__ __forceinline__ size_t align_up(size_t x, size_t a) { return (x + a -
 // when the CTA is aborting or this wait ran out (then it starts the abort).
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                         int* status, int where, long long timeout) {
-  if (mbar_try_wait(bar, parity)) return true;
+  constexpr uint32_t kSuspendNs = 1000000;  // the thread sleeps until completion or 1 ms
+  if (mbar_try_wait_sleep(bar, parity, kSuspendNs)) return true;
   const long long t0 = clock64();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, kSuspendNs)) return true;
     if (*abort_flag) return false;
     if (clock64() - t0 > timeout) {
       *abort_flag = 1;
@@ -108,6 +109,19 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
     }
   }
 }
+
+// Position in a ring of mbarrier-guarded slots: slot index and the parity of
+// the slot's current phase (incremented without divisions).
+struct RingPos {
+  int slot = 0;
+  uint32_t phase = 0;
+  __device__ __forceinline__ void next(int n) {
+    if (++slot == n) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+};
 
 struct ItemDesc {
   int blk, tile, e;
@@ -319,24 +333,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint64_t policy = policy_evict_first();
       uint32_t wcnt = 0;
+      RingPos wp;
       bool ok = true;
       for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
         const ItemDesc d = decode_item(args, it, num_blocks, bpe);
         if (d.e < 0) continue;
         const uint8_t* src = args.wpack + static_cast<long long>(d.e) * args.expert_bytes +
                              static_cast<long long>(d.tile) * args.k_steps * kStepBytes;
-        for (int st = 0; st < n_wst; ++st, ++wcnt) {
-          const int slot = wcnt % WS;
-          const uint32_t ph = (wcnt / WS) & 1;
-          if (!wait_phase(B.we(slot), ph ^ 1, abort_flag, status, kWhereProducer, tmo)) {
+        for (int st = 0; st < n_wst; ++st, ++wcnt, wp.next(WS)) {
+          if (!wait_phase(B.we(wp.slot), wp.phase ^ 1, abort_flag, status, kWhereProducer, tmo)) {
             ok = false;
             break;
           }
           const int nks = min(2, args.k_steps - 2 * st);
           const uint32_t bytes = static_cast<uint32_t>(nks * kStepBytes);
-          mbar_arrive_expect_tx(B.wf(slot), bytes);
-          bulk_g2s(smem_u32(sm.w_ring + static_cast<size_t>(slot) * kWStageBytes),
-                   src + static_cast<long long>(st) * kWStageBytes, bytes, B.wf(slot), policy);
+          mbar_arrive_expect_tx(B.wf(wp.slot), bytes);
+          bulk_g2s(smem_u32(sm.w_ring + static_cast<size_t>(wp.slot) * kWStageBytes),
+                   src + static_cast<long long>(st) * kWStageBytes, bytes, B.wf(wp.slot), policy);
         }
       }
       if (!ok) {
@@ -360,48 +373,50 @@ __global__ void __launch_bounds__(kThreads, 1)
     // independent issuers double the MMA rate.
     const int g = warp - kWarpMma0;
     if (lane == 0) {
-      uint32_t cnt = 0, icnt = 0, dcnt = 0;
+      RingPos rp, ip, dp;
       bool ok = true;
+      // descriptor of ring slot 0 of this parity; later slots add their offset
+      const uint64_t b_desc0 =
+          smem_desc_sw128_kmajor(smem_u32(sm.b_ring + static_cast<size_t>(g * S) * b_slot_bytes));
+      const uint32_t b_slot_step = b_slot_bytes >> 4;  // in descriptor address units
       for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
         const ItemDesc d = decode_item(args, it, num_blocks, bpe);
         if (d.e < 0) continue;
-        const int islot = icnt & 1;
-        if (!wait_phase(B.itf(islot), (icnt >> 1) & 1, abort_flag, status, kWhereMmaItem, tmo)) {
+        if (!wait_phase(B.itf(ip.slot), ip.phase, abort_flag, status, kWhereMmaItem, tmo)) {
           ok = false;
           break;
         }
-        const int n16 = sm.info_n16[islot];  // gather warp 0's copy
-        const int dslot = dcnt % args.d_slots;
-        if (!wait_phase(B.acce(dslot), ((dcnt / args.d_slots) & 1) ^ 1, abort_flag, status,
-                        kWhereMmaAcc, tmo)) {
+        const int n16 = sm.info_n16[ip.slot];  // gather warp 0's copy
+        if (!wait_phase(B.acce(dp.slot), dp.phase ^ 1, abort_flag, status, kWhereMmaAcc, tmo)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t idesc = idesc_bf16_m128(static_cast<uint32_t>(n16));
-        const uint32_t d_tmem = tmem + d_col_base + (dslot * 2 + g) * args.d_cols;
-        for (int ks = g; ks < args.k_steps; ks += 2, ++cnt) {
-          const int slot = g * S + static_cast<int>(cnt % S);
-          const uint32_t ph = (cnt / S) & 1;
-          if (!wait_phase(B.af(slot), ph, abort_flag, status, kWhereMmaA, tmo) ||
-              !wait_phase(B.bf(slot), ph, abort_flag, status, kWhereMmaB, tmo)) {
+        const uint32_t d_tmem = tmem + d_col_base + (dp.slot * 2 + g) * args.d_cols;
+        uint32_t acc = 0;
+        for (int ks = g; ks < args.k_steps; ks += 2, rp.next(S)) {
+          const int slot = g * S + rp.slot;
+          if (!wait_phase(B.af(slot), rp.phase, abort_flag, status, kWhereMmaA, tmo) ||
+              !wait_phase(B.bf(slot), rp.phase, abort_flag, status, kWhereMmaB, tmo)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t b_addr = smem_u32(sm.b_ring + static_cast<size_t>(slot) * b_slot_bytes);
+          const uint64_t b_desc = b_desc0 + static_cast<uint64_t>(rp.slot) * b_slot_step;
           const uint32_t a_tmem = tmem + slot * kAColsPerSlot;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            mma_bf16_ts(d_tmem, a_tmem + kk * 8, smem_desc_sw128_kmajor(b_addr + kk * 32), idesc,
-                        (ks != g || kk != 0) ? 1u : 0u);
+            // +32 bytes of K per MMA inside the 128-byte swizzle row
+            mma_bf16_ts(d_tmem, a_tmem + kk * 8, b_desc + 2 * kk, idesc, acc);
+            acc = 1;
           }
           tc_commit(B.abe(slot));
         }
         if (!ok) break;
-        tc_commit(B.accf(dslot));
-        ++icnt;
-        ++dcnt;
+        tc_commit(B.accf(dp.slot));
+        ip.next(2);
+        dp.next(args.d_slots);
       }
       // every MMA issued by this thread has finished once its final barrier flips
       tc_commit(B.fin(g));
@@ -421,14 +436,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     //  - consecutive rows (grouped families): one 64 x 8 box per atom.
     const int g = warp - kWarpGather0;
     const void* map = &args.tmap;
-    uint32_t cnt = 0, icnt = 0;
+    RingPos rp, ip;
     bool ok = true;
     for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
       const ItemDesc d = decode_item(args, it, num_blocks, bpe);
       if (d.e < 0) continue;
-      const int islot = icnt & 1;
-      ok = __all_sync(0xffffffffu, wait_phase(B.ite(islot), ((icnt >> 1) & 1) ^ 1, abort_flag,
-                                               status, kWhereGatherItem, tmo));
+      const int islot = ip.slot;
+      ok = __all_sync(0xffffffffu, wait_phase(B.ite(islot), ip.phase ^ 1, abort_flag, status,
+                                               kWhereGatherItem, tmo));
       if (!ok) break;
       const int copy = g * 2 + islot;
       int* irow = sm.info_row + copy * bm;
@@ -469,10 +484,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const uint32_t copy_bytes = gather ? 512u : 1024u;
-      for (int ks = g; ks < args.k_steps; ks += 2, ++cnt) {
-        const int slot = g * S + static_cast<int>(cnt % S);
-        ok = __all_sync(0xffffffffu, wait_phase(B.abe(slot), ((cnt / S) & 1) ^ 1, abort_flag,
-                                                 status, kWhereGatherB, tmo));
+      for (int ks = g; ks < args.k_steps; ks += 2, rp.next(S)) {
+        const int slot = g * S + rp.slot;
+        ok = __all_sync(0xffffffffu, wait_phase(B.abe(slot), rp.phase ^ 1, abort_flag, status,
+                                                 kWhereGatherB, tmo));
         if (!ok) break;
         if (lane == 0) mbar_arrive_expect_tx(B.bf(slot), n_copies * copy_bytes);
         __syncwarp();
@@ -487,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
-      ++icnt;
+      ip.next(2);
     }
   } else if (warp >= kWarpDequant0 && warp < kWarpEpilogue0) {
     // ======================= dequantisation into TMEM =======================
@@ -497,14 +512,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    uint32_t wcnt = 0, cnt = 0;
+    RingPos wp, rp;
     bool ok = true;
     for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
       const ItemDesc d = decode_item(args, it, num_blocks, bpe);
       if (d.e < 0) continue;
-      for (int st = 0; st < n_wst; ++st, ++wcnt) {
-        const int wslot = wcnt % WS;
-        ok = __all_sync(0xffffffffu, wait_phase(B.wf(wslot), (wcnt / WS) & 1, abort_flag, status,
+      for (int st = 0; st < n_wst; ++st, wp.next(WS)) {
+        const int wslot = wp.slot;
+        ok = __all_sync(0xffffffffu, wait_phase(B.wf(wslot), wp.phase, abort_flag, status,
                                                  kWhereDequantW, tmo));
         if (!ok) break;
         const int ks = 2 * st + g;
@@ -523,9 +538,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t v[32];
         dequant_group(q0, s0, v);
         dequant_group(q1, s1, v + 16);
-        const int slot = g * S + static_cast<int>(cnt % S);
-        ok = __all_sync(0xffffffffu, wait_phase(B.abe(slot), ((cnt / S) & 1) ^ 1, abort_flag,
-                                                 status, kWhereDequantA, tmo));
+        const int slot = g * S + rp.slot;
+        ok = __all_sync(0xffffffffu, wait_phase(B.abe(slot), rp.phase ^ 1, abort_flag, status,
+                                                 kWhereDequantA, tmo));
         if (!ok) break;
         tc_fence_after();
         tmem_st_32x32b_x32(tmem + lane_base + slot * kAColsPerSlot, v);
@@ -533,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(B.af(slot));
-        ++cnt;
+        rp.next(S);
       }
     }
   } else if (warp >= kWarpEpilogue0) {
@@ -544,15 +559,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    uint32_t icnt = 0, dcnt = 0;
+    RingPos ip, dp;
     for (int it = blockIdx.x; it < items; it += gridDim.x) {
       const ItemDesc d = decode_item(args, it, num_blocks, bpe);
       if (d.e < 0) continue;
-      const int islot = icnt & 1;
-      const int dslot = dcnt % args.d_slots;
-      bool ok = wait_phase(B.accf(dslot), (dcnt / args.d_slots) & 1, abort_flag, status,
-                           kWhereEpiAcc, tmo) &&
-                wait_phase(B.itf(islot), (icnt >> 1) & 1, abort_flag, status, kWhereEpiItem, tmo);
+      const int islot = ip.slot;
+      const int dslot = dp.slot;
+      bool ok = wait_phase(B.accf(dslot), dp.phase, abort_flag, status, kWhereEpiAcc, tmo) &&
+                wait_phase(B.itf(islot), ip.phase, abort_flag, status, kWhereEpiItem, tmo);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       const int n16 = sm.info_n16[islot];  // gather warp 0's copy
@@ -599,8 +613,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(B.acce(dslot));
         mbar_arrive(B.ite(islot));
       }
-      ++icnt;
-      ++dcnt;
+      ip.next(2);
+      dp.next(args.d_slots);
     }
   }
 
