@@ -16,7 +16,7 @@ weight stream (1.19 GB at the EP8 decode shard) is larger than L2 anyway.
 on a bounded sample of the same workload scaled to a whole layer.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                       [--workload ep8_decode|tp8_16|tp8_64|tp8_256|ep8_prefill|tiny]
+                       [--workload ep8_decode|ep8_decode_e12|tp8_16|tp8_64|tp8_256|ep8_prefill|tiny]
 """
 
 from __future__ import annotations
@@ -45,6 +45,10 @@ def make_workload(name):
     from w4a16_int4_moe_gb300 import workloads as wl
     if name == "ep8_decode":
         return wl.ep8_decode()
+    if name == "ep8_decode_e12":
+        # a quarter of the EP8 decode shard (12 experts, 144 rows): the size
+        # that detailed profiler captures run on
+        return wl.ep8_decode(tokens=144, local_experts=12)
     if name.startswith("tp8_"):
         return wl.tp8(int(name.split("_")[1]))
     if name == "ep8_prefill":
@@ -99,13 +103,16 @@ def traffic_record(kernel_file, workload):
 
 
 class ClockSampler:
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples every 20 ms; only the samples whose timestamps fall
+    inside the timed region are summarised."""
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self):
         self.proc = None
         self.path = os.path.join(ROOT, "gpurun_out", "clocks_bench.csv")
+        self.window = None
 
     def start(self):
         try:
@@ -113,10 +120,21 @@ class ClockSampler:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
-                 "-lms", "100", "-i", os.environ.get("LOCAL_RANK", "0")],
+                 "-lms", "20", "-i", os.environ.get("LOCAL_RANK", "0")],
                 stdout=self.fh, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+            return
+        # wait (at most 3 s) for the first sample so that the timed region is covered
+        t_end = time.time() + 3.0
+        while time.time() < t_end:
+            self.fh.flush()
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.05)
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
 
     def stop(self):
         if self.proc is None:
@@ -127,25 +145,33 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.fh.close()
-        sms, maxes, reasons = [], [], set()
+        import datetime
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        samples = []
         with open(self.path) as f:
             for line in f:
                 parts = [x.strip() for x in line.split(",")]
-                if len(parts) < 9:
+                if len(parts) < 10:
                     continue
                 try:
-                    sms.append(float(parts[1]))
-                    maxes.append(float(parts[2]))
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    sm, mx = float(parts[2]), float(parts[3])
                 except ValueError:
                     continue
-                for name, val in zip(names, parts[5:9]):
-                    if val.lower() == "active":
-                        reasons.add(name)
-        if not sms:
+                active = [n for n, v in zip(names, parts[6:10]) if v.lower() == "active"]
+                samples.append((ts, sm, mx, active))
+        if not samples:
             return None
-        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes),
-                "reasons": sorted(reasons), "samples": len(sms)}
+        inside = samples
+        if self.window is not None:
+            t0, t1 = self.window
+            sel = [x for x in samples if t0 - 0.025 <= x[0] <= t1 + 0.025]
+            if sel:
+                inside = sel
+        reasons = sorted({r for x in inside for r in x[3]})
+        return {"sm_mhz": statistics.median(x[1] for x in inside),
+                "sm_max_mhz": max(x[2] for x in inside), "reasons": reasons,
+                "samples": len(inside), "samples_total": len(samples)}
 
 
 def cpu_oracle_sample(p, n_experts_sample=None):
@@ -157,7 +183,7 @@ def cpu_oracle_sample(p, n_experts_sample=None):
     local = (flat >= 0) & (flat < p.num_experts)
     active = np.unique(flat[local])
     if n_experts_sample is None:
-        n_experts_sample = max(1, min(active.size, 8))
+        n_experts_sample = active.size
     rng = np.random.default_rng(0)
     chosen = np.sort(rng.choice(active, size=n_experts_sample, replace=False))
     sub_ids = np.where(np.isin(p.topk_ids, chosen), p.topk_ids, -1)
@@ -261,6 +287,8 @@ def run_ours(args):
         if ev is not None:
             ev[3].record(stream)
 
+    clocks = ClockSampler()
+    clocks.start()
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -269,8 +297,6 @@ def run_ours(args):
         raise SystemExit(f"device status {word:#x} after warm-up")
 
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    clocks = ClockSampler()
-    clocks.start()
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
@@ -279,6 +305,8 @@ def run_ours(args):
         step(events[i])
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
+    t_end_wall = time.time()
+    clocks.mark(t_end_wall - wall, t_end_wall)
     if dist is not None:
         dist.barrier()
     clk = clocks.stop()
@@ -371,8 +399,8 @@ def run_ours(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="ep8_decode")
     ap.add_argument("--ref-experts", type=int, default=2,
