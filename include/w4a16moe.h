@@ -82,8 +82,10 @@ typedef struct {
                       largest MMA N of one work item (16..128, step 16)   */
   int bn;          /* weight rows per tile (MMA M) = 128                  */
   int bk;          /* K elements per pipeline step = 64                   */
-  int stages;      /* weight ring depth, in pairs of K steps (2..16)      */
-  int b_stages;    /* activation ring depth (2..16)                       */
+  int stages;      /* weight ring depth, in stages of 2 K steps (4..16;
+                      rounded down to a multiple of 4)                    */
+  int b_stages;    /* activation ring depth in K steps (8..32, a multiple
+                      of 4)                                               */
   int split_k;     /* 1 (no split of K)                                   */
   int ctas_per_sm; /* 1 (persistent, one CTA per SM)                      */
   int swap_ab;     /* 1: weights are the MMA M operand, tokens the N one  */
@@ -159,11 +161,17 @@ w4a16_status w4a16_unpack(const void* packed, int num_experts, int n, int k, uin
                           uint16_t* scales, void* stream);
 
 /*
- * Device workspace bytes for a GEMM call under `plan` (at least 256: the
- * device status words). The caller zero-fills a new workspace once; the
- * library keeps it zero except when a device-side wait gives up.
+ * Device workspace bytes for a GEMM call under `plan`.
+ *   rows: the routing capacity (rows of sorted_ids) of an indexed GEMM, or 0
+ *         for a grouped GEMM;
+ *   k:    the GEMM's reduction length (columns of its activation rows).
+ * Layout: 256 bytes of device status words, then (indexed GEMM) the routed
+ * activation rows copied into routing order, rows x roundup(k, 64) BF16.
+ * The caller zero-fills a new workspace once; the library keeps the status
+ * words zero except when a device-side wait gives up. One workspace serves
+ * calls that are ordered on one stream.
  */
-size_t w4a16_workspace_size(const w4a16_plan_t* plan, int rows, int n);
+size_t w4a16_workspace_size(const w4a16_plan_t* plan, int rows, int k);
 
 /*
  * Indexed W4A16 MoE GEMM ([P-arex] "调度由每个专家收到的 token 数决定",
@@ -184,8 +192,10 @@ size_t w4a16_workspace_size(const w4a16_plan_t* plan, int rows, int n);
  * not depend on their contents. Blocks with expert -1 and sentinel rows are
  * skipped; ids out of range are ignored, never dereferenced.
  * Requires: k % 32 == 0, n >= 1, plan from w4a16_plan (block_m equal to the
- * align block size, 16..128 step 16), workspace >= w4a16_workspace_size,
- * a, out 16-byte aligned.
+ * align block size, 16..128 step 16), ws_bytes >=
+ * w4a16_workspace_size(plan, capacity, k), a, out 16-byte aligned.
+ * The call first copies the routed rows of `a` into routing order in the
+ * workspace (one extra kernel on `stream`), then runs the GEMM on them.
  */
 w4a16_status w4a16_moe_indexed_gemm(int mode, const void* packed, int num_experts, int n, int k,
                                     const uint16_t* a, int tokens, int topk,
@@ -240,12 +250,13 @@ w4a16_status w4a16_read_device_status(void* workspace, int* detail, void* stream
  * and take a global lock), or a plugin interface that passes only the
  * operation's tensors.
  * Same arguments and results as w4a16_moe_indexed_gemm, without the
- * workspace: the library uses a fixed 64 KiB array of device memory compiled
+ * workspace: the library uses a fixed 32 MiB array of device memory compiled
  * into it, which every GPU that loads the library holds until the process
  * exits. The call allocates nothing. The caller still provides every input
  * and output buffer.
- * - Returns W4A16_ERR_WORKSPACE if w4a16_workspace_size(plan, ...) exceeds
- *   64 KiB.
+ * - Returns W4A16_ERR_WORKSPACE if w4a16_workspace_size(plan, capacity, k)
+ *   exceeds 32 MiB (for k = 7168 that is a routing capacity above 2340
+ *   rows).
  * - The first call on each device looks up the array's device address
  *   (cudaGetSymbolAddress, with that device current); make that first call
  *   before any stream capture begins.

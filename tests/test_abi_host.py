@@ -57,7 +57,8 @@ def test_plan_follows_tok_e(lib):
     for tok_e in (0.3, 5, 12, 40, 80, 81, 150, 400):
         p = ops.w4a16_plan(1024, 8, 48, 4096, 7168, float(tok_e))
         assert 16 <= p.block_m <= 64 and p.block_m % 16 == 0
-        assert 2 <= p.stages <= 16 and p.b_stages % 2 == 0 and p.split_k == 1
+        assert 4 <= p.stages <= 16 and p.stages % 4 == 0 and p.split_k == 1
+        assert 8 <= p.b_stages <= 32 and p.b_stages % 4 == 0
 
 
 def test_plan_rejects_bad_sizes(lib):
@@ -84,7 +85,7 @@ def test_gemm_argument_checks_before_any_launch(lib):
     fake = ctypes.c_void_p(1 << 20)   # never dereferenced: checks fail first
     args = dict(mode=ops.W4A16_GATE_UP, packed=fake, E=8, n=1024, k=512, a=fake, tokens=64,
                 topk=2, sid=fake, eid=fake, ntp=fake, cap=256, w=None, out=fake, flags=0,
-                ws=fake, wsb=256)
+                ws=fake, wsb=1 << 30)
 
     def call(**kw):
         a = dict(args, **kw)
@@ -97,28 +98,35 @@ def test_gemm_argument_checks_before_any_launch(lib):
     assert call(mode=ops.W4A16_DOWN) == ops.W4A16_ERR_INVALID_ARG  # no top-k weights
     assert call(ws=None) == ops.W4A16_ERR_WORKSPACE
     assert call(wsb=16) == ops.W4A16_ERR_WORKSPACE
+    # the workspace holds the routed rows: 256 status bytes + cap x roundup(k, 64) BF16
+    need = ops.w4a16_workspace_size(plan, 256, 512)
+    assert need == 256 + 256 * 512 * 2
+    assert ops.w4a16_workspace_size(plan, 256, 480) == 256 + 256 * 512 * 2
+    assert ops.w4a16_workspace_size(plan, 0, 512) == 256
+    assert call(wsb=need - 1) == ops.W4A16_ERR_WORKSPACE
     assert call(cap=250) == ops.W4A16_ERR_INVALID_ARG          # not a multiple of block_m
     assert call(flags=64) == ops.W4A16_ERR_INVALID_ARG
     assert call(out=ctypes.c_void_p((1 << 20) + 2)) == ops.W4A16_ERR_INVALID_ARG  # misaligned
     bad = ops.Plan.from_buffer_copy(plan)
     bad.block_m = 24
     assert lib.w4a16_moe_indexed_gemm(0, fake, 8, 1024, 512, fake, 64, 2, fake, fake, fake, 240,
-                                      None, fake, 0, ctypes.byref(bad), fake, 256, None) \
-        == ops.W4A16_ERR_INVALID_ARG
-    bad = ops.Plan.from_buffer_copy(plan)
-    bad.block_m = 128   # gathered rows: at most 64 rows per block (half-filled 8-row atoms)
-    assert lib.w4a16_moe_indexed_gemm(0, fake, 8, 1024, 512, fake, 64, 2, fake, fake, fake, 256,
-                                      None, fake, 0, ctypes.byref(bad), fake, 256, None) \
+                                      None, fake, 0, ctypes.byref(bad), fake, 1 << 30, None) \
         == ops.W4A16_ERR_INVALID_ARG
     bad = ops.Plan.from_buffer_copy(plan)
     bad.block_m = 144   # above the largest block (two partial accumulators must fit in TMEM)
     assert lib.w4a16_moe_indexed_gemm(0, fake, 8, 1024, 512, fake, 64, 2, fake, fake, fake, 288,
-                                      None, fake, 0, ctypes.byref(bad), fake, 256, None) \
+                                      None, fake, 0, ctypes.byref(bad), fake, 1 << 30, None) \
         == ops.W4A16_ERR_INVALID_ARG
+    for field, value in (("stages", 3), ("stages", 17), ("b_stages", 6), ("b_stages", 10)):
+        bad = ops.Plan.from_buffer_copy(plan)
+        setattr(bad, field, value)   # weight ring below one stage per warpgroup; odd B stages
+        assert lib.w4a16_moe_indexed_gemm(0, fake, 8, 1024, 512, fake, 64, 2, fake, fake, fake,
+                                          256, None, fake, 0, ctypes.byref(bad), fake, 1 << 30,
+                                          None) == ops.W4A16_ERR_INVALID_ARG, field
     bad = ops.Plan.from_buffer_copy(plan)
     bad.split_k = 2
     assert lib.w4a16_moe_indexed_gemm(0, fake, 8, 1024, 512, fake, 64, 2, fake, fake, fake, 256,
-                                      None, fake, 0, ctypes.byref(bad), fake, 256, None) \
+                                      None, fake, 0, ctypes.byref(bad), fake, 1 << 30, None) \
         == ops.W4A16_ERR_INVALID_ARG
 
 

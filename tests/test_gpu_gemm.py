@@ -36,7 +36,7 @@ def _routing(ids, experts, bm, device):
 def _plan(bm, n, k, stages=None, b_stages=None, grid=0):
     p = ops.w4a16_plan(64, 1, 1, n, k, float(bm))
     p.block_m = bm
-    p.b_stages = b_stages or (8 if bm <= 32 else (6 if bm <= 64 else 4))
+    p.b_stages = b_stages or 8
     p.stages = stages or min(p.stages, 8)
     p.grid = grid
     return p
@@ -44,7 +44,7 @@ def _plan(bm, n, k, stages=None, b_stages=None, grid=0):
 
 def _gate_up(p, packed, routing, plan, device):
     sid, eid, ntp = routing
-    ws = ops.new_workspace(plan, device)
+    ws = ops.new_workspace(plan, device, sid.numel(), p.hidden)
     x = bf16_tensor(p.x, device)
     out = torch.full((p.numel, 2 * p.inter), float("nan"), dtype=torch.bfloat16, device=device)
     ops.w4a16_moe_indexed_gemm(ops.W4A16_GATE_UP, packed, p.num_experts, 2 * p.inter, p.hidden,
@@ -56,7 +56,7 @@ def _gate_up(p, packed, routing, plan, device):
 
 def _down(p, packed, routing, plan, act_bits, device):
     sid, eid, ntp = routing
-    ws = ops.new_workspace(plan, device)
+    ws = ops.new_workspace(plan, device, sid.numel(), p.inter)
     a = bf16_tensor(act_bits, device)
     w = dev(p.topk_weights, device)
     out = torch.full((p.tokens, p.hidden), float("nan"), dtype=torch.float32, device=device)
@@ -156,8 +156,8 @@ def test_schedules_are_bitwise_identical(cuda_dev):
     p = wl.uniform_problem(96, 512, 256, 8, 2, seed=8)
     pk = _pack(p.q_gu, p.s_gu, cuda_dev)
     ref = None
-    for bm, st, bst, grid in [(16, 8, 8, 0), (32, 4, 4, 0), (64, 8, 6, 3), (64, 2, 4, 1),
-                              (16, 3, 12, 5), (48, 5, 10, 7)]:
+    for bm, st, bst, grid in [(16, 8, 8, 0), (32, 4, 16, 0), (64, 8, 8, 3), (64, 4, 12, 1),
+                              (16, 12, 12, 5), (48, 7, 8, 7)]:
         routing = _routing(p.topk_ids, p.num_experts, bm, cuda_dev)
         g = _gate_up(p, pk, routing, _plan(bm, 2 * p.inter, p.hidden, st, bst, grid), cuda_dev)
         bits = bf16_bits(g)[_routed(p)]
@@ -174,7 +174,7 @@ def test_over_allocated_routing_and_validation(cuda_dev):
     cap = ops.w4a16_align_capacity(t.numel(), 8, 32) + 32 * 8   # extra unused blocks
     sid, eid, ntp = ops.w4a16_moe_align_block_size(t, 8, 32, cap)
     plan = _plan(32, 2 * p.inter, p.hidden)
-    ws = ops.new_workspace(plan, cuda_dev)
+    ws = ops.new_workspace(plan, cuda_dev, cap, p.hidden)
     out = torch.empty((p.numel, 2 * p.inter), dtype=torch.bfloat16, device=cuda_dev)
     ops.w4a16_moe_indexed_gemm(ops.W4A16_GATE_UP, pk, 8, 2 * p.inter, p.hidden,
                                bf16_tensor(p.x, cuda_dev), p.tokens, p.topk, sid, eid, ntp, plan,
@@ -203,8 +203,8 @@ def test_down_accumulate_flag(cuda_dev):
     rng = np.random.default_rng(1)
     a_bits = wl.random_activations(rng, p.numel, p.inter)
     y = _down(p, pk, routing, plan, a_bits, cuda_dev)
-    ws = ops.new_workspace(plan, cuda_dev)
     sid, eid, ntp = routing
+    ws = ops.new_workspace(plan, cuda_dev, sid.numel(), p.inter)
     y2 = y.clone()
     ops.w4a16_moe_indexed_gemm(ops.W4A16_DOWN, pk, 8, p.hidden, p.inter,
                                bf16_tensor(a_bits, cuda_dev), p.tokens, p.topk, sid, eid, ntp,

@@ -31,7 +31,7 @@ def test_noalloc_matches_workspace_entry_point_twice(cuda_dev):
     sid, eid, ntp = ops.w4a16_moe_align_block_size(ids, p.num_experts, plan.block_m)
     x = bf16_tensor(p.x, cuda_dev)
     w = dev(p.topk_weights, cuda_dev)
-    ws = ops.new_workspace(plan, cuda_dev)
+    ws = ops.new_workspace(plan, cuda_dev, sid.numel(), max(p.hidden, p.inter))
 
     g_ref = ops.w4a16_moe_indexed_gemm(ops.W4A16_GATE_UP, pk_gu, p.num_experts, 2 * p.inter,
                                        p.hidden, x, p.tokens, p.topk, sid, eid, ntp, plan, ws)

@@ -33,44 +33,29 @@ long long wait_timeout_cycles() {
 
 int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
-// TMEM (512 columns): the operand ring's 2 * S A slots of 32 columns (64
-// BF16 of K per lane), then d_slots accumulator slots, each holding the two
-// partial accumulators (even / odd k steps) of d_cols columns. Two
-// accumulator slots let the epilogue of one item overlap the next item's
-// MMAs; the remaining columns deepen the ring (up to 6 slots per parity).
-int tmem_ring_slots(int block_m, bool gather, int* d_cols, int* d_slots) {
-  const int dcols = round_up(max_mma_n(block_m, gather), 32);
-  const int dsl = (2 * 64 + 2 * 2 * dcols <= 512) ? 2 : 1;
-  int s = 6;
-  while (s > 2 && 64 * s + dsl * 2 * dcols > 512) --s;
-  if (d_cols) *d_cols = dcols;
-  if (d_slots) *d_slots = dsl;
-  return s;
-}
-
 struct Pipeline {
-  int w_stages, ring_slots, d_cols, d_slots;
+  int w_stages, b_stages, d_cols, parts, d_slots;
   size_t smem;
 };
 
-// Validate a plan and derive the pipeline: the operand ring depth is the
-// smaller of what TMEM allows and plan.b_stages / 2. Gathered rows (indexed
-// family) use half of every 8-row atom, so their block is at most 64 rows.
-bool plan_pipeline(const w4a16_plan_t& p, bool gather, Pipeline* out) {
-  if (p.block_m < 16 || p.block_m > (gather ? 64 : 128) || p.block_m % 16 != 0) return false;
+// Validate a plan and derive the pipeline. TMEM holds four A slots of two k
+// steps (64 columns each) and, in the other 256 columns, the partial
+// accumulators of one or two items. plan.stages is the weight ring depth in
+// stages of two k steps (rounded down to a multiple of 4: each of the four
+// dequant warpgroups owns every fourth stage); plan.b_stages is the
+// activation ring depth in k steps (a multiple of 4: an even number of
+// stages).
+bool plan_pipeline(const w4a16_plan_t& p, Pipeline* out) {
+  if (p.block_m < 16 || p.block_m > 128 || p.block_m % 16 != 0) return false;
   if (p.bn != kTileRows || p.bk != kKStep || p.split_k != 1 || p.layout != W4A16_LAYOUT_KTILE64)
     return false;
-  if (p.stages < 2 || p.stages > 16 || p.b_stages < 4 || p.b_stages > 16 || p.b_stages % 2 != 0)
+  if (p.stages < 4 || p.stages > 16 || p.b_stages < 8 || p.b_stages > 32 || p.b_stages % 4 != 0)
     return false;
   Pipeline pl;
-  int s = tmem_ring_slots(p.block_m, gather, &pl.d_cols, &pl.d_slots);
-  if (const char* e = std::getenv("W4A16_TUNE_A_SLOTS")) {
-    const int v = std::atoi(e);
-    if (v >= 2 && v < s) s = v;
-  }
-  pl.ring_slots = std::min(s, p.b_stages / 2);
-  pl.w_stages = p.stages;
-  pl.smem = gemm_smem_bytes(p.block_m, gather, pl.w_stages, pl.ring_slots);
+  if (!tmem_accumulators(p.block_m, &pl.d_cols, &pl.parts, &pl.d_slots)) return false;
+  pl.w_stages = p.stages / 4 * 4;
+  pl.b_stages = p.b_stages / 2;
+  pl.smem = gemm_smem_bytes(p.block_m, pl.w_stages, pl.b_stages);
   if (pl.smem > static_cast<size_t>(kMaxDynSmem)) return false;
   *out = pl;
   return true;
@@ -78,10 +63,27 @@ bool plan_pipeline(const w4a16_plan_t& p, bool gather, Pipeline* out) {
 
 void fill_pipeline(const Pipeline& pl, GemmArgs* g) {
   g->w_stages = pl.w_stages;
-  g->b_stages = 2 * pl.ring_slots;
-  g->a_slots = pl.ring_slots;
+  g->b_stages = pl.b_stages;
+  g->n_parts = pl.parts;
   g->d_cols = pl.d_cols;
   g->d_slots = pl.d_slots;
+}
+
+// Ring depths of a plan: the deepest (activation stages, weight stages) pair
+// that fits in shared memory next to block_m-row activation stages,
+// activation ring first.
+void set_ring_depths(w4a16_plan_t* p) {
+  static const int kDepths[][2] = {{8, 16}, {6, 16}, {8, 12}, {6, 12}, {4, 16},
+                                   {4, 12}, {8, 8},  {6, 8},  {4, 8},  {4, 4}};
+  p->b_stages = 8;
+  p->stages = 4;
+  for (const auto& dw : kDepths) {
+    if (gemm_smem_bytes(p->block_m, dw[1], dw[0]) <= static_cast<size_t>(kMaxDynSmem)) {
+      p->b_stages = 2 * dw[0];
+      p->stages = dw[1];
+      return;
+    }
+  }
 }
 
 int current_sm_count() {
@@ -133,13 +135,7 @@ w4a16_status w4a16_plan(int tokens, int topk, int num_experts, int n, int k, flo
   p.block_m = block_m;
   p.bn = kTileRows;
   p.bk = kKStep;
-  const int ring = tmem_ring_slots(block_m, true, nullptr, nullptr);
-  p.b_stages = 2 * ring;
-  // weight ring: as deep as shared memory allows (up to 16 stages of 9 KB)
-  int ws = 16;
-  while (ws > 2 && gemm_smem_bytes(block_m, true, ws, ring) > static_cast<size_t>(kMaxDynSmem))
-    --ws;
-  p.stages = ws;
+  set_ring_depths(&p);
   p.split_k = 1;
   p.ctas_per_sm = 1;
   p.swap_ab = 1;
@@ -212,11 +208,10 @@ w4a16_status w4a16_unpack(const void* packed, int num_experts, int n, int k, uin
                                    scales, static_cast<cudaStream_t>(stream)));
 }
 
-size_t w4a16_workspace_size(const w4a16_plan_t* plan, int rows, int n) {
+size_t w4a16_workspace_size(const w4a16_plan_t* plan, int rows, int k) {
   (void)plan;
-  (void)rows;
-  (void)n;
-  return kStatusBytes;
+  if (rows <= 0 || k <= 0) return kStatusBytes;
+  return kStatusBytes + (permuted_bytes(rows, k) + 255) / 256 * 256;
 }
 
 w4a16_status w4a16_moe_indexed_gemm(int mode, const void* packed, int num_experts, int n, int k,
@@ -239,10 +234,10 @@ w4a16_status w4a16_moe_indexed_gemm(int mode, const void* packed, int num_expert
     return W4A16_ERR_INVALID_ARG;
   if (!aligned16(packed) || !aligned16(out) || (a != nullptr && !aligned16(a)))
     return W4A16_ERR_INVALID_ARG;
-  if (workspace == nullptr || ws_bytes < w4a16_workspace_size(plan, tokens * topk, n))
+  if (workspace == nullptr || ws_bytes < w4a16_workspace_size(plan, capacity, k))
     return W4A16_ERR_WORKSPACE;
   Pipeline pl;
-  if (!plan_pipeline(*plan, true, &pl)) return W4A16_ERR_INVALID_ARG;
+  if (!plan_pipeline(*plan, &pl)) return W4A16_ERR_INVALID_ARG;
   const int bm = plan->block_m;
   if (capacity % bm != 0) return W4A16_ERR_INVALID_ARG;
   const long long numel = static_cast<long long>(tokens) * topk;
@@ -290,10 +285,20 @@ w4a16_status w4a16_moe_indexed_gemm(int mode, const void* packed, int num_expert
   g.k = k;
   g.n_tiles = packed_tiles(n);
   g.k_steps = packed_ksteps(k);
-  g.act = a;
+  // routed rows into routing order (after the status block of the workspace)
+  const int sms = current_sm_count();
+  if (sms <= 0) return W4A16_ERR_CUDA;
+  uint16_t* permuted =
+      reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(workspace) + kStatusBytes);
+  const int a_div = mode == W4A16_DOWN ? 1 : topk;
+  if (!encode_permuted_tmap(&g.tmap, permuted, capacity, permuted_row_elems(k), bm))
+    return W4A16_ERR_CUDA;
+  if (launch_permute_rows(a, k, a_div, static_cast<int>(numel), sorted_ids, num_tokens_padded,
+                          capacity, permuted, sms, s) != cudaSuccess)
+    return W4A16_ERR_CUDA;
+  g.act = permuted;
   g.gather_rows = 1;
-  g.act_rows = static_cast<int>(mode == W4A16_DOWN ? numel : tokens);
-  if (!encode_act_tmap(&g.tmap, a, g.act_rows, k, 1)) return W4A16_ERR_CUDA;
+  g.act_rows = capacity;
   g.family = kIndexed;
   g.out_mode = mode == W4A16_DOWN ? kOutF32WeightedAdd : kOutBf16;
   g.sorted_ids = sorted_ids;
@@ -301,7 +306,7 @@ w4a16_status w4a16_moe_indexed_gemm(int mode, const void* packed, int num_expert
   g.num_tokens_padded = num_tokens_padded;
   g.capacity = capacity;
   g.numel = static_cast<int>(numel);
-  g.a_div = mode == W4A16_DOWN ? 1 : topk;
+  g.a_div = a_div;
   g.o_div = mode == W4A16_DOWN ? topk : 1;
   g.topk_weights = topk_weights;
   g.block_m = bm;
@@ -309,8 +314,6 @@ w4a16_status w4a16_moe_indexed_gemm(int mode, const void* packed, int num_expert
   g.status = static_cast<int*>(workspace);
   fill_pipeline(pl, &g);
   g.timeout_cycles = wait_timeout_cycles();
-  const int sms = current_sm_count();
-  if (sms <= 0) return W4A16_ERR_CUDA;
   long long grid = plan->grid > 0 ? plan->grid : static_cast<long long>(sms) * plan->ctas_per_sm;
   const long long max_items = static_cast<long long>(capacity / bm) * g.n_tiles;
   grid = std::max<long long>(1, std::min(grid, max_items));
@@ -335,13 +338,15 @@ w4a16_status w4a16_moe_grouped_gemm(int kind, const void* packed, int num_expert
   if (plan == nullptr) {
     const int rows = expected_m > 0 ? expected_m : std::max(1, m);
     w4a16_plan(rows, 1, 1, n, k, static_cast<float>(rows), &local);
-    if (rows > 80) local.block_m = 128;  // consecutive rows fill whole atoms
+    if (rows > 80) {
+      local.block_m = 128;
+      set_ring_depths(&local);
+    }
     plan = &local;
   }
-  if (workspace == nullptr || ws_bytes < w4a16_workspace_size(plan, m, n))
-    return W4A16_ERR_WORKSPACE;
+  if (workspace == nullptr || ws_bytes < kStatusBytes) return W4A16_ERR_WORKSPACE;
   Pipeline pl;
-  if (!plan_pipeline(*plan, false, &pl)) return W4A16_ERR_INVALID_ARG;
+  if (!plan_pipeline(*plan, &pl)) return W4A16_ERR_INVALID_ARG;
   const int bm = plan->block_m;
   const long long rows_total =
       kind == W4A16_GROUPED_MASKED ? static_cast<long long>(num_experts) * m : m;
@@ -384,7 +389,7 @@ w4a16_status w4a16_moe_grouped_gemm(int kind, const void* packed, int num_expert
   g.act = a;
   g.gather_rows = 0;
   g.act_rows = static_cast<int>(rows_total);
-  if (!encode_act_tmap(&g.tmap, a, rows_total, k, 8)) return W4A16_ERR_CUDA;
+  if (!encode_act_tmap(&g.tmap, a, rows_total, k, bm)) return W4A16_ERR_CUDA;
   g.family = kind == W4A16_GROUPED_CONTIGUOUS ? kContiguous : kMasked;
   g.out_mode = kOutBf16;
   g.layout = layout;

@@ -27,6 +27,13 @@ constexpr int kStatusBytes = 256;
 inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 inline long long ceil_div_ll(long long a, long long b) { return (a + b - 1) / b; }
 
+// Permuted activation rows of the indexed GEMM (in the workspace, after the
+// status block): [capacity][k rounded up to 64] BF16.
+inline int permuted_row_elems(int k) { return ceil_div(k, kKStep) * kKStep; }
+inline size_t permuted_bytes(long long rows, int k) {
+  return static_cast<size_t>(rows) * permuted_row_elems(k) * 2;
+}
+
 inline int packed_tiles(int n) { return ceil_div(n, kTileRows); }
 inline int packed_ksteps(int k) { return ceil_div(k, kKStep); }
 inline size_t packed_expert_bytes(int n, int k) {
@@ -37,12 +44,12 @@ enum Family { kIndexed = 0, kContiguous = 1, kMasked = 2 };
 enum OutMode { kOutBf16 = 0, kOutF32WeightedAdd = 1 };
 
 struct GemmArgs {
-  // Activation tensor map (BF16 [act_rows, k], 128-byte swizzle, box 64 x
-  // box_rows): box_rows 1 for the row gather (tile::gather4), 8 for
-  // consecutive rows.
+  // Activation tensor map: the permuted rows of the indexed family (3-D,
+  // two k steps per box) or the rows of the grouped families (2-D, one k step
+  // per box); box rows = block_m, 128-byte swizzle.
   CUtensorMap tmap;
   int act_rows;
-  int gather_rows;  // 1: rows gathered four at a time, 4 real rows per 8-row atom
+  int gather_rows;  // 1: routed rows (indexed family), 0: consecutive rows
   const uint8_t* wpack;
   long long expert_bytes;
   int num_experts, n, k, n_tiles, k_steps;
@@ -65,18 +72,25 @@ struct GemmArgs {
   int block_m;
   void* out;
   int* status;
-  // pipeline configuration (derived from the plan)
-  int w_stages, b_stages, d_slots, d_cols, a_slots;
+  // pipeline configuration (derived from the plan): weight ring stages (a
+  // multiple of 4), activation ring stages (even), partial accumulators (MMA
+  // issuers), accumulator slots and the TMEM columns of one accumulator
+  int w_stages, b_stages, n_parts, d_slots, d_cols;
   long long timeout_cycles;
 };
 
 int device_sm_count(int device);
-// Largest MMA N of a block: gathered rows fill half of every 8-row atom.
-__host__ __device__ inline int max_mma_n(int block_m, bool gather) {
-  return gather ? 2 * block_m : block_m;
-}
-size_t gemm_smem_bytes(int block_m, bool gather, int w_stages, int ring_slots);
+size_t gemm_smem_bytes(int block_m, int w_stages, int b_stages);
+// TMEM split for a block of block_m rows: columns of one accumulator, the
+// number of partial accumulators (MMA issuers) and of accumulator slots.
+// False when even one accumulator does not fit.
+bool tmem_accumulators(int block_m, int* d_cols, int* parts, int* d_slots);
+// 2-D map of BF16 [rows, k] (box 64 x box_rows, 128-byte swizzle).
 bool encode_act_tmap(CUtensorMap* map, const void* act, long long rows, int k, int box_rows);
+// 3-D map of the permuted rows [rows, k_pad]: dims (64 columns, rows, k_pad /
+// 64 chunks), box 64 x box_rows x 2 (two k steps), 128-byte swizzle.
+bool encode_permuted_tmap(CUtensorMap* map, const void* act, long long rows, int k_pad,
+                          int box_rows);
 cudaError_t launch_moe_gemm(const GemmArgs& args, int grid, cudaStream_t stream);
 
 cudaError_t launch_align(const int32_t* topk_ids, int numel, int num_experts, int block_m,
@@ -88,6 +102,10 @@ cudaError_t launch_prepack(const uint8_t* q, const uint16_t* scales, int num_exp
                            int k, uint8_t* packed, cudaStream_t stream);
 cudaError_t launch_unpack(const uint8_t* packed, int num_experts, int n, int k, uint8_t* q,
                           uint16_t* scales, cudaStream_t stream);
+
+cudaError_t launch_permute_rows(const uint16_t* a, int k, int a_div, int numel,
+                                const int32_t* sorted_ids, const int32_t* num_tokens_padded,
+                                int capacity, uint16_t* dst, int sms, cudaStream_t stream);
 
 cudaError_t launch_silu_and_mul(const uint16_t* in, int rows, int inter, uint16_t* out,
                                 cudaStream_t stream);

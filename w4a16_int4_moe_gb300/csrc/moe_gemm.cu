@@ -9,9 +9,11 @@
 // for every shape and builds it on tcgen05:
 //
 //   weights (packed uint4 + BF16 scales) --bulk copy--> shared-memory ring
-//     --dequant warps: (q - 8) * s in registers, tcgen05.st--> TMEM (A)
-//   tokens (BF16 rows gathered through the routing) --cp.async, 128-byte
-//     swizzle--> shared-memory ring (B)
+//     --dequant warpgroups: (q - 8) * s in registers, tcgen05.st--> TMEM (A)
+//   tokens --TMA tensor copies, 128-byte swizzle--> shared-memory ring (B):
+//     the indexed family's routed rows, copied once into routing order
+//     (permute.cu), arrive two k steps per copy; the grouped families' rows
+//     one k step per copy
 //   tcgen05.mma kind::f16, M = 128 weight rows, N = the block's tokens
 //     (rounded to 16, chosen per block at run time), K = 16 per instruction,
 //     FP32 accumulators in TMEM (D)
@@ -22,6 +24,14 @@
 // shared-memory port free for the token operand: at decode (N = 16) a
 // shared-memory A operand would cost more shared bandwidth than the HBM
 // stream delivers weights.
+//
+// The pipeline moves in stages of two 64-k steps (9216 bytes of packed
+// weights): every handshake is paid once per stage, four dequant warpgroups
+// work on four consecutive stages, and up to four MMA issuers split the k
+// steps (each tcgen05.mma holds its issuing thread for tens of cycles, so at
+// small N the issue rate, not the tensor core, sets the pace). Each issuer
+// owns a partial FP32 accumulator; the epilogue adds them in a fixed order,
+// so results do not depend on the schedule.
 //
 // Work item = (routing block, 128-row weight tile), full K. Persistent grid;
 // CTA c takes items c, c + grid, ... Every device-side wait is bounded: a wait
@@ -41,34 +51,39 @@ namespace w4a16 {
 
 namespace {
 
-constexpr int kThreads = 576;
-constexpr int kWStageBytes = 2 * kStepBytes;  // one weight stage = 2 k steps
-constexpr int kAColsPerSlot = 32;             // 64 BF16 of K per TMEM lane
+constexpr int kThreads = 864;
+constexpr int kWStageBytes = 2 * kStepBytes;  // one stage = 2 k steps of packed weights
+constexpr int kASlots = 4;                    // A slots in TMEM = dequant warpgroups
+constexpr int kAColsPerSlot = 64;             // 2 k steps x 64 BF16 of K per TMEM lane
+constexpr int kAColsPerStep = 32;
+constexpr int kItemSlots = 4;                 // routing-info ring depth (items)
+constexpr int kMaxIssuers = 4;
 constexpr int kTmemCols = 512;
 
-// warp roles (warp 3 idles; the warpgroups start at multiples of 4 warps so
-// that warp % 4 selects the TMEM lane quarter each warp may access)
-constexpr int kWarpProducer = 0;
-constexpr int kWarpMma0 = 1;        // MMA issuer of the even k steps (+ TMEM allocation)
-constexpr int kWarpMma1 = 2;        // MMA issuer of the odd k steps
-constexpr int kWarpDequant0 = 4;    // 8 warps (2 warpgroups)
-constexpr int kWarpEpilogue0 = 12;  // 4 warps
-constexpr int kWarpGather0 = 16;    // 2 warps
+// Warp roles. The dequant and epilogue warpgroups start at multiples of 4
+// warps, so that warp % 4 selects the TMEM lane quarter each warp may access.
+constexpr int kWarpProducer = 0;    // weight bulk copies
+constexpr int kWarpMma0 = 1;        // MMA issuers 0..2 in warps 1..3 (warp 1 allocates TMEM)
+constexpr int kWarpDequant0 = 4;    // 16 warps: 4 warpgroups, one per A slot
+constexpr int kWarpEpilogue0 = 20;  // 4 warps
+constexpr int kWarpMma3 = 24;       // MMA issuer 3
+constexpr int kWarpGather = 25;     // activation rows
+constexpr int kWarpRouter = 26;     // per-item routing info, items ahead of the MMA
 
 // where codes recorded in the status word when a wait gives up
 enum Where {
   kWhereProducer = 1, kWhereDequantW = 2, kWhereDequantA = 3, kWhereGatherItem = 4,
   kWhereGatherB = 5, kWhereMmaItem = 6, kWhereMmaAcc = 7, kWhereMmaA = 8, kWhereMmaB = 9,
-  kWhereEpiAcc = 10, kWhereEpiItem = 11, kWhereDrain = 12
+  kWhereEpiAcc = 10, kWhereEpiItem = 11, kWhereDrain = 12, kWhereRouter = 13
 };
 
 struct Smem {
-  uint8_t* b_ring;      // [2 parities][S slots][block_m rows][128 B], 128-byte swizzle
+  uint8_t* b_ring;      // [BS stages][2 k steps][block_m rows][128 B], 128-byte swizzle
   uint8_t* w_ring;      // [WS stages][2 k steps][kStepBytes]
-  int* info_row;        // [2 gather warps][2 item slots][block_m]: activation row, -1 = none
-  int* info_dst;        // [2][2][block_m]: output row, -1 = not a real row
-  float* info_wt;       // [2][2][block_m]: top-k weight (down pass)
-  int* info_n16;        // [2][2]: MMA N of the item
+  int* info_dst;        // [kItemSlots][block_m]: output row, -1 = not a real row
+  float* info_wt;       // [kItemSlots][block_m]: top-k weight (down pass)
+  int* info_n16;        // [kItemSlots]: MMA N of the item
+  int* info_rows;       // [kItemSlots]: real rows (last real row + 1)
   uint64_t* bars;
   uint32_t* tmem_base;
   volatile int* abort_flag;
@@ -76,19 +91,21 @@ struct Smem {
 
 // mbarrier addresses (shared-window offsets, 8 bytes each)
 struct Bars {
-  uint32_t w_full, w_empty, a_full, b_full, ab_empty, item_full, item_empty, acc_full, acc_empty,
-      final_bar;
+  uint32_t w_full, w_empty, a_full, a_empty, b_full, b_empty, item_full, item_empty, acc_full,
+      acc_empty, final_bar;
   __device__ uint32_t wf(int i) const { return w_full + 8u * i; }
   __device__ uint32_t we(int i) const { return w_empty + 8u * i; }
   __device__ uint32_t af(int i) const { return a_full + 8u * i; }
+  __device__ uint32_t ae(int i) const { return a_empty + 8u * i; }
   __device__ uint32_t bf(int i) const { return b_full + 8u * i; }
-  __device__ uint32_t abe(int i) const { return ab_empty + 8u * i; }
+  __device__ uint32_t be(int i) const { return b_empty + 8u * i; }
   __device__ uint32_t itf(int i) const { return item_full + 8u * i; }
   __device__ uint32_t ite(int i) const { return item_empty + 8u * i; }
   __device__ uint32_t accf(int i) const { return acc_full + 8u * i; }
   __device__ uint32_t acce(int i) const { return acc_empty + 8u * i; }
   __device__ uint32_t fin(int i) const { return final_bar + 8u * i; }
 };
+constexpr int kNumBarsFixed = 2 * kASlots + 2 * kItemSlots + 2 + 2 + kMaxIssuers;
 
 __device__ __forceinline__ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -110,8 +127,25 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
   }
 }
 
+// Warp-uniform bounded wait: every lane observes the phase itself (so each
+// lane's later reads are ordered after the completion it saw); the warp goes
+// on only if all lanes saw it.
+__device__ __forceinline__ bool warp_wait_phase(uint32_t bar, uint32_t parity,
+                                             volatile int* abort_flag, int* status, int where,
+                                             long long timeout) {
+  return __all_sync(0xffffffffu, wait_phase(bar, parity, abort_flag, status, where, timeout));
+}
+
+// Drain wait (abort path): wait, with a bound, for a phase that copies
+// already issued will complete.
+__device__ __forceinline__ void drain_phase(uint32_t bar, uint32_t parity, long long timeout) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity) && clock64() - t0 < timeout) {
+  }
+}
+
 // Position in a ring of mbarrier-guarded slots: slot index and the parity of
-// the slot's current phase (incremented without divisions).
+// the slot's current phase (advanced without divisions).
 struct RingPos {
   int slot = 0;
   uint32_t phase = 0;
@@ -121,7 +155,41 @@ struct RingPos {
       phase ^= 1u;
     }
   }
+  // advance by `step` slots, step <= n
+  __device__ __forceinline__ void advance(int step, int n) {
+    slot += step;
+    if (slot >= n) {
+      slot -= n;
+      phase ^= 1u;
+    }
+  }
 };
+
+// How the k steps of an item are split among the MMA issuers: with P partial
+// accumulators, issuer q takes the k steps ks with ks % P == q. Stage u
+// (k steps 2u, 2u + 1) is then read by min(P, 2) issuers; for P == 4,
+// issuer q sees only the stages of parity q >> 1.
+struct IssuerPlan {
+  int stride, first, j0, j1;  // stages u = first + stride * i; k steps j0..j1 of each
+};
+__device__ __forceinline__ IssuerPlan issuer_plan(int q, int parts) {
+  IssuerPlan p;
+  if (parts == 4) {
+    p.stride = 2;
+    p.first = q >> 1;
+    p.j0 = p.j1 = q & 1;
+  } else if (parts == 2) {
+    p.stride = 1;
+    p.first = 0;
+    p.j0 = p.j1 = q;
+  } else {
+    p.stride = 1;
+    p.first = 0;
+    p.j0 = 0;
+    p.j1 = 1;
+  }
+  return p;
+}
 
 struct ItemDesc {
   int blk, tile, e;
@@ -149,24 +217,21 @@ __device__ __forceinline__ ItemDesc decode_item(const GemmArgs& a, int it, int n
   return d;
 }
 
-// Row j of block `blk`: activation row, output row (-1 = not a real row) and
-// the top-k weight of the down pass.
-__device__ __forceinline__ void row_info(const GemmArgs& a, const ItemDesc& d, int j, int& src,
-                                         int& dst, float& wt) {
-  src = -1;
+// Row j of block `blk`: output row (-1 = not a real row) and the top-k
+// weight of the down pass.
+__device__ __forceinline__ void row_info(const GemmArgs& a, const ItemDesc& d, int j, int& dst,
+                                         float& wt) {
   dst = -1;
   wt = 0.f;
   if (a.family == kIndexed) {
     const int id = __ldg(a.sorted_ids + static_cast<long long>(d.blk) * a.block_m + j);
     if (id >= 0 && id < a.numel) {
-      src = id / a.a_div;
       dst = id / a.o_div;
       wt = (a.out_mode == kOutF32WeightedAdd) ? __ldg(a.topk_weights + id) : 1.f;
     }
   } else if (a.family == kContiguous) {
     const int r = d.blk * a.block_m + j;
     if (r < a.m && __ldg(a.layout + r) == d.e) {
-      src = r;
       dst = r;
       wt = 1.f;
     }
@@ -175,8 +240,7 @@ __device__ __forceinline__ void row_info(const GemmArgs& a, const ItemDesc& d, i
     const int rl = (d.blk - d.e * bpe) * a.block_m + j;
     const int valid = min(max(__ldg(a.layout + d.e), 0), a.m);
     if (rl < valid) {
-      src = d.e * a.m + rl;
-      dst = src;
+      dst = d.e * a.m + rl;
       wt = 1.f;
     }
   }
@@ -213,6 +277,13 @@ __device__ __forceinline__ void dequant_group(const uint4 q, uint32_t scale_bits
 
 }  // namespace
 
+// Stage bookkeeping shared by every role. An item's k range is split into
+// stages of two 64-k steps; the stage count is padded to an even number (the
+// pad stage moves no data), so that every item starts on an even global
+// stage and the split of k steps among the MMA issuers is the same for every
+// item. Global stage u -> A slot u % 4 (dequant warpgroup u % 4), B slot
+// u % BS, weight slot u % WS (WS % 4 == 0, BS even).
+
 __global__ void __launch_bounds__(kThreads, 1)
     w4a16_moe_gemm_kernel(const __grid_constant__ GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
@@ -223,27 +294,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* base = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
   const int bm = args.block_m;
-  const int S = args.a_slots;  // operand ring slots per k-step parity
   const int WS = args.w_stages;
+  const int BS = args.b_stages;
+  const int parts = args.n_parts;
   const bool gather = args.gather_rows != 0;
-  const uint32_t b_slot_bytes = static_cast<uint32_t>(max_mma_n(bm, gather)) * 128u;
+  const uint32_t b_step_bytes = static_cast<uint32_t>(bm) * 128u;
+  const uint32_t b_stage_bytes = 2u * b_step_bytes;
   Smem sm;
   size_t off = 0;
   sm.b_ring = base;
-  off += static_cast<size_t>(2 * S) * b_slot_bytes;
+  off += static_cast<size_t>(BS) * b_stage_bytes;
   sm.w_ring = base + off;
   off += static_cast<size_t>(WS) * kWStageBytes;
-  sm.info_row = reinterpret_cast<int*>(base + off);
-  off += 4 * bm * sizeof(int);
   sm.info_dst = reinterpret_cast<int*>(base + off);
-  off += 4 * bm * sizeof(int);
+  off += kItemSlots * bm * sizeof(int);
   sm.info_wt = reinterpret_cast<float*>(base + off);
-  off += 4 * bm * sizeof(float);
+  off += kItemSlots * bm * sizeof(float);
   sm.info_n16 = reinterpret_cast<int*>(base + off);
-  off += 4 * sizeof(int);
+  off += kItemSlots * sizeof(int);
+  sm.info_rows = reinterpret_cast<int*>(base + off);
+  off += kItemSlots * sizeof(int);
   off = align_up(off, 8);
   sm.bars = reinterpret_cast<uint64_t*>(base + off);
-  off += (2 * WS + 6 * S + 10) * 8;
+  off += (2 * WS + 2 * BS + kNumBarsFixed) * 8;
   sm.tmem_base = reinterpret_cast<uint32_t*>(base + off);
   off += 4;
   sm.abort_flag = reinterpret_cast<volatile int*>(base + off);
@@ -255,40 +328,49 @@ __global__ void __launch_bounds__(kThreads, 1)
     b0 += 8 * WS;
     B.w_empty = b0;
     b0 += 8 * WS;
-    B.a_full = b0;
-    b0 += 8 * 2 * S;
     B.b_full = b0;
-    b0 += 8 * 2 * S;
-    B.ab_empty = b0;
-    b0 += 8 * 2 * S;
+    b0 += 8 * BS;
+    B.b_empty = b0;
+    b0 += 8 * BS;
+    B.a_full = b0;
+    b0 += 8 * kASlots;
+    B.a_empty = b0;
+    b0 += 8 * kASlots;
     B.item_full = b0;
-    b0 += 16;
+    b0 += 8 * kItemSlots;
     B.item_empty = b0;
-    b0 += 16;
+    b0 += 8 * kItemSlots;
     B.acc_full = b0;
     b0 += 16;
     B.acc_empty = b0;
     b0 += 16;
     B.final_bar = b0;
   }
+  // issuers that read each stage (each commits once per stage)
+  const int readers = parts < 2 ? parts : 2;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < WS; ++i) {
-      mbar_init(B.wf(i), 1);
-      mbar_init(B.we(i), 8);  // every dequant warp releases every stage
+      mbar_init(B.wf(i), 1);  // the producer's arrival (+ the copy's bytes)
+      mbar_init(B.we(i), 4);  // the 4 warps of the warpgroup that read the stage
     }
-    for (int i = 0; i < 2 * S; ++i) {
-      mbar_init(B.af(i), 4);   // the 4 warps of the dequant warpgroup
-      mbar_init(B.bf(i), 1);   // the gather warp's expect_tx (plus the copies' bytes)
-      mbar_init(B.abe(i), 1);  // one tcgen05.commit of the MMA issuer
+    for (int i = 0; i < BS; ++i) {
+      mbar_init(B.bf(i), 1);        // the gather warp's arrival (+ tensor-copy bytes)
+      mbar_init(B.be(i), readers);  // tcgen05.commit of the stage's issuers
+    }
+    for (int i = 0; i < kASlots; ++i) {
+      mbar_init(B.af(i), 4);        // the 4 warps of the slot's dequant warpgroup
+      mbar_init(B.ae(i), readers);
+    }
+    for (int i = 0; i < kItemSlots; ++i) {
+      mbar_init(B.itf(i), 1);  // the router warp
+      mbar_init(B.ite(i), 4);  // the 4 epilogue warps
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(B.itf(i), 2);   // lane 0 of each gather warp
-      mbar_init(B.ite(i), 4);   // the 4 epilogue warps
-      mbar_init(B.accf(i), 2);  // one tcgen05.commit per MMA issuer
+      mbar_init(B.accf(i), parts);  // one tcgen05.commit per MMA issuer
       mbar_init(B.acce(i), 4);
-      mbar_init(B.fin(i), 1);
     }
+    for (int i = 0; i < kMaxIssuers; ++i) mbar_init(B.fin(i), 1);
     *sm.abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -315,24 +397,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     num_blocks = args.num_experts * bpe;
   }
   const int items = num_blocks * args.n_tiles;
-  // TMEM columns: the 2*S A slots (32 columns each), then per accumulator
-  // slot the two partial accumulators (even / odd k steps), d_cols each.
-  const int d_col_base = 2 * S * kAColsPerSlot;
-  const int n_wst = (args.k_steps + 1) / 2;
+  // TMEM columns: the kASlots A slots (64 columns each), then per accumulator
+  // slot the `parts` partial accumulators, d_cols each.
+  const int d_col_base = kASlots * kAColsPerSlot;
+  const int n_st = (args.k_steps + 1) / 2;  // stages holding data
+  const int n_stp = n_st + (n_st & 1);      // stages per item (even)
   const long long tmo = args.timeout_cycles;
   volatile int* abort_flag = sm.abort_flag;
   int* status = args.status;
-
-  // The k steps of one parity g form one pipeline: dequant warpgroup g fills
-  // the A slot (TMEM), gather warp g the B slot (shared memory) of ring slot
-  // g*S + c % S, where c counts that parity's k steps over all items; MMA
-  // issuer g consumes both and frees the slot with one tcgen05.commit.
+  const int mma_q = warp == kWarpMma3 ? 3 : warp - kWarpMma0;  // issuer index of MMA warps
 
   if (warp == kWarpProducer) {
     // ======================= weight producer (bulk copies) ==================
     if (lane == 0) {
       const uint64_t policy = policy_evict_first();
-      uint32_t wcnt = 0;
+      uint32_t issued = 0;  // stages whose w_full phase this thread started
       RingPos wp;
       bool ok = true;
       for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
@@ -340,45 +419,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (d.e < 0) continue;
         const uint8_t* src = args.wpack + static_cast<long long>(d.e) * args.expert_bytes +
                              static_cast<long long>(d.tile) * args.k_steps * kStepBytes;
-        for (int st = 0; st < n_wst; ++st, ++wcnt, wp.next(WS)) {
+        for (int st = 0; st < n_stp; ++st, wp.next(WS)) {
           if (!wait_phase(B.we(wp.slot), wp.phase ^ 1, abort_flag, status, kWhereProducer, tmo)) {
             ok = false;
             break;
           }
-          const int nks = min(2, args.k_steps - 2 * st);
-          const uint32_t bytes = static_cast<uint32_t>(nks * kStepBytes);
-          mbar_arrive_expect_tx(B.wf(wp.slot), bytes);
-          bulk_g2s(smem_u32(sm.w_ring + static_cast<size_t>(wp.slot) * kWStageBytes),
-                   src + static_cast<long long>(st) * kWStageBytes, bytes, B.wf(wp.slot), policy);
+          const int nks = min(2, max(0, args.k_steps - 2 * st));
+          if (nks > 0) {
+            const uint32_t bytes = static_cast<uint32_t>(nks * kStepBytes);
+            mbar_arrive_expect_tx(B.wf(wp.slot), bytes);
+            bulk_g2s(smem_u32(sm.w_ring + static_cast<size_t>(wp.slot) * kWStageBytes),
+                     src + static_cast<long long>(st) * kWStageBytes, bytes, B.wf(wp.slot),
+                     policy);
+          } else {
+            mbar_arrive(B.wf(wp.slot));  // pad stage: no data
+          }
+          ++issued;
         }
       }
       if (!ok) {
         // Let every copy already issued land before the CTA can exit.
-        const uint32_t first = wcnt > static_cast<uint32_t>(WS) ? wcnt - WS : 0;
-        for (uint32_t u = first; u < wcnt; ++u) {
-          const int slot = u % WS;
-          const uint32_t ph = (u / WS) & 1;
-          const long long t0 = clock64();
-          while (!mbar_try_wait(B.wf(slot), ph) && clock64() - t0 < tmo) {
-          }
-        }
+        const uint32_t first = issued > static_cast<uint32_t>(WS) ? issued - WS : 0;
+        for (uint32_t u = first; u < issued; ++u) drain_phase(B.wf(u % WS), (u / WS) & 1, tmo);
       }
     }
-  } else if (warp == kWarpMma0 || warp == kWarpMma1) {
+  } else if ((warp >= kWarpMma0 && warp < kWarpDequant0) || warp == kWarpMma3) {
     // ======================= MMA issuers ====================================
-    // Issuer g owns the k steps with ks % 2 == g and accumulates into its own
-    // FP32 partial accumulator; the epilogue adds the two partials in a fixed
-    // order. At small N one issuing thread, not the tensor core, sets the
-    // pace (each tcgen05.mma blocks its issuer for tens of cycles), so two
-    // independent issuers double the MMA rate.
-    const int g = warp - kWarpMma0;
-    if (lane == 0) {
-      RingPos rp, ip, dp;
+    // Issuer q takes the k steps ks % parts == q of every item and
+    // accumulates them into its own FP32 partial accumulator.
+    const int q = mma_q;
+    if (lane == 0 && q < parts) {
+      const IssuerPlan pl = issuer_plan(q, parts);
+      RingPos ip, dp, ap, bp;
+      ap.slot = pl.first;
+      bp.slot = pl.first;
       bool ok = true;
-      // descriptor of ring slot 0 of this parity; later slots add their offset
-      const uint64_t b_desc0 =
-          smem_desc_sw128_kmajor(smem_u32(sm.b_ring + static_cast<size_t>(g * S) * b_slot_bytes));
-      const uint32_t b_slot_step = b_slot_bytes >> 4;  // in descriptor address units
+      const uint64_t b_desc0 = smem_desc_sw128_kmajor(smem_u32(sm.b_ring));
       for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
         const ItemDesc d = decode_item(args, it, num_blocks, bpe);
         if (d.e < 0) continue;
@@ -386,224 +462,244 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        const int n16 = sm.info_n16[ip.slot];  // gather warp 0's copy
+        const int n16 = sm.info_n16[ip.slot];
         if (!wait_phase(B.acce(dp.slot), dp.phase ^ 1, abort_flag, status, kWhereMmaAcc, tmo)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t idesc = idesc_bf16_m128(static_cast<uint32_t>(n16));
-        const uint32_t d_tmem = tmem + d_col_base + (dp.slot * 2 + g) * args.d_cols;
+        const uint32_t d_tmem = tmem + d_col_base + (dp.slot * parts + q) * args.d_cols;
         uint32_t acc = 0;
-        for (int ks = g; ks < args.k_steps; ks += 2, rp.next(S)) {
-          const int slot = g * S + rp.slot;
-          if (!wait_phase(B.af(slot), rp.phase, abort_flag, status, kWhereMmaA, tmo) ||
-              !wait_phase(B.bf(slot), rp.phase, abort_flag, status, kWhereMmaB, tmo)) {
+        for (int st = pl.first; st < n_stp; st += pl.stride) {
+          if (!wait_phase(B.af(ap.slot), ap.phase, abort_flag, status, kWhereMmaA, tmo) ||
+              !wait_phase(B.bf(bp.slot), bp.phase, abort_flag, status, kWhereMmaB, tmo)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t b_desc = b_desc0 + static_cast<uint64_t>(rp.slot) * b_slot_step;
-          const uint32_t a_tmem = tmem + slot * kAColsPerSlot;
+          for (int j = pl.j0; j <= pl.j1; ++j) {
+            if (2 * st + j >= args.k_steps) break;
+            // slot and k-step offsets are multiples of 1024 bytes
+            const uint64_t b_desc =
+                b_desc0 + ((static_cast<uint32_t>(bp.slot) * b_stage_bytes + j * b_step_bytes) >> 4);
+            const uint32_t a_tmem = tmem + ap.slot * kAColsPerSlot + j * kAColsPerStep;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            // +32 bytes of K per MMA inside the 128-byte swizzle row
-            mma_bf16_ts(d_tmem, a_tmem + kk * 8, b_desc + 2 * kk, idesc, acc);
-            acc = 1;
+            for (int kk = 0; kk < 4; ++kk) {
+              // +32 bytes of K per MMA inside the 128-byte swizzle row
+              mma_bf16_ts(d_tmem, a_tmem + kk * 8, b_desc + 2 * kk, idesc, acc);
+              acc = 1;
+            }
           }
-          tc_commit(B.abe(slot));
+          tc_commit(B.ae(ap.slot));
+          tc_commit(B.be(bp.slot));
+          ap.advance(pl.stride, kASlots);
+          bp.advance(pl.stride, BS);
         }
         if (!ok) break;
         tc_commit(B.accf(dp.slot));
-        ip.next(2);
+        ip.next(kItemSlots);
         dp.next(args.d_slots);
       }
       // every MMA issued by this thread has finished once its final barrier flips
-      tc_commit(B.fin(g));
-      const long long t0 = clock64();
-      while (!mbar_try_wait(B.fin(g), 0) && clock64() - t0 < tmo) {
-      }
+      tc_commit(B.fin(q));
+      drain_phase(B.fin(q), 0, tmo);
     }
-  } else if (warp >= kWarpGather0) {
-    // ======================= activation loads (TMA) =========================
-    // Gather warp g fills the B slots of parity g with tensor copies that
-    // write the 128-byte-swizzled K-major layout the MMA descriptor expects
-    // and count their bytes on the slot's mbarrier.
-    //  - gathered rows (indexed family): tile::gather4 puts 4 routed rows at
-    //    the start of an 8-row swizzle atom (rows 4..7 of the atom are not
-    //    used), so every copy starts 1024-byte aligned; the MMA N covers 8
-    //    columns per 4 rows and the epilogue skips the unused columns;
-    //  - consecutive rows (grouped families): one 64 x 8 box per atom.
-    const int g = warp - kWarpGather0;
-    const void* map = &args.tmap;
-    RingPos rp, ip;
-    bool ok = true;
-    for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
+  } else if (warp == kWarpRouter) {
+    // ======================= routing info, items ahead ======================
+    // Resolves each item's rows (activation row, output row, top-k weight)
+    // into the item ring up to kItemSlots items ahead, so that the global
+    // loads of the routing tensors stay off the copy and MMA critical path.
+    RingPos ip;
+    for (int it = blockIdx.x; it < items; it += gridDim.x) {
       const ItemDesc d = decode_item(args, it, num_blocks, bpe);
       if (d.e < 0) continue;
-      const int islot = ip.slot;
-      ok = __all_sync(0xffffffffu, wait_phase(B.ite(islot), ip.phase ^ 1, abort_flag, status,
-                                               kWhereGatherItem, tmo));
-      if (!ok) break;
-      const int copy = g * 2 + islot;
-      int* irow = sm.info_row + copy * bm;
-      int* idst = sm.info_dst + copy * bm;
-      float* iwt = sm.info_wt + copy * bm;
+      if (!warp_wait_phase(B.ite(ip.slot), ip.phase ^ 1, abort_flag, status, kWhereRouter, tmo))
+        break;
+      int* idst = sm.info_dst + ip.slot * bm;
+      float* iwt = sm.info_wt + ip.slot * bm;
       int maxj = -1;
       for (int j = lane; j < bm; j += 32) {
-        int s, dd;
+        int dd;
         float w;
-        row_info(args, d, j, s, dd, w);
-        irow[j] = s;
+        row_info(args, d, j, dd, w);
         idst[j] = dd;
         iwt[j] = w;
         if (dd >= 0) maxj = j;
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) maxj = max(maxj, __shfl_xor_sync(0xffffffffu, maxj, o));
-      // atoms to load and the MMA N (a multiple of 16 columns)
-      const int rows_needed = max(maxj + 1, 1);
-      const int n_copies = gather ? (rows_needed + 3) / 4 : (rows_needed + 7) / 8;
-      const int n_mma = ((n_copies * 8) + 15) & ~15;
-      if (lane == 0) sm.info_n16[copy] = n_mma;
+      const int rows = max(maxj + 1, 1);
+      if (lane == 0) {
+        sm.info_rows[ip.slot] = rows;
+        sm.info_n16[ip.slot] = (rows + 15) & ~15;
+      }
       __syncwarp();
-      if (lane == 0) mbar_arrive(B.itf(islot));
-      // per-lane copy coordinates, fixed for the item
-      int r0 = args.act_rows, r1 = args.act_rows, r2 = args.act_rows, r3 = args.act_rows;
-      if (lane < n_copies) {
-        if (gather) {
-          const int j = 4 * lane;
-          r0 = irow[j] >= 0 ? irow[j] : args.act_rows;
-          r1 = (j + 1 < bm && irow[j + 1] >= 0) ? irow[j + 1] : args.act_rows;
-          r2 = (j + 2 < bm && irow[j + 2] >= 0) ? irow[j + 2] : args.act_rows;
-          r3 = (j + 3 < bm && irow[j + 3] >= 0) ? irow[j + 3] : args.act_rows;
-        } else {
-          // first row of this atom in the activation tensor (consecutive rows)
-          r0 = (args.family == kContiguous) ? d.blk * bm + 8 * lane
-                                            : d.e * args.m + (d.blk - d.e * bpe) * bm + 8 * lane;
-        }
-      }
-      const uint32_t copy_bytes = gather ? 512u : 1024u;
-      for (int ks = g; ks < args.k_steps; ks += 2, rp.next(S)) {
-        const int slot = g * S + rp.slot;
-        ok = __all_sync(0xffffffffu, wait_phase(B.abe(slot), rp.phase ^ 1, abort_flag, status,
-                                                 kWhereGatherB, tmo));
-        if (!ok) break;
-        if (lane == 0) mbar_arrive_expect_tx(B.bf(slot), n_copies * copy_bytes);
-        __syncwarp();
-        if (lane < n_copies) {
-          const uint32_t dst =
-              smem_u32(sm.b_ring + static_cast<size_t>(slot) * b_slot_bytes) + lane * 1024u;
-          if (gather) {
-            tma_gather4(dst, map, ks * kKStep, r0, r1, r2, r3, B.bf(slot));
-          } else {
-            tma_load_2d(dst, map, ks * kKStep, r0, B.bf(slot));
+      if (lane == 0) mbar_arrive(B.itf(ip.slot));
+      ip.next(kItemSlots);
+    }
+  } else if (warp == kWarpGather) {
+    // ======================= activation rows (TMA) ==========================
+    // Fills the B slot of every stage with the block's rows in the
+    // 128-byte-swizzled K-major layout of the MMA descriptor (8-row atoms of
+    // 1024 bytes), counted in bytes on the slot's mbarrier:
+    //  - indexed family: the routed rows were copied into sorted order
+    //    beforehand, so block b's rows are rows b*block_m.. of that buffer and
+    //    one 3-D box (64 columns x block_m rows x 2 k steps) fills a stage;
+    //  - grouped families: one 2-D box (64 columns x block_m rows) per k step.
+    // Rows past the tensor and k steps past k read zeros.
+    if (lane == 0) {
+      RingPos bp;
+      uint32_t issued = 0;  // stages whose b_full phase this thread started
+      bool ok = true;
+      for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
+        const ItemDesc d = decode_item(args, it, num_blocks, bpe);
+        if (d.e < 0) continue;
+        const int box_row = (args.family == kMasked) ? d.e * args.m + (d.blk - d.e * bpe) * bm
+                                                     : d.blk * bm;
+        for (int st = 0; st < n_stp; ++st, bp.next(BS)) {
+          if (!wait_phase(B.be(bp.slot), bp.phase ^ 1, abort_flag, status, kWhereGatherB, tmo)) {
+            ok = false;
+            break;
           }
+          const int nks = min(2, max(0, args.k_steps - 2 * st));
+          const uint32_t dst = smem_u32(sm.b_ring + static_cast<size_t>(bp.slot) * b_stage_bytes);
+          if (nks == 0) {
+            mbar_arrive(B.bf(bp.slot));  // pad stage: no data
+          } else if (gather) {
+            mbar_arrive_expect_tx(B.bf(bp.slot), b_stage_bytes);
+            tma_load_3d(dst, &args.tmap, 0, box_row, 2 * st, B.bf(bp.slot));
+          } else {
+            mbar_arrive_expect_tx(B.bf(bp.slot), nks * b_step_bytes);
+            for (int j = 0; j < nks; ++j)
+              tma_load_2d(dst + j * b_step_bytes, &args.tmap, (2 * st + j) * kKStep, box_row,
+                          B.bf(bp.slot));
+          }
+          ++issued;
         }
       }
-      if (!ok) break;
-      ip.next(2);
+      if (!ok) {
+        // wait, bounded, for the last tensor copies issued
+        const uint32_t first = issued > static_cast<uint32_t>(BS) ? issued - BS : 0;
+        for (uint32_t x = first; x < issued; ++x) drain_phase(B.bf(x % BS), (x / BS) & 1, tmo);
+      }
     }
   } else if (warp >= kWarpDequant0 && warp < kWarpEpilogue0) {
     // ======================= dequantisation into TMEM =======================
-    // Warpgroup g dequantises the k steps with ks % 2 == g; thread r of the
-    // warpgroup owns weight row r of the tile, i.e. TMEM lane r.
-    const int g = (warp - kWarpDequant0) >> 2;
+    // Warpgroup wg dequantises the stages with global index u % 4 == wg into
+    // A slot wg; thread r of the warpgroup owns weight row r (TMEM lane r).
+    const int wg = (warp - kWarpDequant0) >> 2;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    RingPos wp, rp;
+    const uint32_t a_cols = tmem + lane_base + wg * kAColsPerSlot;
+    RingPos wp;            // weight slot of this warpgroup's next stage
+    wp.advance(wg, WS);    // its first stage is global stage wg (WS % 4 == 0)
+    uint32_t a_phase = 0;  // uses of A slot wg so far, mod 2
+    int u = 0;             // global stage index of this CTA
     bool ok = true;
     for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
       const ItemDesc d = decode_item(args, it, num_blocks, bpe);
       if (d.e < 0) continue;
-      for (int st = 0; st < n_wst; ++st, wp.next(WS)) {
-        const int wslot = wp.slot;
-        ok = __all_sync(0xffffffffu, wait_phase(B.wf(wslot), wp.phase, abort_flag, status,
-                                                 kWhereDequantW, tmo));
+      // item-local stages of this warpgroup: st = wg - u (mod 4), step 4
+      for (int st = (wg - u) & 3; st < n_stp; st += 4) {
+        ok = warp_wait_phase(B.wf(wp.slot), wp.phase, abort_flag, status, kWhereDequantW, tmo);
         if (!ok) break;
-        const int ks = 2 * st + g;
-        if (ks >= args.k_steps) {
-          __syncwarp();
-          if (lane == 0) mbar_arrive(B.we(wslot));
-          continue;
+        const int nks = min(2, max(0, args.k_steps - 2 * st));
+        const uint8_t* stp = sm.w_ring + static_cast<size_t>(wp.slot) * kWStageBytes;
+        uint4 qv[2][2];
+        uint32_t sc[2][2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          if (j < nks) {
+            const uint8_t* sj = stp + j * kStepBytes;
+            qv[j][0] = *reinterpret_cast<const uint4*>(sj + r * 16);
+            qv[j][1] = *reinterpret_cast<const uint4*>(sj + 2048 + r * 16);
+            sc[j][0] = *reinterpret_cast<const uint16_t*>(sj + kStepQBytes + r * 2);
+            sc[j][1] = *reinterpret_cast<const uint16_t*>(sj + kStepQBytes + 256 + r * 2);
+          }
         }
-        const uint8_t* stp = sm.w_ring + static_cast<size_t>(wslot) * kWStageBytes + g * kStepBytes;
-        const uint4 q0 = *reinterpret_cast<const uint4*>(stp + r * 16);
-        const uint4 q1 = *reinterpret_cast<const uint4*>(stp + 2048 + r * 16);
-        const uint32_t s0 = *reinterpret_cast<const uint16_t*>(stp + kStepQBytes + r * 2);
-        const uint32_t s1 = *reinterpret_cast<const uint16_t*>(stp + kStepQBytes + 256 + r * 2);
         __syncwarp();
-        if (lane == 0) mbar_arrive(B.we(wslot));
-        uint32_t v[32];
-        dequant_group(q0, s0, v);
-        dequant_group(q1, s1, v + 16);
-        const int slot = g * S + rp.slot;
-        ok = __all_sync(0xffffffffu, wait_phase(B.abe(slot), rp.phase ^ 1, abort_flag, status,
-                                                 kWhereDequantA, tmo));
+        if (lane == 0) mbar_arrive(B.we(wp.slot));
+        wp.advance(4, WS);
+        // the MMAs of this slot's previous use must be done before overwriting
+        ok = warp_wait_phase(B.ae(wg), a_phase ^ 1, abort_flag, status, kWhereDequantA, tmo);
         if (!ok) break;
         tc_fence_after();
-        tmem_st_32x32b_x32(tmem + lane_base + slot * kAColsPerSlot, v);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          if (j < nks) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {  // one 32-k group: 16 BF16x2 columns
+              uint32_t v[16];
+              dequant_group(qv[j][h], sc[j][h], v);
+              tmem_st_32x32b_x16(a_cols + j * kAColsPerStep + h * 16, v);
+            }
+          }
+        }
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(B.af(slot));
-        rp.next(S);
+        if (lane == 0) mbar_arrive(B.af(wg));
+        a_phase ^= 1u;
       }
+      u += n_stp;
     }
-  } else if (warp >= kWarpEpilogue0) {
+  } else if (warp >= kWarpEpilogue0 && warp < kWarpEpilogue0 + 4) {
     // ======================= epilogue =======================================
-    // Thread r owns weight row r of the tile (TMEM lane r): it reads the
-    // block's token columns of both partial accumulators and writes output
-    // column tile*128 + r.
+    // Thread r owns weight row r of the tile (TMEM lane r): it adds the
+    // partial accumulators of the block's token columns in a fixed order and
+    // writes output column tile*128 + r.
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const int live_parts = min(parts, args.k_steps);  // partial q holds k step q first
     RingPos ip, dp;
     for (int it = blockIdx.x; it < items; it += gridDim.x) {
       const ItemDesc d = decode_item(args, it, num_blocks, bpe);
       if (d.e < 0) continue;
       const int islot = ip.slot;
       const int dslot = dp.slot;
-      bool ok = wait_phase(B.accf(dslot), dp.phase, abort_flag, status, kWhereEpiAcc, tmo) &&
-                wait_phase(B.itf(islot), ip.phase, abort_flag, status, kWhereEpiItem, tmo);
-      if (!__all_sync(0xffffffffu, ok)) break;
+      if (!warp_wait_phase(B.accf(dslot), dp.phase, abort_flag, status, kWhereEpiAcc, tmo) ||
+          !warp_wait_phase(B.itf(islot), ip.phase, abort_flag, status, kWhereEpiItem, tmo))
+        break;
       tc_fence_after();
-      const int n16 = sm.info_n16[islot];  // gather warp 0's copy
+      const int n16 = sm.info_n16[islot];
       const int* idst = sm.info_dst + islot * bm;
       const float* iwt = sm.info_wt + islot * bm;
       const int ng = d.tile * kTileRows + r;
       const bool row_ok = ng < args.n;
-      const uint32_t dcol0 = tmem + lane_base + d_col_base + (dslot * 2) * args.d_cols;
-      const uint32_t dcol1 = dcol0 + args.d_cols;
-      const bool odd_steps = args.k_steps > 1;  // the odd-k accumulator holds data
+      const uint32_t dcol0 = tmem + lane_base + d_col_base + dslot * parts * args.d_cols;
       for (int j0 = 0; j0 < n16; j0 += 16) {
-        uint32_t v[16], w[16];
-        tmem_ld_32x32b_x16(dcol0 + j0, v);
-        if (odd_steps) tmem_ld_32x32b_x16(dcol1 + j0, w);
-        tmem_ld_wait();
+        float acc[16];
+        {
+          uint32_t v[16];
+          tmem_ld_32x32b_x16(dcol0 + j0, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) acc[jj] = __uint_as_float(v[jj]);
+        }
+        for (int p = 1; p < live_parts; ++p) {
+          uint32_t v[16];
+          tmem_ld_32x32b_x16(dcol0 + p * args.d_cols + j0, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) acc[jj] += __uint_as_float(v[jj]);
+        }
         if (!row_ok) continue;
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) {
-          // MMA column -> block row (gathered rows use 4 of every 8 columns)
-          const int c = j0 + jj;
-          int j = c;
-          if (gather) {
-            if ((c & 7) >= 4) continue;
-            j = (c >> 3) * 4 + (c & 3);
-          }
+          const int j = j0 + jj;  // MMA column = block row
           if (j >= bm) continue;
           const int dr = idst[j];
           if (dr < 0) continue;
-          const float x = odd_steps ? __uint_as_float(v[jj]) + __uint_as_float(w[jj])
-                                    : __uint_as_float(v[jj]);
           if (args.out_mode == kOutF32WeightedAdd) {
             float* o = static_cast<float*>(args.out) + static_cast<long long>(dr) * args.n + ng;
-            atomicAdd(o, iwt[j] * x);
+            atomicAdd(o, iwt[j] * acc[jj]);
           } else {
             __nv_bfloat16* o =
                 static_cast<__nv_bfloat16*>(args.out) + static_cast<long long>(dr) * args.n + ng;
-            *o = __float2bfloat16_rn(x);
+            *o = __float2bfloat16_rn(acc[jj]);
           }
         }
       }
@@ -613,7 +709,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(B.acce(dslot));
         mbar_arrive(B.ite(islot));
       }
-      ip.next(2);
+      ip.next(kItemSlots);
       dp.next(args.d_slots);
     }
   }
@@ -628,15 +724,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-size_t gemm_smem_bytes(int block_m, bool gather, int w_stages, int ring_slots) {
+size_t gemm_smem_bytes(int block_m, int w_stages, int b_stages) {
   size_t off = 1024;  // alignment slack
-  off += static_cast<size_t>(2 * ring_slots) * max_mma_n(block_m, gather) * 128;
+  off += static_cast<size_t>(b_stages) * 2 * block_m * 128;
   off += static_cast<size_t>(w_stages) * kWStageBytes;
-  off += 4 * static_cast<size_t>(block_m) * (4 + 4 + 4) + 4 * 4;
+  off += static_cast<size_t>(kItemSlots) * block_m * (4 + 4) + 2 * kItemSlots * 4;
   off = (off + 7) / 8 * 8;
-  off += (2 * w_stages + 6 * ring_slots + 10) * 8;
+  off += (2 * w_stages + 2 * b_stages + kNumBarsFixed) * 8;
   off += 8;
   return off;
+}
+
+bool tmem_accumulators(int block_m, int* d_cols, int* parts, int* d_slots) {
+  const int dcols = (block_m + 31) / 32 * 32;
+  const int free_cols = kTmemCols - kASlots * kAColsPerSlot;
+  int p = 4;
+  while (p > 1 && p * dcols > free_cols) p >>= 1;
+  if (p * dcols > free_cols) return false;
+  *d_cols = dcols;
+  *parts = p;
+  *d_slots = (2 * p * dcols <= free_cols) ? 2 : 1;
+  return true;
 }
 
 bool encode_act_tmap(CUtensorMap* map, const void* act, long long rows, int k, int box_rows) {
@@ -662,6 +770,32 @@ bool encode_act_tmap(CUtensorMap* map, const void* act, long long rows, int k, i
          CUDA_SUCCESS;
 }
 
+bool encode_permuted_tmap(CUtensorMap* map, const void* act, long long rows, int k_pad,
+                          int box_rows) {
+  using EncodeFn = PFN_cuTensorMapEncodeTiled_v12000;
+  static EncodeFn encode = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      encode = reinterpret_cast<EncodeFn>(fn);
+  });
+  if (encode == nullptr || rows <= 0 || rows > (1LL << 31) || k_pad <= 0 || k_pad % kKStep != 0)
+    return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kKStep), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(k_pad / kKStep)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(k_pad) * 2, kKStep * 2};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kKStep), static_cast<cuuint32_t>(box_rows), 2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(act), dims, strides,
+                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
 int device_sm_count(int device) {
   static std::mutex mu;
   static int cache[64] = {0};
@@ -678,7 +812,7 @@ int device_sm_count(int device) {
 cudaError_t launch_moe_gemm(const GemmArgs& args, int grid, cudaStream_t stream) {
   // At least 118 KB so that two CTAs never share an SM: each CTA allocates
   // all 512 TMEM columns.
-  size_t smem = gemm_smem_bytes(args.block_m, args.gather_rows != 0, args.w_stages, args.a_slots);
+  size_t smem = gemm_smem_bytes(args.block_m, args.w_stages, args.b_stages);
   if (smem < 118 * 1024) smem = 118 * 1024;
   cudaError_t err = cudaFuncSetAttribute(w4a16_moe_gemm_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -19,8 +19,10 @@
 
 namespace {
 
-// Largest workspace the no-allocation entry point can provide.
-constexpr size_t kNoAllocScratchBytes = 64 * 1024;
+// Largest workspace the no-allocation entry point can provide: the status
+// block plus the routed activation rows of, e.g., a gate_up call with
+// capacity 2048 and k 7168 (28 MiB).
+constexpr size_t kNoAllocScratchBytes = 32u << 20;
 
 // File-scope scratch: zero at module load, shared by every call on a device.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
@@ -52,8 +54,8 @@ extern "C" w4a16_status w4a16_moe_indexed_gemm_noalloc(
   if ((flags & ~(W4A16_FLAG_VALIDATE_ROUTING | W4A16_FLAG_ACCUMULATE |
                  W4A16_FLAG_SYNC_STATUS)) != 0)
     return W4A16_ERR_INVALID_ARG;
-  if (tokens < 0 || topk <= 0) return W4A16_ERR_INVALID_ARG;
-  const size_t need = w4a16_workspace_size(plan, tokens * topk, n);
+  if (tokens < 0 || topk <= 0 || k <= 0 || capacity < 0) return W4A16_ERR_INVALID_ARG;
+  const size_t need = w4a16_workspace_size(plan, capacity, k);
   if (need > kNoAllocScratchBytes) return W4A16_ERR_WORKSPACE;
 
   int device = 0;

@@ -63,7 +63,10 @@ class W4A16MoE:
         self.ntp = torch.empty(1, dtype=torch.int32, device=dev)
         self.inter_buf = torch.empty((numel, 2 * self.inter), dtype=torch.bfloat16, device=dev)
         self.act_buf = torch.empty((numel, self.inter), dtype=torch.bfloat16, device=dev)
-        self.workspace = ops.new_workspace(self.plan_gu, dev)
+        # one workspace for both GEMMs (ordered on one stream): status words
+        # and the routed rows of the wider activation (x, k = hidden)
+        self.workspace = ops.new_workspace(self.plan_gu, dev, self.capacity,
+                                           max(self.hidden, self.inter))
 
     def align(self, topk_ids: torch.Tensor, stream=None):
         return ops.w4a16_moe_align_block_size(

@@ -149,8 +149,10 @@ def w4a16_prepack_size(num_experts: int, n: int, k: int, group: int = 32,
     return int(out.value)
 
 
-def w4a16_workspace_size(plan: Plan, rows: int = 0, n: int = 0) -> int:
-    return int(load_library().w4a16_workspace_size(ctypes.byref(plan), rows, n))
+def w4a16_workspace_size(plan: Plan, rows: int = 0, k: int = 0) -> int:
+    """rows: routing capacity of an indexed GEMM (0 for grouped); k: the
+    GEMM's reduction length."""
+    return int(load_library().w4a16_workspace_size(ctypes.byref(plan), rows, k))
 
 
 # ---------------------------------------------------------------- device --
@@ -196,8 +198,8 @@ def w4a16_unpack(packed: torch.Tensor, num_experts: int, n: int, k: int, stream=
     return q, s
 
 
-def new_workspace(plan: Plan, device, rows: int = 0, n: int = 0) -> torch.Tensor:
-    return torch.zeros(w4a16_workspace_size(plan, rows, n), dtype=torch.uint8, device=device)
+def new_workspace(plan: Plan, device, rows: int = 0, k: int = 0) -> torch.Tensor:
+    return torch.zeros(w4a16_workspace_size(plan, rows, k), dtype=torch.uint8, device=device)
 
 
 def w4a16_moe_indexed_gemm(mode: int, packed: torch.Tensor, num_experts: int, n: int, k: int,
@@ -263,7 +265,7 @@ def w4a16_moe_indexed_gemm_noalloc(mode: int, packed: torch.Tensor, num_experts:
                                    out: Optional[torch.Tensor] = None, flags: int = 0,
                                    stream=None):
     """w4a16_moe_indexed_gemm for callers that cannot allocate device memory:
-    no workspace argument; the library's built-in 64 KiB device array serves
+    no workspace argument; the library's built-in 32 MiB device array serves
     as the workspace. Only ``out`` is allocated here when the caller passes
     none (a caller that cannot allocate passes its own)."""
     if out is None:
