@@ -269,12 +269,16 @@ w4a16_status w4a16_moe_indexed_gemm(int mode, const void* packed, int num_expert
     }
   }
 
-  if (mode == W4A16_DOWN && !(flags & W4A16_FLAG_ACCUMULATE) && tokens > 0) {
-    const cudaError_t e =
-        cudaMemsetAsync(out, 0, static_cast<size_t>(tokens) * n * sizeof(float), s);
-    if (e != cudaSuccess) return W4A16_ERR_CUDA;
+  // the down pass adds into `out`: zeroed first unless ACCUMULATE (by the
+  // row-permute kernel below, or here when there is nothing to multiply)
+  const size_t zero_bytes = (mode == W4A16_DOWN && !(flags & W4A16_FLAG_ACCUMULATE))
+                                ? static_cast<size_t>(tokens) * n * sizeof(float)
+                                : 0;
+  if (numel == 0 || capacity == 0) {
+    if (zero_bytes > 0 && cudaMemsetAsync(out, 0, zero_bytes, s) != cudaSuccess)
+      return W4A16_ERR_CUDA;
+    return W4A16_OK;
   }
-  if (numel == 0 || capacity == 0) return W4A16_OK;
 
   GemmArgs g;
   std::memset(&g, 0, sizeof(g));
@@ -293,8 +297,15 @@ w4a16_status w4a16_moe_indexed_gemm(int mode, const void* packed, int num_expert
   const int a_div = mode == W4A16_DOWN ? 1 : topk;
   if (!encode_permuted_tmap(&g.tmap, permuted, capacity, permuted_row_elems(k), bm))
     return W4A16_ERR_CUDA;
+  // (n * 4 bytes per row is a multiple of 16 when n % 4 == 0; otherwise the
+  // tail is cleared separately)
+  const size_t zero_vec_bytes = zero_bytes / 16 * 16;
+  if (zero_bytes != zero_vec_bytes &&
+      cudaMemsetAsync(static_cast<uint8_t*>(out) + zero_vec_bytes, 0, zero_bytes - zero_vec_bytes,
+                      s) != cudaSuccess)
+    return W4A16_ERR_CUDA;
   if (launch_permute_rows(a, k, a_div, static_cast<int>(numel), sorted_ids, num_tokens_padded,
-                          capacity, permuted, sms, s) != cudaSuccess)
+                          capacity, permuted, out, zero_vec_bytes, sms, s) != cudaSuccess)
     return W4A16_ERR_CUDA;
   g.act = permuted;
   g.gather_rows = 1;
@@ -317,7 +328,7 @@ w4a16_status w4a16_moe_indexed_gemm(int mode, const void* packed, int num_expert
   long long grid = plan->grid > 0 ? plan->grid : static_cast<long long>(sms) * plan->ctas_per_sm;
   const long long max_items = static_cast<long long>(capacity / bm) * g.n_tiles;
   grid = std::max<long long>(1, std::min(grid, max_items));
-  return cuda_status(launch_moe_gemm(g, static_cast<int>(grid), s));
+  return cuda_status(launch_moe_gemm(g, static_cast<int>(grid), true, s));
 }
 
 w4a16_status w4a16_moe_grouped_gemm(int kind, const void* packed, int num_experts, int n, int k,
@@ -406,7 +417,7 @@ w4a16_status w4a16_moe_grouped_gemm(int kind, const void* packed, int num_expert
                                : static_cast<long long>(num_experts) * ((m + bm - 1) / bm);
   long long grid = plan->grid > 0 ? plan->grid : static_cast<long long>(sms) * plan->ctas_per_sm;
   grid = std::max<long long>(1, std::min(grid, blocks * g.n_tiles));
-  return cuda_status(launch_moe_gemm(g, static_cast<int>(grid), s));
+  return cuda_status(launch_moe_gemm(g, static_cast<int>(grid), false, s));
 }
 
 w4a16_status w4a16_silu_and_mul(const uint16_t* in, int rows, int inter, uint16_t* out,

@@ -91,7 +91,9 @@ bool encode_act_tmap(CUtensorMap* map, const void* act, long long rows, int k, i
 // 64 chunks), box 64 x box_rows x 2 (two k steps), 128-byte swizzle.
 bool encode_permuted_tmap(CUtensorMap* map, const void* act, long long rows, int k_pad,
                           int box_rows);
-cudaError_t launch_moe_gemm(const GemmArgs& args, int grid, cudaStream_t stream);
+// dependent = true: launched as a programmatic dependent of the previous
+// kernel on `stream` (the row permute), see w4a16_permute_rows_kernel.
+cudaError_t launch_moe_gemm(const GemmArgs& args, int grid, bool dependent, cudaStream_t stream);
 
 cudaError_t launch_align(const int32_t* topk_ids, int numel, int num_experts, int block_m,
                          int capacity, int32_t* sorted_ids, int32_t* expert_ids,
@@ -103,9 +105,12 @@ cudaError_t launch_prepack(const uint8_t* q, const uint16_t* scales, int num_exp
 cudaError_t launch_unpack(const uint8_t* packed, int num_experts, int n, int k, uint8_t* q,
                           uint16_t* scales, cudaStream_t stream);
 
+// Routed rows into routing order; also zeroes zero_bytes (a multiple of 16)
+// at `zero` when given. Triggers the programmatic launch of the next kernel.
 cudaError_t launch_permute_rows(const uint16_t* a, int k, int a_div, int numel,
                                 const int32_t* sorted_ids, const int32_t* num_tokens_padded,
-                                int capacity, uint16_t* dst, int sms, cudaStream_t stream);
+                                int capacity, uint16_t* dst, void* zero, size_t zero_bytes,
+                                int sms, cudaStream_t stream);
 
 cudaError_t launch_silu_and_mul(const uint16_t* in, int rows, int inter, uint16_t* out,
                                 cudaStream_t stream);

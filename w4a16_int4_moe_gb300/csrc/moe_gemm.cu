@@ -548,6 +548,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     //    one 3-D box (64 columns x block_m rows x 2 k steps) fills a stage;
     //  - grouped families: one 2-D box (64 columns x block_m rows) per k step.
     // Rows past the tensor and k steps past k read zeros.
+    // the token rows may come from the previous grid (the row permute)
+    grid_dependency_wait();
     if (lane == 0) {
       RingPos bp;
       uint32_t issued = 0;  // stages whose b_full phase this thread started
@@ -654,6 +656,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = quarter * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const int live_parts = min(parts, args.k_steps);  // partial q holds k step q first
+    grid_dependency_wait();  // the previous grid may zero the output this one adds into
     RingPos ip, dp;
     for (int it = blockIdx.x; it < items; it += gridDim.x) {
       const ItemDesc d = decode_item(args, it, num_blocks, bpe);
@@ -809,7 +812,7 @@ int device_sm_count(int device) {
   return cache[device];
 }
 
-cudaError_t launch_moe_gemm(const GemmArgs& args, int grid, cudaStream_t stream) {
+cudaError_t launch_moe_gemm(const GemmArgs& args, int grid, bool dependent, cudaStream_t stream) {
   // At least 118 KB so that two CTAs never share an SM: each CTA allocates
   // all 512 TMEM columns.
   size_t smem = gemm_smem_bytes(args.block_m, args.w_stages, args.b_stages);
@@ -818,8 +821,17 @@ cudaError_t launch_moe_gemm(const GemmArgs& args, int grid, cudaStream_t stream)
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  w4a16_moe_gemm_kernel<<<grid, kThreads, smem, stream>>>(args);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = dependent ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, w4a16_moe_gemm_kernel, args);
 }
 
 }  // namespace w4a16

@@ -18,11 +18,24 @@
 
 namespace w4a16 {
 
-// One thread per 16-byte chunk of a destination row.
+// One thread per 16-byte chunk of a destination row; the same grid also
+// zeroes `zero` (zero_vec16 chunks of 16 bytes, the down pass's FP32 output)
+// when it is given. The GEMM that consumes these rows is launched as a
+// programmatic dependent of this grid: it may start (and stream weights)
+// while this grid still runs, and waits for its completion before it reads
+// the rows or adds into the output.
 __global__ void w4a16_permute_rows_kernel(const uint16_t* __restrict__ a, int k, int k_pad,
                                           int a_div, int numel, const int32_t* __restrict__ sorted_ids,
                                           const int32_t* __restrict__ num_tokens_padded,
-                                          int capacity, uint16_t* __restrict__ dst) {
+                                          int capacity, uint16_t* __restrict__ dst,
+                                          uint4* __restrict__ zero, long long zero_vec16) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  {
+    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+         i < zero_vec16; i += stride)
+      zero[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
   int rows = __ldg(num_tokens_padded);
   rows = min(max(rows, 0), capacity);
   const int chunks = k_pad / 8;
@@ -43,16 +56,20 @@ __global__ void w4a16_permute_rows_kernel(const uint16_t* __restrict__ a, int k,
 
 cudaError_t launch_permute_rows(const uint16_t* a, int k, int a_div, int numel,
                                 const int32_t* sorted_ids, const int32_t* num_tokens_padded,
-                                int capacity, uint16_t* dst, int sms, cudaStream_t stream) {
+                                int capacity, uint16_t* dst, void* zero, size_t zero_bytes,
+                                int sms, cudaStream_t stream) {
   const int k_pad = permuted_row_elems(k);
   const long long total = static_cast<long long>(capacity) * (k_pad / 8);
-  if (total == 0) return cudaSuccess;
+  const long long zvec = static_cast<long long>(zero_bytes / 16);
+  const long long work = total > zvec ? total : zvec;
+  if (work == 0) return cudaSuccess;
   const int threads = 256;
-  const long long want = (total + threads - 1) / threads;
+  const long long want = (work + threads - 1) / threads;
   const long long cap = static_cast<long long>(sms > 0 ? sms : 1) * 8;
   const int blocks = static_cast<int>(want < cap ? want : cap);
-  w4a16_permute_rows_kernel<<<blocks, threads, 0, stream>>>(a, k, k_pad, a_div, numel, sorted_ids,
-                                                            num_tokens_padded, capacity, dst);
+  w4a16_permute_rows_kernel<<<blocks, threads, 0, stream>>>(
+      a, k, k_pad, a_div, numel, sorted_ids, num_tokens_padded, capacity, dst,
+      static_cast<uint4*>(zero), zvec);
   return cudaGetLastError();
 }
 
