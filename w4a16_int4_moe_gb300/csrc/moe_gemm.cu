@@ -741,7 +741,7 @@ size_t gemm_smem_bytes(int block_m, int w_stages, int b_stages) {
 bool tmem_accumulators(int block_m, int* d_cols, int* parts, int* d_slots) {
   const int dcols = (block_m + 31) / 32 * 32;
   const int free_cols = kTmemCols - kASlots * kAColsPerSlot;
-  int p = 4;
+  int p = kMaxIssuers;
   while (p > 1 && p * dcols > free_cols) p >>= 1;
   if (p * dcols > free_cols) return false;
   *d_cols = dcols;
