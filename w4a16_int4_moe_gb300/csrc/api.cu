@@ -45,14 +45,15 @@ struct Pipeline {
 // dequant warpgroups owns every fourth stage); plan.b_stages is the
 // activation ring depth in k steps (a multiple of 4: an even number of
 // stages).
-bool plan_pipeline(const w4a16_plan_t& p, Pipeline* out) {
+bool plan_pipeline(const w4a16_plan_t& p, int k, Pipeline* out) {
   if (p.block_m < 16 || p.block_m > 128 || p.block_m % 16 != 0) return false;
   if (p.bn != kTileRows || p.bk != kKStep || p.split_k != 1 || p.layout != W4A16_LAYOUT_KTILE64)
     return false;
   if (p.stages < 4 || p.stages > 16 || p.b_stages < 8 || p.b_stages > 32 || p.b_stages % 4 != 0)
     return false;
   Pipeline pl;
-  if (!tmem_accumulators(p.block_m, &pl.d_cols, &pl.parts, &pl.d_slots)) return false;
+  if (!tmem_accumulators(p.block_m, packed_ksteps(k), &pl.d_cols, &pl.parts, &pl.d_slots))
+    return false;
   pl.w_stages = p.stages / 4 * 4;
   pl.b_stages = p.b_stages / 2;
   pl.smem = gemm_smem_bytes(p.block_m, pl.w_stages, pl.b_stages);
@@ -237,7 +238,7 @@ w4a16_status w4a16_moe_indexed_gemm(int mode, const void* packed, int num_expert
   if (workspace == nullptr || ws_bytes < w4a16_workspace_size(plan, capacity, k))
     return W4A16_ERR_WORKSPACE;
   Pipeline pl;
-  if (!plan_pipeline(*plan, &pl)) return W4A16_ERR_INVALID_ARG;
+  if (!plan_pipeline(*plan, k, &pl)) return W4A16_ERR_INVALID_ARG;
   const int bm = plan->block_m;
   if (capacity % bm != 0) return W4A16_ERR_INVALID_ARG;
   const long long numel = static_cast<long long>(tokens) * topk;
@@ -357,7 +358,7 @@ w4a16_status w4a16_moe_grouped_gemm(int kind, const void* packed, int num_expert
   }
   if (workspace == nullptr || ws_bytes < kStatusBytes) return W4A16_ERR_WORKSPACE;
   Pipeline pl;
-  if (!plan_pipeline(*plan, &pl)) return W4A16_ERR_INVALID_ARG;
+  if (!plan_pipeline(*plan, k, &pl)) return W4A16_ERR_INVALID_ARG;
   const int bm = plan->block_m;
   const long long rows_total =
       kind == W4A16_GROUPED_MASKED ? static_cast<long long>(num_experts) * m : m;

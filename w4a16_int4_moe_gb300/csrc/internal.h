@@ -81,10 +81,11 @@ struct GemmArgs {
 
 int device_sm_count(int device);
 size_t gemm_smem_bytes(int block_m, int w_stages, int b_stages);
-// TMEM split for a block of block_m rows: columns of one accumulator, the
-// number of partial accumulators (MMA issuers) and of accumulator slots.
+// TMEM split for a block of block_m rows and a reduction of k_steps 64-k
+// steps: columns of one accumulator, the number of partial accumulators (MMA
+// issuers) and of accumulator slots.
 // False when even one accumulator does not fit.
-bool tmem_accumulators(int block_m, int* d_cols, int* parts, int* d_slots);
+bool tmem_accumulators(int block_m, int k_steps, int* d_cols, int* parts, int* d_slots);
 // 2-D map of BF16 [rows, k] (box 64 x box_rows, 128-byte swizzle).
 bool encode_act_tmap(CUtensorMap* map, const void* act, long long rows, int k, int box_rows);
 // 3-D map of the permuted rows [rows, k_pad]: dims (64 columns, rows, k_pad /

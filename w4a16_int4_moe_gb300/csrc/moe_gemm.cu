@@ -56,9 +56,11 @@ constexpr int kWStageBytes = 2 * kStepBytes;  // one stage = 2 k steps of packed
 constexpr int kASlots = 4;                    // A slots in TMEM = dequant warpgroups
 constexpr int kAColsPerSlot = 64;             // 2 k steps x 64 BF16 of K per TMEM lane
 constexpr int kAColsPerStep = 32;
-constexpr int kItemSlots = 4;                 // routing-info ring depth (items)
+constexpr int kItemSlots = 8;                 // routing-info ring depth (items)
+constexpr int kMaxDSlots = 4;                 // accumulator slots (items in flight in TMEM)
 constexpr int kMaxIssuers = 4;
 constexpr int kTmemCols = 512;
+constexpr int kEpiTileBytes = 4 * 16 * 32 * 4;  // epilogue transpose staging
 
 // Warp roles. The dequant and epilogue warpgroups start at multiples of 4
 // warps, so that warp % 4 selects the TMEM lane quarter each warp may access.
@@ -84,6 +86,7 @@ struct Smem {
   float* info_wt;       // [kItemSlots][block_m]: top-k weight (down pass)
   int* info_n16;        // [kItemSlots]: MMA N of the item
   int* info_rows;       // [kItemSlots]: real rows (last real row + 1)
+  float* epi_tile;      // [4 epilogue warps][16 token rows][32 weight rows]
   uint64_t* bars;
   uint32_t* tmem_base;
   volatile int* abort_flag;
@@ -105,7 +108,7 @@ struct Bars {
   __device__ uint32_t acce(int i) const { return acc_empty + 8u * i; }
   __device__ uint32_t fin(int i) const { return final_bar + 8u * i; }
 };
-constexpr int kNumBarsFixed = 2 * kASlots + 2 * kItemSlots + 2 + 2 + kMaxIssuers;
+constexpr int kNumBarsFixed = 2 * kASlots + 2 * kItemSlots + 2 * kMaxDSlots + kMaxIssuers;
 
 __device__ __forceinline__ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -314,6 +317,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   off += kItemSlots * sizeof(int);
   sm.info_rows = reinterpret_cast<int*>(base + off);
   off += kItemSlots * sizeof(int);
+  off = align_up(off, 16);
+  sm.epi_tile = reinterpret_cast<float*>(base + off);
+  off += kEpiTileBytes;
   off = align_up(off, 8);
   sm.bars = reinterpret_cast<uint64_t*>(base + off);
   off += (2 * WS + 2 * BS + kNumBarsFixed) * 8;
@@ -341,9 +347,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     B.item_empty = b0;
     b0 += 8 * kItemSlots;
     B.acc_full = b0;
-    b0 += 16;
+    b0 += 8 * kMaxDSlots;
     B.acc_empty = b0;
-    b0 += 16;
+    b0 += 8 * kMaxDSlots;
     B.final_bar = b0;
   }
   // issuers that read each stage (each commits once per stage)
@@ -366,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(B.itf(i), 1);  // the router warp
       mbar_init(B.ite(i), 4);  // the 4 epilogue warps
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kMaxDSlots; ++i) {
       mbar_init(B.accf(i), parts);  // one tcgen05.commit per MMA issuer
       mbar_init(B.acce(i), 4);
     }
@@ -649,13 +655,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= kWarpEpilogue0 && warp < kWarpEpilogue0 + 4) {
     // ======================= epilogue =======================================
-    // Thread r owns weight row r of the tile (TMEM lane r): it adds the
-    // partial accumulators of the block's token columns in a fixed order and
-    // writes output column tile*128 + r.
+    // Warp q reads TMEM lanes 32q..32q+31 (weight rows of the tile = output
+    // columns tile*128 + 32q + lane): per 16 token columns it adds the
+    // partial accumulators in a fixed order, stages the 32 x 16 values
+    // transposed in shared memory, and then writes 4 consecutive output
+    // columns of one token row per operation (an 8-byte BF16 store, or a
+    // float4 atomic add of the top-k weighted values in the down pass).
     const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const int live_parts = min(parts, args.k_steps);  // partial q holds k step q first
+    float* tile = sm.epi_tile + quarter * (16 * 32);    // [16 token rows][32 weight rows]
+    const int c4 = lane & 7;                            // 4-column group of this lane
+    const int jr0 = lane >> 3;                          // first token row of this lane
+    const bool vec4 = (args.n & 3) == 0;
     grid_dependency_wait();  // the previous grid may zero the output this one adds into
     RingPos ip, dp;
     for (int it = blockIdx.x; it < items; it += gridDim.x) {
@@ -667,44 +679,74 @@ __global__ void __launch_bounds__(kThreads, 1)
           !warp_wait_phase(B.itf(islot), ip.phase, abort_flag, status, kWhereEpiItem, tmo))
         break;
       tc_fence_after();
-      const int n16 = sm.info_n16[islot];
+      const int rows = sm.info_rows[islot];
       const int* idst = sm.info_dst + islot * bm;
       const float* iwt = sm.info_wt + islot * bm;
-      const int ng = d.tile * kTileRows + r;
-      const bool row_ok = ng < args.n;
+      // first output column of this lane's 4-column group
+      const int ng = d.tile * kTileRows + quarter * 32 + 4 * c4;
       const uint32_t dcol0 = tmem + lane_base + d_col_base + dslot * parts * args.d_cols;
-      for (int j0 = 0; j0 < n16; j0 += 16) {
-        float acc[16];
-        {
-          uint32_t v[16];
-          tmem_ld_32x32b_x16(dcol0 + j0, v);
+      for (int j0 = 0; j0 < rows; j0 += 16) {
+        // the first two partial accumulators with one TMEM round trip, any
+        // further ones one by one; summed in the fixed order
+        // ((p0 + p1) + p2) + p3
+        uint32_t v[16], w[16];
+        tmem_ld_32x32b_x16(dcol0 + j0, v);
+        if (live_parts > 1) tmem_ld_32x32b_x16(dcol0 + args.d_cols + j0, w);
+        tmem_ld_wait();
+        if (live_parts > 1) {
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj)
+            v[jj] = __float_as_uint(__uint_as_float(v[jj]) + __uint_as_float(w[jj]));
+        }
+        for (int p = 2; p < live_parts; ++p) {
+          tmem_ld_32x32b_x16(dcol0 + p * args.d_cols + j0, w);
           tmem_ld_wait();
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) acc[jj] = __uint_as_float(v[jj]);
+          for (int jj = 0; jj < 16; ++jj)
+            v[jj] = __float_as_uint(__uint_as_float(v[jj]) + __uint_as_float(w[jj]));
         }
-        for (int p = 1; p < live_parts; ++p) {
-          uint32_t v[16];
-          tmem_ld_32x32b_x16(dcol0 + p * args.d_cols + j0, v);
-          tmem_ld_wait();
+        // transpose through shared memory: tile[jj][lane] = value of token
+        // column j0 + jj for weight row lane
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) acc[jj] += __uint_as_float(v[jj]);
-        }
-        if (!row_ok) continue;
-#pragma unroll
-        for (int jj = 0; jj < 16; ++jj) {
-          const int j = j0 + jj;  // MMA column = block row
-          if (j >= bm) continue;
+        for (int jj = 0; jj < 16; ++jj) tile[jj * 32 + lane] = __uint_as_float(v[jj]);
+        __syncwarp();
+        // lane (jr, c4) writes token row j0 + jr, columns ng..ng+3
+        for (int jr = jr0; jr < 16 && j0 + jr < rows; jr += 4) {
+          const int j = j0 + jr;
           const int dr = idst[j];
-          if (dr < 0) continue;
+          if (dr < 0 || ng >= args.n) continue;
+          const float4 x = *reinterpret_cast<const float4*>(tile + jr * 32 + 4 * c4);
           if (args.out_mode == kOutF32WeightedAdd) {
             float* o = static_cast<float*>(args.out) + static_cast<long long>(dr) * args.n + ng;
-            atomicAdd(o, iwt[j] * acc[jj]);
+            const float wt = iwt[j];
+            if (vec4) {
+              atomicAdd(reinterpret_cast<float4*>(o),
+                        make_float4(wt * x.x, wt * x.y, wt * x.z, wt * x.w));
+            } else {
+              atomicAdd(o, wt * x.x);
+              if (ng + 1 < args.n) atomicAdd(o + 1, wt * x.y);
+              if (ng + 2 < args.n) atomicAdd(o + 2, wt * x.z);
+              if (ng + 3 < args.n) atomicAdd(o + 3, wt * x.w);
+            }
           } else {
             __nv_bfloat16* o =
                 static_cast<__nv_bfloat16*>(args.out) + static_cast<long long>(dr) * args.n + ng;
-            *o = __float2bfloat16_rn(acc[jj]);
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(x.x, x.y);
+            const __nv_bfloat162 hi = __floats2bfloat162_rn(x.z, x.w);
+            if (vec4) {
+              uint2 pk;
+              pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+              pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+              *reinterpret_cast<uint2*>(o) = pk;
+            } else {
+              o[0] = lo.x;
+              if (ng + 1 < args.n) o[1] = lo.y;
+              if (ng + 2 < args.n) o[2] = hi.x;
+              if (ng + 3 < args.n) o[3] = hi.y;
+            }
           }
         }
+        __syncwarp();  // the tile is rewritten by the next 16 token columns
       }
       tc_fence_before();
       __syncwarp();
@@ -732,21 +774,26 @@ size_t gemm_smem_bytes(int block_m, int w_stages, int b_stages) {
   off += static_cast<size_t>(b_stages) * 2 * block_m * 128;
   off += static_cast<size_t>(w_stages) * kWStageBytes;
   off += static_cast<size_t>(kItemSlots) * block_m * (4 + 4) + 2 * kItemSlots * 4;
+  off = (off + 15) / 16 * 16 + kEpiTileBytes;
   off = (off + 7) / 8 * 8;
   off += (2 * w_stages + 2 * b_stages + kNumBarsFixed) * 8;
   off += 8;
   return off;
 }
 
-bool tmem_accumulators(int block_m, int* d_cols, int* parts, int* d_slots) {
+bool tmem_accumulators(int block_m, int k_steps, int* d_cols, int* parts, int* d_slots) {
   const int dcols = (block_m + 31) / 32 * 32;
   const int free_cols = kTmemCols - kASlots * kAColsPerSlot;
-  int p = kMaxIssuers;
+  // Four issuers by default; short reductions (a few stages per item) take
+  // two, so that more items fit in TMEM at once and the epilogue reads half
+  // as many partial accumulators per item.
+  int p = k_steps <= 8 ? 2 : kMaxIssuers;
   while (p > 1 && p * dcols > free_cols) p >>= 1;
   if (p * dcols > free_cols) return false;
   *d_cols = dcols;
   *parts = p;
-  *d_slots = (2 * p * dcols <= free_cols) ? 2 : 1;
+  const int slots = free_cols / (p * dcols);
+  *d_slots = slots < kMaxDSlots ? slots : kMaxDSlots;
   return true;
 }
 
