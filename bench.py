@@ -386,7 +386,7 @@ def run_ours(args):
             "traffic": None if traffic is None else traffic["dram_bytes_per_launch"],
             "algorithmic_bytes": work["gate_up"]["bytes"],
         },
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": 6 * args.steps,  # align, permute + gate_up, silu, permute + down
         "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "clocks": clk,
