@@ -237,7 +237,11 @@ w4a16_status w4a16_silu_and_mul(const uint16_t* in, int rows, int inter, uint16_
  * Synchronise `stream`, read the device status word of `workspace`, reset it
  * to zero, and return W4A16_OK or W4A16_ERR_TIMEOUT (a device-side wait of a
  * GEMM gave up after about a second; the kernel then ended early and its
- * output is incomplete). *detail (optional) receives the raw word.
+ * output is incomplete). *detail (optional) receives the raw word:
+ * 0x1000 | code of the wait that gave up.
+ * The bound, in SM clock cycles, is read from the environment variable
+ * W4A16_WAIT_TIMEOUT_CYCLES at each GEMM call (default 2e9); lowering it
+ * makes the failure path testable without any GPU fault.
  */
 w4a16_status w4a16_read_device_status(void* workspace, int* detail, void* stream);
 

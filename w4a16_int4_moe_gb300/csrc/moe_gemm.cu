@@ -139,8 +139,11 @@ __device__ __forceinline__ bool warp_wait_phase(uint32_t bar, uint32_t parity,
   return __all_sync(0xffffffffu, wait_phase(bar, parity, abort_flag, status, where, timeout));
 }
 
-// Drain wait (abort path): wait, with a bound, for a phase that copies
-// already issued will complete.
+// Drain wait (abort path): wait for a phase that copies or MMAs already
+// issued will complete. They finish within microseconds, so the bound is a
+// fixed, generous one (about 2 s) and never the wait timeout, which a caller
+// may set very short: a CTA must not exit while its copies still land.
+constexpr long long kDrainCycles = 4000000000LL;
 __device__ __forceinline__ void drain_phase(uint32_t bar, uint32_t parity, long long timeout) {
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity) && clock64() - t0 < timeout) {
@@ -446,7 +449,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) {
         // Let every copy already issued land before the CTA can exit.
         const uint32_t first = issued > static_cast<uint32_t>(WS) ? issued - WS : 0;
-        for (uint32_t u = first; u < issued; ++u) drain_phase(B.wf(u % WS), (u / WS) & 1, tmo);
+        for (uint32_t u = first; u < issued; ++u)
+          drain_phase(B.wf(u % WS), (u / WS) & 1, kDrainCycles);
       }
     }
   } else if ((warp >= kWarpMma0 && warp < kWarpDequant0) || warp == kWarpMma3) {
@@ -509,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // every MMA issued by this thread has finished once its final barrier flips
       tc_commit(B.fin(q));
-      drain_phase(B.fin(q), 0, tmo);
+      drain_phase(B.fin(q), 0, kDrainCycles);
     }
   } else if (warp == kWarpRouter) {
     // ======================= routing info, items ahead ======================
@@ -589,7 +593,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) {
         // wait, bounded, for the last tensor copies issued
         const uint32_t first = issued > static_cast<uint32_t>(BS) ? issued - BS : 0;
-        for (uint32_t x = first; x < issued; ++x) drain_phase(B.bf(x % BS), (x / BS) & 1, tmo);
+        for (uint32_t x = first; x < issued; ++x)
+          drain_phase(B.bf(x % BS), (x / BS) & 1, kDrainCycles);
       }
     }
   } else if (warp >= kWarpDequant0 && warp < kWarpEpilogue0) {
