@@ -49,7 +49,15 @@ typedef enum {
 } w4a16_status;
 
 /* GEMM modes of the indexed family. */
-enum { W4A16_GATE_UP = 0, W4A16_DOWN = 1 };
+enum {
+  W4A16_GATE_UP = 0,      /* out BF16 [tokens*topk, n]: the gate_up projection   */
+  W4A16_DOWN = 1,         /* out FP32 [tokens, n]: weighted scatter-add           */
+  W4A16_GATE_UP_SILU = 2  /* gate_up with the activation fused into the epilogue:
+                             out BF16 [tokens*topk, n/2] = bf16(silu(g) * u),
+                             g, u the BF16-rounded gate and up outputs; weights
+                             packed with W4A16_LAYOUT_KTILE64_GLU16 and the plan's
+                             layout set to it                                  */
+};
 /* Grouped families. */
 enum { W4A16_GROUPED_CONTIGUOUS = 0, W4A16_GROUPED_MASKED = 1 };
 /* Call flags. */
@@ -64,7 +72,15 @@ enum {
                                       zeroing it                            */
 };
 /* Packed weight layouts (w4a16_prepack). One layout serves every family. */
-enum { W4A16_LAYOUT_KTILE64 = 0 };
+enum {
+  W4A16_LAYOUT_KTILE64 = 0,      /* 128 consecutive rows per tile                */
+  W4A16_LAYOUT_KTILE64_GLU16 = 1 /* gate_up weights [2I, k] with gate rows [0, I)
+                                    and up rows [I, 2I): tile t holds, for each
+                                    of its four 32-row quarters q, gate rows
+                                    64t+16q .. +15 then the matching up rows
+                                    I+64t+16q .. +15 (I % 64 == 0), so that the
+                                    epilogue pairs them inside one warp        */
+};
 
 /* Static description of a status code. Never NULL. */
 const char* w4a16_status_string(int status);
@@ -156,8 +172,9 @@ w4a16_status w4a16_prepack(const uint8_t* q, const uint16_t* scales, int num_exp
                            int k, int group, int layout, void* packed, size_t packed_bytes,
                            void* stream);
 
-/* Inverse of w4a16_prepack (for checking a packed blob byte for byte). */
-w4a16_status w4a16_unpack(const void* packed, int num_experts, int n, int k, uint8_t* q,
+/* Inverse of w4a16_prepack (for checking a packed blob byte for byte);
+ * `layout` is the one the blob was packed with. */
+w4a16_status w4a16_unpack(const void* packed, int num_experts, int n, int k, int layout, uint8_t* q,
                           uint16_t* scales, void* stream);
 
 /*
@@ -188,6 +205,14 @@ size_t w4a16_workspace_size(const w4a16_plan_t* plan, int rows, int k);
  *            out[i / topk, :] += topk_weights.flat[i] * ( a[i, :] . W_e^T ).
  *            `out` is zeroed first unless W4A16_FLAG_ACCUMULATE. Summation
  *            order across the top-k rows of a token is not fixed.
+ *   GATE_UP_SILU: as GATE_UP with n = 2*inter (gate rows, then up rows), but
+ *            out BF16 [tokens*topk, n/2] receives
+ *            bf16( silu(g) * u ), g = bf16(x . Wgate^T), u = bf16(x . Wup^T),
+ *            silu(g) = g / (1 + exp(-g)) in fp32: the same values as GATE_UP
+ *            followed by w4a16_silu_and_mul, in one pass (the activation is
+ *            this library's reading, see w4a16_silu_and_mul). Requires
+ *            packed with W4A16_LAYOUT_KTILE64_GLU16, plan->layout equal to
+ *            it, and n % 128 == 0.
  * The routing buffers may be over-allocated (capacity rows); the grid does
  * not depend on their contents. Blocks with expert -1 and sentinel rows are
  * skipped; ids out of range are ignored, never dereferenced.

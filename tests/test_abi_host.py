@@ -77,6 +77,10 @@ def test_prepack_size_and_unsupported_schemes(lib):
     assert lib.w4a16_prepack_size(1, 128, 100, 32, 0, ctypes.byref(out)) == ops.W4A16_ERR_UNSUPPORTED
     assert lib.w4a16_prepack_size(1, 128, 128, 32, 7, ctypes.byref(out)) == ops.W4A16_ERR_UNSUPPORTED
     assert lib.w4a16_prepack(None, None, 1, 128, 128, 16, 0, None, 0, None) == ops.W4A16_ERR_UNSUPPORTED
+    # the interleaved gate/up layout needs whole 128-row tiles (n = 2I, I % 64 == 0)
+    glu = ops.W4A16_LAYOUT_KTILE64_GLU16
+    assert ops.w4a16_prepack_size(2, 512, 256, layout=glu) == ops.w4a16_prepack_size(2, 512, 256)
+    assert lib.w4a16_prepack_size(1, 192, 128, 32, glu, ctypes.byref(out)) == ops.W4A16_ERR_UNSUPPORTED
     assert lib.w4a16_prepack(None, None, 1, 128, 128, 32, 0, None, 0, None) == ops.W4A16_ERR_INVALID_ARG
 
 
@@ -123,6 +127,18 @@ def test_gemm_argument_checks_before_any_launch(lib):
         assert lib.w4a16_moe_indexed_gemm(0, fake, 8, 1024, 512, fake, 64, 2, fake, fake, fake,
                                           256, None, fake, 0, ctypes.byref(bad), fake, 1 << 30,
                                           None) == ops.W4A16_ERR_INVALID_ARG, field
+    # the fused activation needs the interleaved packing named in the plan, and
+    # the other modes the plain one
+    glu_plan = ops.Plan.from_buffer_copy(plan)
+    glu_plan.layout = ops.W4A16_LAYOUT_KTILE64_GLU16
+    assert call(mode=ops.W4A16_GATE_UP_SILU) == ops.W4A16_ERR_INVALID_ARG
+    assert lib.w4a16_moe_indexed_gemm(ops.W4A16_GATE_UP, fake, 8, 1024, 512, fake, 64, 2, fake,
+                                      fake, fake, 256, None, fake, 0, ctypes.byref(glu_plan),
+                                      fake, 1 << 30, None) == ops.W4A16_ERR_INVALID_ARG
+    assert lib.w4a16_moe_indexed_gemm(ops.W4A16_GATE_UP_SILU, fake, 8, 1000, 512, fake, 64, 2,
+                                      fake, fake, fake, 256, None, fake, 0,
+                                      ctypes.byref(glu_plan), fake, 1 << 30, None) \
+        == ops.W4A16_ERR_UNSUPPORTED   # n not whole 128-row tiles
     bad = ops.Plan.from_buffer_copy(plan)
     bad.split_k = 2
     assert lib.w4a16_moe_indexed_gemm(0, fake, 8, 1024, 512, fake, 64, 2, fake, fake, fake, 256,

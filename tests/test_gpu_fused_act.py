@@ -1,0 +1,106 @@
+"""The gate_up GEMM with the activation fused into its epilogue
+(W4A16_GATE_UP_SILU over W4A16_LAYOUT_KTILE64_GLU16 weights).
+
+It must give exactly the bits of the unfused path (gate_up to BF16, then
+w4a16_silu_and_mul), and match the oracle's silu(g) * up on the BF16 gate_up
+outputs within the activation tolerance.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from w4a16_int4_moe_gb300 import moe as moe_mod
+from w4a16_int4_moe_gb300 import ops
+from w4a16_int4_moe_gb300 import workloads as wl
+from helpers import assert_close, bf16_bits, bf16_tensor, dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _fused_and_unfused(p, device, bm=None):
+    q, s = dev(p.q_gu, device), dev(p.s_gu.view(np.int16), device)
+    pk = ops.w4a16_prepack(q, s)
+    pk_glu = ops.w4a16_prepack(q, s, layout=ops.W4A16_LAYOUT_KTILE64_GLU16)
+    plan = ops.w4a16_plan(p.tokens, p.topk, p.num_experts, 2 * p.inter, p.hidden,
+                          p.tok_e_hint())
+    if bm:
+        plan.block_m = bm
+        plan.stages, plan.b_stages = min(plan.stages, 8), 8   # fit larger token stages
+    sid, eid, ntp = ops.w4a16_moe_align_block_size(dev(p.topk_ids, device), p.num_experts,
+                                                   plan.block_m)
+    ws = ops.new_workspace(plan, device, sid.numel(), p.hidden)
+    x = bf16_tensor(p.x, device)
+    g = ops.w4a16_moe_indexed_gemm(ops.W4A16_GATE_UP, pk, p.num_experts, 2 * p.inter, p.hidden,
+                                   x, p.tokens, p.topk, sid, eid, ntp, plan, ws)
+    act_ref = ops.w4a16_silu_and_mul(g)
+    glu_plan = ops.Plan.from_buffer_copy(plan)
+    glu_plan.layout = ops.W4A16_LAYOUT_KTILE64_GLU16
+    act = torch.full((p.numel, p.inter), float("nan"), dtype=torch.bfloat16, device=device)
+    ops.w4a16_moe_indexed_gemm(ops.W4A16_GATE_UP_SILU, pk_glu, p.num_experts, 2 * p.inter,
+                               p.hidden, x, p.tokens, p.topk, sid, eid, ntp, glu_plan, ws,
+                               out=act)
+    st, word = ops.w4a16_read_device_status(ws)
+    assert st == ops.W4A16_OK, hex(word)
+    routed = ((p.topk_ids >= 0) & (p.topk_ids < p.num_experts)).reshape(-1)
+    return bf16_bits(g), bf16_bits(act_ref), bf16_bits(act), routed
+
+
+@pytest.mark.parametrize("bm", [16, 32, 64])
+def test_fused_activation_tiny(cuda_dev, bm):
+    p = wl.tiny(seed=51)
+    g_bits, ref_bits, act_bits, routed = _fused_and_unfused(p, cuda_dev, bm)
+    np.testing.assert_array_equal(act_bits[routed], ref_bits[routed])
+    a_ref = oracle.bf16_bits_to_f64(oracle.silu_and_mul(g_bits[routed]))
+    assert_close(oracle.bf16_bits_to_f64(act_bits[routed]), a_ref, f"fused act bm={bm}",
+                 rel_l2=4e-3, max_abs_frac=1e-2)
+    # against the float64 chain from the inputs: gate_up, BF16, then silu * up
+    g_ref = oracle.indexed_gate_up(p.x, p.topk_ids, p.q_gu, p.s_gu)
+    a_chain = oracle.silu_and_mul(oracle.f64_to_bf16_bits(np.nan_to_num(g_ref[routed])))
+    assert_close(oracle.bf16_bits_to_f64(act_bits[routed]), oracle.bf16_bits_to_f64(a_chain),
+                 f"fused act vs oracle chain bm={bm}", rel_l2=1e-2, max_abs_frac=2e-2)
+
+
+def test_fused_activation_tp8_shape(cuda_dev):
+    p = wl.uniform_problem(64, 1024, 256, 48, 8, seed=52)   # I = 256: 4 fused tiles
+    g_bits, ref_bits, act_bits, routed = _fused_and_unfused(p, cuda_dev)
+    np.testing.assert_array_equal(act_bits[routed], ref_bits[routed])
+
+
+def test_fused_activation_ep8_decode_full_size(cuda_dev):
+    p = wl.ep8_decode()
+    g_bits, ref_bits, act_bits, routed = _fused_and_unfused(p, cuda_dev)
+    np.testing.assert_array_equal(act_bits[routed], ref_bits[routed])
+    # sampled act columns against the oracle on their gate and up columns
+    cols = np.array([0, 1, 63, 64, 511, 1000, 1337, 2047])
+    g_ref = oracle.indexed_gate_up(p.x, p.topk_ids, p.q_gu, p.s_gu,
+                                   cols=np.concatenate([cols, p.inter + cols]))
+    gb = oracle.f64_to_bf16_bits(np.nan_to_num(g_ref[routed]))
+    g = oracle.bf16_bits_to_f64(gb[:, :len(cols)])
+    u = oracle.bf16_bits_to_f64(gb[:, len(cols):])
+    a_ref = g / (1.0 + np.exp(-g)) * u
+    assert_close(oracle.bf16_bits_to_f64(act_bits[routed][:, cols]), a_ref,
+                 "fused act EP8 sampled columns", rel_l2=1e-2, max_abs_frac=2e-2)
+
+
+def test_layer_forward_with_fused_activation(cuda_dev):
+    p = wl.tiny(seed=53)
+
+    def t(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(cuda_dev)
+
+    dn = moe_mod.PackedExperts.from_checkpoint(t(p.q_dn), t(p.s_dn.view(np.int16)))
+    gu = moe_mod.PackedExperts.from_checkpoint(t(p.q_gu), t(p.s_gu.view(np.int16)))
+    gu_glu = moe_mod.PackedExperts.from_checkpoint(
+        t(p.q_gu), t(p.s_gu.view(np.int16)), layout=ops.W4A16_LAYOUT_KTILE64_GLU16)
+    x, ids, w = bf16_tensor(p.x, cuda_dev), t(p.topk_ids), t(p.topk_weights)
+    y_plain = moe_mod.W4A16MoE(gu, dn, p.topk, p.tokens, device=cuda_dev).forward(x, ids, w)
+    layer = moe_mod.W4A16MoE(gu_glu, dn, p.topk, p.tokens, device=cuda_dev)
+    assert layer.fused_act
+    y_fused = layer.forward(x, ids, w)
+    torch.cuda.synchronize()
+    # same activation bits, so the down pass sees the same input; only the
+    # order of its atomic adds may differ
+    assert_close(y_fused.cpu().numpy(), y_plain.cpu().numpy(), "layer fused vs plain",
+                 rel_l2=1e-6, max_abs_frac=1e-6)

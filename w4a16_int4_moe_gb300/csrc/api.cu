@@ -47,8 +47,8 @@ struct Pipeline {
 // stages).
 bool plan_pipeline(const w4a16_plan_t& p, int k, Pipeline* out) {
   if (p.block_m < 16 || p.block_m > 128 || p.block_m % 16 != 0) return false;
-  if (p.bn != kTileRows || p.bk != kKStep || p.split_k != 1 || p.layout != W4A16_LAYOUT_KTILE64)
-    return false;
+  if (p.bn != kTileRows || p.bk != kKStep || p.split_k != 1) return false;
+  if (p.layout != W4A16_LAYOUT_KTILE64 && p.layout != W4A16_LAYOUT_KTILE64_GLU16) return false;
   if (p.stages < 4 || p.stages > 16 || p.b_stages < 8 || p.b_stages > 32 || p.b_stages % 4 != 0)
     return false;
   Pipeline pl;
@@ -177,8 +177,11 @@ w4a16_status w4a16_moe_align_block_size(const int32_t* topk_ids, int tokens, int
 w4a16_status w4a16_prepack_size(int num_experts, int n, int k, int group, int layout,
                                 size_t* bytes) {
   if (bytes == nullptr || num_experts <= 0 || n <= 0 || k <= 0) return W4A16_ERR_INVALID_ARG;
-  if (group != kGroup || k % kGroup != 0 || layout != W4A16_LAYOUT_KTILE64)
+  if (group != kGroup || k % kGroup != 0) return W4A16_ERR_UNSUPPORTED;
+  if (layout != W4A16_LAYOUT_KTILE64 && layout != W4A16_LAYOUT_KTILE64_GLU16)
     return W4A16_ERR_UNSUPPORTED;
+  // the interleaved gate/up layout pairs 64-row halves of the two projections
+  if (layout == W4A16_LAYOUT_KTILE64_GLU16 && n % kTileRows != 0) return W4A16_ERR_UNSUPPORTED;
   *bytes = static_cast<size_t>(num_experts) * packed_expert_bytes(n, k);
   return W4A16_OK;
 }
@@ -193,20 +196,23 @@ w4a16_status w4a16_prepack(const uint8_t* q, const uint16_t* scales, int num_exp
   if (!aligned16(q) || !aligned16(packed) || (reinterpret_cast<uintptr_t>(scales) & 1u))
     return W4A16_ERR_INVALID_ARG;
   if (packed_bytes < need) return W4A16_ERR_INVALID_ARG;
-  return cuda_status(launch_prepack(q, scales, num_experts, n, k, static_cast<uint8_t*>(packed),
+  return cuda_status(launch_prepack(q, scales, num_experts, n, k, layout,
+                                    static_cast<uint8_t*>(packed),
                                     static_cast<cudaStream_t>(stream)));
 }
 
-w4a16_status w4a16_unpack(const void* packed, int num_experts, int n, int k, uint8_t* q,
-                          uint16_t* scales, void* stream) {
+w4a16_status w4a16_unpack(const void* packed, int num_experts, int n, int k, int layout,
+                          uint8_t* q, uint16_t* scales, void* stream) {
   if (packed == nullptr || q == nullptr || scales == nullptr || num_experts <= 0 || n <= 0 ||
       k <= 0)
     return W4A16_ERR_INVALID_ARG;
-  if (k % kGroup != 0) return W4A16_ERR_UNSUPPORTED;
+  size_t bytes = 0;
+  const w4a16_status st = w4a16_prepack_size(num_experts, n, k, kGroup, layout, &bytes);
+  if (st != W4A16_OK) return st;
   if (!aligned16(q) || !aligned16(packed) || (reinterpret_cast<uintptr_t>(scales) & 1u))
     return W4A16_ERR_INVALID_ARG;
-  return cuda_status(launch_unpack(static_cast<const uint8_t*>(packed), num_experts, n, k, q,
-                                   scales, static_cast<cudaStream_t>(stream)));
+  return cuda_status(launch_unpack(static_cast<const uint8_t*>(packed), num_experts, n, k, layout,
+                                   q, scales, static_cast<cudaStream_t>(stream)));
 }
 
 size_t w4a16_workspace_size(const w4a16_plan_t* plan, int rows, int k) {
@@ -222,7 +228,8 @@ w4a16_status w4a16_moe_indexed_gemm(int mode, const void* packed, int num_expert
                                     const float* topk_weights, void* out, int flags,
                                     const w4a16_plan_t* plan, void* workspace, size_t ws_bytes,
                                     void* stream) {
-  if (mode != W4A16_GATE_UP && mode != W4A16_DOWN) return W4A16_ERR_INVALID_ARG;
+  if (mode != W4A16_GATE_UP && mode != W4A16_DOWN && mode != W4A16_GATE_UP_SILU)
+    return W4A16_ERR_INVALID_ARG;
   if (num_experts <= 0 || n <= 0 || k <= 0 || tokens < 0 || topk <= 0 || capacity < 0)
     return W4A16_ERR_INVALID_ARG;
   if (k % kGroup != 0) return W4A16_ERR_UNSUPPORTED;
@@ -239,6 +246,10 @@ w4a16_status w4a16_moe_indexed_gemm(int mode, const void* packed, int num_expert
     return W4A16_ERR_WORKSPACE;
   Pipeline pl;
   if (!plan_pipeline(*plan, k, &pl)) return W4A16_ERR_INVALID_ARG;
+  // the fused activation needs the interleaved gate/up packing, and only it
+  const bool glu = mode == W4A16_GATE_UP_SILU;
+  if (glu != (plan->layout == W4A16_LAYOUT_KTILE64_GLU16)) return W4A16_ERR_INVALID_ARG;
+  if (glu && n % kTileRows != 0) return W4A16_ERR_UNSUPPORTED;
   const int bm = plan->block_m;
   if (capacity % bm != 0) return W4A16_ERR_INVALID_ARG;
   const long long numel = static_cast<long long>(tokens) * topk;
@@ -312,7 +323,7 @@ w4a16_status w4a16_moe_indexed_gemm(int mode, const void* packed, int num_expert
   g.gather_rows = 1;
   g.act_rows = capacity;
   g.family = kIndexed;
-  g.out_mode = mode == W4A16_DOWN ? kOutF32WeightedAdd : kOutBf16;
+  g.out_mode = mode == W4A16_DOWN ? kOutF32WeightedAdd : (glu ? kOutGluBf16 : kOutBf16);
   g.sorted_ids = sorted_ids;
   g.expert_ids = expert_ids;
   g.num_tokens_padded = num_tokens_padded;
@@ -358,7 +369,8 @@ w4a16_status w4a16_moe_grouped_gemm(int kind, const void* packed, int num_expert
   }
   if (workspace == nullptr || ws_bytes < kStatusBytes) return W4A16_ERR_WORKSPACE;
   Pipeline pl;
-  if (!plan_pipeline(*plan, k, &pl)) return W4A16_ERR_INVALID_ARG;
+  if (!plan_pipeline(*plan, k, &pl) || plan->layout != W4A16_LAYOUT_KTILE64)
+    return W4A16_ERR_INVALID_ARG;
   const int bm = plan->block_m;
   const long long rows_total =
       kind == W4A16_GROUPED_MASKED ? static_cast<long long>(num_experts) * m : m;

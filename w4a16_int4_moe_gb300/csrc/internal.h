@@ -41,7 +41,17 @@ inline size_t packed_expert_bytes(int n, int k) {
 }
 
 enum Family { kIndexed = 0, kContiguous = 1, kMasked = 2 };
-enum OutMode { kOutBf16 = 0, kOutF32WeightedAdd = 1 };
+enum OutMode { kOutBf16 = 0, kOutF32WeightedAdd = 1, kOutGluBf16 = 2 };
+
+// Source row (of the [n, k] weight matrix) of row `row` of packed tile `tile`.
+// W4A16_LAYOUT_KTILE64_GLU16 interleaves gate rows [0, n/2) and up rows
+// [n/2, n) by 16 inside each 32-row quarter of a tile.
+__host__ __device__ inline int packed_source_row(int n, int layout, int tile, int row) {
+  if (layout != W4A16_LAYOUT_KTILE64_GLU16) return tile * kTileRows + row;
+  const int q = row >> 5, i = row & 31;
+  const int col = tile * 64 + q * 16 + (i & 15);
+  return i < 16 ? col : n / 2 + col;
+}
 
 struct GemmArgs {
   // Activation tensor map: the permuted rows of the indexed family (3-D,
@@ -102,9 +112,9 @@ cudaError_t launch_align(const int32_t* topk_ids, int numel, int num_experts, in
 size_t align_smem_bytes(int num_experts);
 
 cudaError_t launch_prepack(const uint8_t* q, const uint16_t* scales, int num_experts, int n,
-                           int k, uint8_t* packed, cudaStream_t stream);
-cudaError_t launch_unpack(const uint8_t* packed, int num_experts, int n, int k, uint8_t* q,
-                          uint16_t* scales, cudaStream_t stream);
+                           int k, int layout, uint8_t* packed, cudaStream_t stream);
+cudaError_t launch_unpack(const uint8_t* packed, int num_experts, int n, int k, int layout,
+                          uint8_t* q, uint16_t* scales, cudaStream_t stream);
 
 // Routed rows into routing order; also zeroes zero_bytes (a multiple of 16)
 // at `zero` when given. Triggers the programmatic launch of the next kernel.

@@ -290,6 +290,10 @@ __device__ __forceinline__ void dequant_group(const uint4 q, uint32_t scale_bits
 // item. Global stage u -> A slot u % 4 (dequant warpgroup u % 4), B slot
 // u % BS, weight slot u % WS (WS % 4 == 0, BS even).
 
+// kGlu: the fused-activation epilogue (out_mode kOutGluBf16) is compiled
+// into its own instantiation so that it cannot change the register
+// allocation of the plain kernel.
+template <bool kGlu>
 __global__ void __launch_bounds__(kThreads, 1)
     w4a16_moe_gemm_kernel(const __grid_constant__ GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
@@ -710,48 +714,80 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int jj = 0; jj < 16; ++jj)
             v[jj] = __float_as_uint(__uint_as_float(v[jj]) + __uint_as_float(w[jj]));
         }
-        // transpose through shared memory: tile[jj][lane] = value of token
-        // column j0 + jj for weight row lane
+        if constexpr (kGlu) {
+          // Fused activation: lanes 0..15 hold gate columns, lanes 16..31 the
+          // matching up columns (W4A16_LAYOUT_KTILE64_GLU16). Both are rounded
+          // to BF16 as the unfused gate_up output would be, then combined as
+          // silu(g) * u in FP32; the 16 x 16 results are staged transposed and
+          // written 4 columns of one token row at a time.
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj) tile[jj * 32 + lane] = __uint_as_float(v[jj]);
-        __syncwarp();
-        // lane (jr, c4) writes token row j0 + jr, columns ng..ng+3
-        for (int jr = jr0; jr < 16 && j0 + jr < rows; jr += 4) {
-          const int j = j0 + jr;
-          const int dr = idst[j];
-          if (dr < 0 || ng >= args.n) continue;
-          const float4 x = *reinterpret_cast<const float4*>(tile + jr * 32 + 4 * c4);
-          if (args.out_mode == kOutF32WeightedAdd) {
-            float* o = static_cast<float*>(args.out) + static_cast<long long>(dr) * args.n + ng;
-            const float wt = iwt[j];
-            if (vec4) {
-              atomicAdd(reinterpret_cast<float4*>(o),
-                        make_float4(wt * x.x, wt * x.y, wt * x.z, wt * x.w));
-            } else {
-              atomicAdd(o, wt * x.x);
-              if (ng + 1 < args.n) atomicAdd(o + 1, wt * x.y);
-              if (ng + 2 < args.n) atomicAdd(o + 2, wt * x.z);
-              if (ng + 3 < args.n) atomicAdd(o + 3, wt * x.w);
-            }
-          } else {
-            __nv_bfloat16* o =
-                static_cast<__nv_bfloat16*>(args.out) + static_cast<long long>(dr) * args.n + ng;
+          for (int jj = 0; jj < 16; ++jj) {
+            const float mine = __uint_as_float(v[jj]);
+            const float other = __shfl_xor_sync(0xffffffffu, mine, 16);
+            const float g = __bfloat162float(__float2bfloat16_rn(mine));
+            const float u = __bfloat162float(__float2bfloat16_rn(other));
+            if (lane < 16) tile[jj * 16 + lane] = g / (1.0f + expf(-g)) * u;
+          }
+          __syncwarp();
+          const int inter = args.n >> 1;
+          const int gcol = d.tile * 64 + quarter * 16 + 4 * (lane & 3);
+          for (int jr = lane >> 2; jr < 16 && j0 + jr < rows; jr += 8) {
+            const int dr = idst[j0 + jr];
+            if (dr < 0) continue;
+            const float4 x = *reinterpret_cast<const float4*>(tile + jr * 16 + 4 * (lane & 3));
             const __nv_bfloat162 lo = __floats2bfloat162_rn(x.x, x.y);
             const __nv_bfloat162 hi = __floats2bfloat162_rn(x.z, x.w);
-            if (vec4) {
-              uint2 pk;
-              pk.x = *reinterpret_cast<const uint32_t*>(&lo);
-              pk.y = *reinterpret_cast<const uint32_t*>(&hi);
-              *reinterpret_cast<uint2*>(o) = pk;
+            uint2 pk;
+            pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+            pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+            *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(args.out) +
+                                      static_cast<long long>(dr) * inter + gcol) = pk;
+          }
+          __syncwarp();  // the tile is rewritten by the next 16 token columns
+        } else {
+          // transpose through shared memory: tile[jj][lane] = value of token
+          // column j0 + jj for weight row lane
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) tile[jj * 32 + lane] = __uint_as_float(v[jj]);
+          __syncwarp();
+          // lane (jr, c4) writes token row j0 + jr, columns ng..ng+3
+          for (int jr = jr0; jr < 16 && j0 + jr < rows; jr += 4) {
+            const int j = j0 + jr;
+            const int dr = idst[j];
+            if (dr < 0 || ng >= args.n) continue;
+            const float4 x = *reinterpret_cast<const float4*>(tile + jr * 32 + 4 * c4);
+            if (args.out_mode == kOutF32WeightedAdd) {
+              float* o = static_cast<float*>(args.out) + static_cast<long long>(dr) * args.n + ng;
+              const float wt = iwt[j];
+              if (vec4) {
+                atomicAdd(reinterpret_cast<float4*>(o),
+                          make_float4(wt * x.x, wt * x.y, wt * x.z, wt * x.w));
+              } else {
+                atomicAdd(o, wt * x.x);
+                if (ng + 1 < args.n) atomicAdd(o + 1, wt * x.y);
+                if (ng + 2 < args.n) atomicAdd(o + 2, wt * x.z);
+                if (ng + 3 < args.n) atomicAdd(o + 3, wt * x.w);
+              }
             } else {
-              o[0] = lo.x;
-              if (ng + 1 < args.n) o[1] = lo.y;
-              if (ng + 2 < args.n) o[2] = hi.x;
-              if (ng + 3 < args.n) o[3] = hi.y;
+              __nv_bfloat16* o =
+                  static_cast<__nv_bfloat16*>(args.out) + static_cast<long long>(dr) * args.n + ng;
+              const __nv_bfloat162 lo = __floats2bfloat162_rn(x.x, x.y);
+              const __nv_bfloat162 hi = __floats2bfloat162_rn(x.z, x.w);
+              if (vec4) {
+                uint2 pk;
+                pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+                pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+                *reinterpret_cast<uint2*>(o) = pk;
+              } else {
+                o[0] = lo.x;
+                if (ng + 1 < args.n) o[1] = lo.y;
+                if (ng + 2 < args.n) o[2] = hi.x;
+                if (ng + 3 < args.n) o[3] = hi.y;
+              }
             }
           }
+          __syncwarp();  // the tile is rewritten by the next 16 token columns
         }
-        __syncwarp();  // the tile is rewritten by the next 16 token columns
       }
       tc_fence_before();
       __syncwarp();
@@ -869,8 +905,9 @@ cudaError_t launch_moe_gemm(const GemmArgs& args, int grid, bool dependent, cuda
   // all 512 TMEM columns.
   size_t smem = gemm_smem_bytes(args.block_m, args.w_stages, args.b_stages);
   if (smem < 118 * 1024) smem = 118 * 1024;
-  cudaError_t err = cudaFuncSetAttribute(w4a16_moe_gemm_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const bool glu = args.out_mode == kOutGluBf16;
+  auto kernel = glu ? w4a16_moe_gemm_kernel<true> : w4a16_moe_gemm_kernel<false>;
+  cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
@@ -883,7 +920,7 @@ cudaError_t launch_moe_gemm(const GemmArgs& args, int grid, bool dependent, cuda
   attr[0].val.programmaticStreamSerializationAllowed = dependent ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, w4a16_moe_gemm_kernel, args);
+  return cudaLaunchKernelEx(&cfg, kernel, args);
 }
 
 }  // namespace w4a16

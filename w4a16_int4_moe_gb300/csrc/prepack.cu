@@ -6,7 +6,9 @@
 // The layout is fixed at load (same page, section
 // "调度由每个专家收到的 token 数决定").
 //
-// Output: for each expert, 128-row tiles; inside a tile, 64-k steps back to
+// Output: for each expert, 128-row tiles (rows in order, or, with
+// W4A16_LAYOUT_KTILE64_GLU16, gate and up rows interleaved by 16: see
+// packed_source_row); inside a tile, 64-k steps back to
 // back; one step = q [2 groups][128 rows][16 B] then scales [2][128] BF16.
 // Inside every 32-bit word (8 consecutive k) the nibbles are reordered so
 // that (word >> 4i) & 0x000F000F holds k = 2i in the low half and k = 2i + 1
@@ -49,7 +51,8 @@ __device__ __forceinline__ uint32_t unshuffle_word(uint32_t r) {
 // one scale.
 __global__ void w4a16_prepack_kernel(const uint8_t* __restrict__ q,
                                      const uint16_t* __restrict__ scales, int num_experts, int n,
-                                     int k, int n_tiles, int k_steps, uint8_t* __restrict__ packed) {
+                                     int k, int n_tiles, int k_steps, int layout,
+                                     uint8_t* __restrict__ packed) {
   const long long total = static_cast<long long>(num_experts) * n_tiles * k_steps * 2 * kTileRows;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
@@ -62,7 +65,7 @@ __global__ void w4a16_prepack_kernel(const uint8_t* __restrict__ q,
     rest /= k_steps;
     const int tile = static_cast<int>(rest % n_tiles);
     const int e = static_cast<int>(rest / n_tiles);
-    const int nn = tile * kTileRows + row;
+    const int nn = packed_source_row(n, layout, tile, row);
     const int k0 = ks * kKStep + g * kGroup;
     uint4 out = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
     uint16_t sc = 0;
@@ -81,8 +84,8 @@ __global__ void w4a16_prepack_kernel(const uint8_t* __restrict__ q,
 }
 
 __global__ void w4a16_unpack_kernel(const uint8_t* __restrict__ packed, int num_experts, int n,
-                                    int k, int n_tiles, int k_steps, uint8_t* __restrict__ q,
-                                    uint16_t* __restrict__ scales) {
+                                    int k, int n_tiles, int k_steps, int layout,
+                                    uint8_t* __restrict__ q, uint16_t* __restrict__ scales) {
   const long long total = static_cast<long long>(num_experts) * n * (k / kGroup);
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
@@ -91,7 +94,14 @@ __global__ void w4a16_unpack_kernel(const uint8_t* __restrict__ packed, int num_
     const long long src_row = idx / (k / kGroup);
     const int nn = static_cast<int>(src_row % n);
     const int e = static_cast<int>(src_row / n);
-    const int tile = nn / kTileRows, row = nn % kTileRows;
+    int tile = nn / kTileRows, row = nn % kTileRows;
+    if (layout == W4A16_LAYOUT_KTILE64_GLU16) {
+      // inverse of packed_source_row: gate column c or up column c (n/2 + c)
+      const bool up = nn >= n / 2;
+      const int c = up ? nn - n / 2 : nn;
+      tile = c / 64;
+      row = ((c % 64) / 16) * 32 + (up ? 16 : 0) + c % 16;
+    }
     const int ks = grp / 2, g = grp % 2;
     const uint8_t* step = packed + ((static_cast<long long>(e) * n_tiles + tile) * k_steps + ks) *
                                        static_cast<long long>(kStepBytes);
@@ -105,7 +115,7 @@ __global__ void w4a16_unpack_kernel(const uint8_t* __restrict__ packed, int num_
 }
 
 cudaError_t launch_prepack(const uint8_t* q, const uint16_t* scales, int num_experts, int n,
-                           int k, uint8_t* packed, cudaStream_t stream) {
+                           int k, int layout, uint8_t* packed, cudaStream_t stream) {
   const long long total =
       static_cast<long long>(num_experts) * packed_tiles(n) * packed_ksteps(k) * 2 * kTileRows;
   if (total == 0) return cudaSuccess;
@@ -113,19 +123,20 @@ cudaError_t launch_prepack(const uint8_t* q, const uint16_t* scales, int num_exp
   const long long want = (total + threads - 1) / threads;
   const int blocks = static_cast<int>(want < 65536 ? want : 65536);
   w4a16_prepack_kernel<<<blocks, threads, 0, stream>>>(q, scales, num_experts, n, k,
-                                                       packed_tiles(n), packed_ksteps(k), packed);
+                                                       packed_tiles(n), packed_ksteps(k), layout,
+                                                       packed);
   return cudaGetLastError();
 }
 
-cudaError_t launch_unpack(const uint8_t* packed, int num_experts, int n, int k, uint8_t* q,
-                          uint16_t* scales, cudaStream_t stream) {
+cudaError_t launch_unpack(const uint8_t* packed, int num_experts, int n, int k, int layout,
+                          uint8_t* q, uint16_t* scales, cudaStream_t stream) {
   const long long total = static_cast<long long>(num_experts) * n * (k / kGroup);
   if (total == 0) return cudaSuccess;
   const int threads = 256;
   const long long want = (total + threads - 1) / threads;
   const int blocks = static_cast<int>(want < 65536 ? want : 65536);
   w4a16_unpack_kernel<<<blocks, threads, 0, stream>>>(packed, num_experts, n, k, packed_tiles(n),
-                                                      packed_ksteps(k), q, scales);
+                                                      packed_ksteps(k), layout, q, scales);
   return cudaGetLastError();
 }
 

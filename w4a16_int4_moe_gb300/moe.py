@@ -24,10 +24,15 @@ class PackedExperts:
     n: int
     k: int
 
+    layout: int = ops.W4A16_LAYOUT_KTILE64
+
     @classmethod
-    def from_checkpoint(cls, q: torch.Tensor, scales: torch.Tensor, group: int = 32):
+    def from_checkpoint(cls, q: torch.Tensor, scales: torch.Tensor, group: int = 32,
+                        layout: int = ops.W4A16_LAYOUT_KTILE64):
+        """layout W4A16_LAYOUT_KTILE64_GLU16 (gate_up weights only) enables the
+        fused gate_up + activation call."""
         e, n, kh = q.shape
-        return cls(ops.w4a16_prepack(q, scales, group), e, n, kh * 2)
+        return cls(ops.w4a16_prepack(q, scales, group, layout), e, n, kh * 2, layout)
 
 
 class W4A16MoE:
@@ -35,6 +40,8 @@ class W4A16MoE:
 
     def __init__(self, gate_up: PackedExperts, down: PackedExperts, topk: int,
                  max_tokens: int, tok_e_hint: float = 0.0, device=None):
+        """With gate_up packed as W4A16_LAYOUT_KTILE64_GLU16 the activation is
+        fused into the gate_up call (forward skips the separate pass)."""
         assert gate_up.num_experts == down.num_experts
         assert gate_up.n == 2 * down.k and gate_up.k == down.n
         self.gate_up, self.down = gate_up, down
@@ -52,6 +59,8 @@ class W4A16MoE:
                                       self.gate_up.k, hint)
         self.plan_dn = ops.w4a16_plan(tokens, self.topk, self.num_experts, self.down.n,
                                       self.down.k, hint)
+        self.fused_act = self.gate_up.layout == ops.W4A16_LAYOUT_KTILE64_GLU16
+        self.plan_gu.layout = self.gate_up.layout
         # both GEMMs read the same routing blocks
         self.plan_dn.block_m = self.plan_gu.block_m
         self.block_m = self.plan_gu.block_m
@@ -80,6 +89,14 @@ class W4A16MoE:
             self.gate_up.k, x, tokens, self.topk, self.sorted_ids, self.expert_ids, self.ntp,
             self.plan_gu, self.workspace, out=self.inter_buf[:numel], stream=stream)
 
+    def gate_up_act(self, x: torch.Tensor, tokens: int, stream=None):
+        """gate_up with the activation fused: writes act_buf directly."""
+        numel = tokens * self.topk
+        return ops.w4a16_moe_indexed_gemm(
+            ops.W4A16_GATE_UP_SILU, self.gate_up.packed, self.num_experts, self.gate_up.n,
+            self.gate_up.k, x, tokens, self.topk, self.sorted_ids, self.expert_ids, self.ntp,
+            self.plan_gu, self.workspace, out=self.act_buf[:numel], stream=stream)
+
     def activation(self, tokens: int, stream=None):
         numel = tokens * self.topk
         return ops.w4a16_silu_and_mul(self.inter_buf[:numel], out=self.act_buf[:numel],
@@ -102,7 +119,10 @@ class W4A16MoE:
         if out is None:
             out = torch.empty((tokens, self.hidden), dtype=torch.float32, device=x.device)
         self.align(topk_ids, stream)
-        self.gate_up_gemm(x, tokens, stream)
-        self.activation(tokens, stream)
+        if self.fused_act:
+            self.gate_up_act(x, tokens, stream)
+        else:
+            self.gate_up_gemm(x, tokens, stream)
+            self.activation(tokens, stream)
         self.down_gemm(tokens, topk_weights, out, stream)
         return out

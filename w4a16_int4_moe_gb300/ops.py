@@ -26,11 +26,13 @@ W4A16_ERR_TIMEOUT = 6
 
 W4A16_GATE_UP = 0
 W4A16_DOWN = 1
+W4A16_GATE_UP_SILU = 2
 W4A16_GROUPED_CONTIGUOUS = 0
 W4A16_GROUPED_MASKED = 1
 W4A16_FLAG_VALIDATE_ROUTING = 1
 W4A16_FLAG_ACCUMULATE = 2
 W4A16_LAYOUT_KTILE64 = 0
+W4A16_LAYOUT_KTILE64_GLU16 = 1
 W4A16_FLAG_SYNC_STATUS = 4
 
 # Every symbol include/w4a16moe.h declares.
@@ -85,7 +87,7 @@ def load_library(path: Optional[str] = None):
         "w4a16_moe_align_block_size": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
         "w4a16_prepack_size": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(_Z)]),
         "w4a16_prepack": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _Z, _P]),
-        "w4a16_unpack": (_I, [_P, _I, _I, _I, _P, _P, _P]),
+        "w4a16_unpack": (_I, [_P, _I, _I, _I, _I, _P, _P, _P]),
         "w4a16_workspace_size": (_Z, [ctypes.POINTER(Plan), _I, _I]),
         "w4a16_moe_indexed_gemm": (_I, [_I, _P, _I, _I, _I, _P, _I, _I, _P, _P, _P, _I, _P, _P,
                                         _I, ctypes.POINTER(Plan), _P, _Z, _P]),
@@ -190,11 +192,12 @@ def w4a16_prepack(q: torch.Tensor, scales: torch.Tensor, group: int = 32,
     return out
 
 
-def w4a16_unpack(packed: torch.Tensor, num_experts: int, n: int, k: int, stream=None):
+def w4a16_unpack(packed: torch.Tensor, num_experts: int, n: int, k: int,
+                 layout: int = W4A16_LAYOUT_KTILE64, stream=None):
     q = torch.empty((num_experts, n, k // 2), dtype=torch.uint8, device=packed.device)
     s = torch.empty((num_experts, n, k // 32), dtype=torch.int16, device=packed.device)
     _check("w4a16_unpack", load_library().w4a16_unpack(
-        _ptr(packed), num_experts, n, k, _ptr(q), _ptr(s), _stream(stream)))
+        _ptr(packed), num_experts, n, k, layout, _ptr(q), _ptr(s), _stream(stream)))
     return q, s
 
 
@@ -208,10 +211,13 @@ def w4a16_moe_indexed_gemm(mode: int, packed: torch.Tensor, num_experts: int, n:
                            plan: Plan, workspace: torch.Tensor,
                            topk_weights: Optional[torch.Tensor] = None,
                            out: Optional[torch.Tensor] = None, flags: int = 0, stream=None):
-    """GATE_UP: out BF16 [tokens*topk, n]; DOWN: out FP32 [tokens, n]."""
+    """GATE_UP: out BF16 [tokens*topk, n]; GATE_UP_SILU: out BF16
+    [tokens*topk, n/2]; DOWN: out FP32 [tokens, n]."""
     if out is None:
         if mode == W4A16_GATE_UP:
             out = torch.empty((tokens * topk, n), dtype=torch.bfloat16, device=a.device)
+        elif mode == W4A16_GATE_UP_SILU:
+            out = torch.empty((tokens * topk, n // 2), dtype=torch.bfloat16, device=a.device)
         else:
             out = torch.empty((tokens, n), dtype=torch.float32, device=a.device)
     _check("w4a16_moe_indexed_gemm", load_library().w4a16_moe_indexed_gemm(
