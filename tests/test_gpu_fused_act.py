@@ -104,3 +104,14 @@ def test_layer_forward_with_fused_activation(cuda_dev):
     # order of its atomic adds may differ
     assert_close(y_fused.cpu().numpy(), y_plain.cpu().numpy(), "layer fused vs plain",
                  rel_l2=1e-6, max_abs_frac=1e-6)
+
+
+def test_gemm_from_pack_quantized_checkpoint(cuda_dev):
+    # weights handed over as compressed-tensors int32 words give the same GEMM
+    from w4a16_int4_moe_gb300 import checkpoint
+    p = wl.tiny(seed=54)
+    words = torch.from_numpy(np.ascontiguousarray(p.q_gu)).view(torch.int32).to(cuda_dev)
+    scales = torch.from_numpy(p.s_gu.view(np.int16)).view(torch.bfloat16).to(cuda_dev)
+    pe = checkpoint.packed_experts_from_pack_quantized(words, scales)
+    ref = ops.w4a16_prepack(dev(p.q_gu, cuda_dev), dev(p.s_gu.view(np.int16), cuda_dev))
+    assert torch.equal(pe.packed, ref)
