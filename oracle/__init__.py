@@ -38,4 +38,5 @@ from .moe_oracle import (  # noqa: F401
     grouped_contiguous,
     grouped_masked,
     moe_layer,
+    topk_softmax,
 )

@@ -270,3 +270,39 @@ def moe_layer(x_bits, topk_ids, topk_weights, q_gu, s_gu, q_dn, s_dn):
     a_bits = silu_and_mul(g_bits)
     y = indexed_down(a_bits, topk_ids, topk_weights, q_dn, s_dn)
     return g, g_bits, a_bits, y
+
+
+def topk_softmax(logits, topk: int, renormalize: bool = True, expert_offset: int = 0,
+                 num_local_experts=None):
+    """Routing front end: softmax over the global experts, top-k, local ids.
+
+    Reading (the pages route top-8 of 384 experts but leave the router to
+    the serving stack; the workloads draw softmax weights renormalised over
+    the chosen k):
+    * p = softmax(logits) over all experts, in float64;
+    * the k experts with the largest logits are chosen, larger first, ties
+      to the lower expert id. The logit decides, not p, so the choice is made
+      on the input values themselves;
+    * weights = p of the chosen experts, divided by their sum if `renormalize`;
+    * ids become local: g - expert_offset when that lies in
+      [0, num_local_experts), else -1 (an expert of another GPU).
+
+    logits float [T, E]. Returns (ids int32 [T, k], weights float64 [T, k])."""
+    lg = np.asarray(logits, dtype=np.float64)
+    t, e = lg.shape
+    if num_local_experts is None:
+        num_local_experts = e
+    ids = np.empty((t, topk), dtype=np.int32)
+    w = np.empty((t, topk), dtype=np.float64)
+    for i in range(t):
+        row = lg[i]
+        p = np.exp(row - row.max())
+        p /= p.sum()
+        order = np.lexsort((np.arange(e), -row))[:topk]   # by logit desc, then id asc
+        sel = p[order]
+        if renormalize:
+            sel = sel / sel.sum()
+        loc = order - expert_offset
+        ids[i] = np.where((loc >= 0) & (loc < num_local_experts), loc, -1)
+        w[i] = sel
+    return ids, w

@@ -371,3 +371,54 @@ def test_planted_dropped_topk_weight_is_caught(monkeypatch):
     monkeypatch.setattr(mo, "indexed_down", unweighted)
     with pytest.raises(AssertionError):
         test_brute_force_per_token_layer(0, 2, 4)
+
+
+# ------------------------------------------------------------ top-k routing --
+
+def test_topk_softmax_golden_tie_and_local_ids():
+    # hand-derived: logits 1, 3, 3, 0.5; the two 3s tie -> lower id first;
+    # renormalised over the pair their softmax weights are 1/2 each
+    lg = np.array([[1.0, 3.0, 3.0, 0.5]])
+    ids, w = oracle.topk_softmax(lg, 2)
+    assert ids.tolist() == [[1, 2]]
+    np.testing.assert_allclose(w, [[0.5, 0.5]], rtol=0, atol=1e-15)
+    # this GPU holds global experts 2..3: expert 1 is another GPU's
+    ids, _ = oracle.topk_softmax(lg, 2, expert_offset=2, num_local_experts=2)
+    assert ids.tolist() == [[-1, 0]]
+    # without renormalisation the weights are the plain softmax values
+    _, w = oracle.topk_softmax(lg, 2, renormalize=False)
+    e = np.exp([1.0, 3.0, 3.0, 0.5])
+    np.testing.assert_allclose(w, [[e[1] / e.sum(), e[2] / e.sum()]], rtol=1e-15)
+
+
+def test_topk_softmax_all_experts_is_the_library_softmax():
+    from scipy.special import softmax
+    rng = np.random.default_rng(7)
+    lg = rng.standard_normal((5, 9))
+    ids, w = oracle.topk_softmax(lg, 9, renormalize=False)
+    for t in range(5):
+        np.testing.assert_allclose(w[t], softmax(lg[t])[ids[t]], rtol=1e-12)
+        assert sorted(ids[t].tolist()) == list(range(9))
+        assert np.all(np.diff(lg[t][ids[t]]) <= 0)
+
+
+def test_topk_softmax_brute_force_over_subsets():
+    import itertools
+    rng = np.random.default_rng(8)
+    for t in range(20):
+        lg = rng.standard_normal((1, 7))
+        k = int(rng.integers(1, 5))
+        ids, w = oracle.topk_softmax(lg, k)
+        best = max(itertools.combinations(range(7), k), key=lambda c: lg[0, list(c)].sum())
+        assert set(ids[0].tolist()) == set(best)
+        assert abs(w.sum() - 1.0) < 1e-12 and np.all(w > 0)
+        assert np.all(np.diff(w[0]) <= 1e-15)            # larger logit, larger weight first
+
+
+def test_planted_ascending_topk_is_caught(monkeypatch):
+    import oracle.moe_oracle as om
+    real = om.np.lexsort
+    monkeypatch.setattr(om.np, "lexsort", lambda keys: real((keys[0], -keys[1])))
+    lg = np.array([[1.0, 3.0, 3.0, 0.5]])
+    ids, _ = om.topk_softmax(lg, 2)
+    assert ids.tolist() != [[1, 2]]
