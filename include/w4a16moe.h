@@ -249,6 +249,31 @@ w4a16_status w4a16_moe_grouped_gemm(int kind, const void* packed, int num_expert
                                     const w4a16_plan_t* plan, void* workspace, size_t ws_bytes,
                                     void* stream);
 
+/* Element types of w4a16_topk_softmax's logits. */
+enum { W4A16_DTYPE_F32 = 0, W4A16_DTYPE_BF16 = 1 };
+
+/*
+ * Routing front end: router logits -> the top-k routing tensors the align
+ * and the GEMMs consume. The pages route each token to the top 8 of 384
+ * experts and hand the operator the serving stack's routing tensors
+ * ([P-arex] "调度由每个专家收到的 token 数决定"); the router is this library's
+ * reading:
+ *   p = softmax(logits[t, :]) over all num_experts experts (FP32);
+ *   the topk experts with the largest logits are chosen, larger first, ties
+ *   to the lower expert id (the logit decides, exactly);
+ *   topk_weights[t, s] = p of choice s, divided by the sum of the chosen p
+ *   when `renormalize` != 0;
+ *   topk_ids[t, s] = choice s - expert_offset when that lies in
+ *   [0, num_local_experts) (an expert of this GPU), else -1.
+ * logits: device [tokens, num_experts] of logits_dtype; topk_ids int32 and
+ * topk_weights fp32 [tokens, topk], device. num_experts <= 1024, topk <= 32
+ * (W4A16_ERR_UNSUPPORTED beyond). No host synchronisation: graph-capturable.
+ */
+w4a16_status w4a16_topk_softmax(const void* logits, int logits_dtype, int tokens,
+                                int num_experts, int topk, int renormalize, int expert_offset,
+                                int num_local_experts, int32_t* topk_ids, float* topk_weights,
+                                void* stream);
+
 /*
  * Activation between gate_up and down (the pages leave it out of the timed
  * pair, [P-arex] "六个场景的逐层测量与限定条件"; its form is this library's

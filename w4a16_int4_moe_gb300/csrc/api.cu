@@ -110,7 +110,7 @@ const char* w4a16_status_string(int status) {
   }
 }
 
-int w4a16_version(void) { return 100; }
+int w4a16_version(void) { return 110; }
 
 w4a16_status w4a16_plan(int tokens, int topk, int num_experts, int n, int k, float tok_e_hint,
                         w4a16_plan_t* out) {
@@ -431,6 +431,25 @@ w4a16_status w4a16_moe_grouped_gemm(int kind, const void* packed, int num_expert
   long long grid = plan->grid > 0 ? plan->grid : static_cast<long long>(sms) * plan->ctas_per_sm;
   grid = std::max<long long>(1, std::min(grid, blocks * g.n_tiles));
   return cuda_status(launch_moe_gemm(g, static_cast<int>(grid), false, s));
+}
+
+w4a16_status w4a16_topk_softmax(const void* logits, int logits_dtype, int tokens,
+                                int num_experts, int topk, int renormalize, int expert_offset,
+                                int num_local_experts, int32_t* topk_ids, float* topk_weights,
+                                void* stream) {
+  if (tokens < 0 || num_experts <= 0 || topk <= 0 || num_local_experts < 0)
+    return W4A16_ERR_INVALID_ARG;
+  if (logits_dtype != W4A16_DTYPE_F32 && logits_dtype != W4A16_DTYPE_BF16)
+    return W4A16_ERR_INVALID_ARG;
+  if (num_experts > 1024 || topk > 32 || topk > num_experts) return W4A16_ERR_UNSUPPORTED;
+  if (tokens > 0 && (logits == nullptr || topk_ids == nullptr || topk_weights == nullptr))
+    return W4A16_ERR_INVALID_ARG;
+  const int sms = current_sm_count();
+  if (sms <= 0) return W4A16_ERR_CUDA;
+  return cuda_status(launch_topk_softmax(logits, logits_dtype == W4A16_DTYPE_BF16, tokens,
+                                         num_experts, topk, renormalize != 0, expert_offset,
+                                         num_local_experts, topk_ids, topk_weights, sms,
+                                         static_cast<cudaStream_t>(stream)));
 }
 
 w4a16_status w4a16_silu_and_mul(const uint16_t* in, int rows, int inter, uint16_t* out,

@@ -123,6 +123,11 @@ cudaError_t launch_permute_rows(const uint16_t* a, int k, int a_div, int numel,
                                 int capacity, uint16_t* dst, void* zero, size_t zero_bytes,
                                 int sms, cudaStream_t stream);
 
+cudaError_t launch_topk_softmax(const void* logits, int bf16_logits, int tokens, int num_experts,
+                                int topk, int renormalize, int expert_offset, int num_local,
+                                int32_t* topk_ids, float* topk_weights, int sms,
+                                cudaStream_t stream);
+
 cudaError_t launch_silu_and_mul(const uint16_t* in, int rows, int inter, uint16_t* out,
                                 cudaStream_t stream);
 

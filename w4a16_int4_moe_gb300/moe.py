@@ -109,6 +109,28 @@ class W4A16MoE:
             self.act_buf[:numel], tokens, self.topk, self.sorted_ids, self.expert_ids, self.ntp,
             self.plan_dn, self.workspace, topk_weights=topk_weights, out=out, stream=stream)
 
+    def route(self, router_logits: torch.Tensor, expert_offset: int = 0,
+              renormalize: bool = True, stream=None):
+        """Router logits [T, E_global] (fp32 or BF16) -> (topk_ids, topk_weights)
+        for this GPU's experts [expert_offset, expert_offset + num_experts),
+        on the device (w4a16_topk_softmax)."""
+        tokens = router_logits.shape[0]
+        if not hasattr(self, "_route_ids") or self._route_ids.shape[0] < tokens:
+            self._route_ids = torch.empty((self.max_tokens, self.topk), dtype=torch.int32,
+                                          device=self.device)
+            self._route_w = torch.empty((self.max_tokens, self.topk), dtype=torch.float32,
+                                        device=self.device)
+        out = (self._route_ids[:tokens], self._route_w[:tokens])
+        return ops.w4a16_topk_softmax(router_logits, self.topk, renormalize, expert_offset,
+                                      self.num_experts, out=out, stream=stream)
+
+    def forward_from_logits(self, x: torch.Tensor, router_logits: torch.Tensor,
+                            expert_offset: int = 0, renormalize: bool = True,
+                            out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+        """The whole layer from router logits: route, align, gate_up(+act), down."""
+        ids, w = self.route(router_logits, expert_offset, renormalize, stream)
+        return self.forward(x, ids, w, out=out, stream=stream)
+
     def forward(self, x: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor,
                 out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
         """x BF16 [T, H], topk_ids int32 [T, topk], topk_weights fp32 [T, topk]

@@ -33,6 +33,8 @@ W4A16_FLAG_VALIDATE_ROUTING = 1
 W4A16_FLAG_ACCUMULATE = 2
 W4A16_LAYOUT_KTILE64 = 0
 W4A16_LAYOUT_KTILE64_GLU16 = 1
+W4A16_DTYPE_F32 = 0
+W4A16_DTYPE_BF16 = 1
 W4A16_FLAG_SYNC_STATUS = 4
 
 # Every symbol include/w4a16moe.h declares.
@@ -41,6 +43,7 @@ EXPORTED = (
     "w4a16_moe_align_block_size", "w4a16_prepack_size", "w4a16_prepack", "w4a16_unpack",
     "w4a16_workspace_size", "w4a16_moe_indexed_gemm", "w4a16_moe_grouped_gemm",
     "w4a16_silu_and_mul", "w4a16_read_device_status", "w4a16_moe_indexed_gemm_noalloc",
+    "w4a16_topk_softmax",
 )
 
 
@@ -94,6 +97,7 @@ def load_library(path: Optional[str] = None):
         "w4a16_moe_grouped_gemm": (_I, [_I, _P, _I, _I, _I, _P, _I, _P, _I, _P, _I,
                                         ctypes.POINTER(Plan), _P, _Z, _P]),
         "w4a16_silu_and_mul": (_I, [_P, _I, _I, _P, _P]),
+        "w4a16_topk_softmax": (_I, [_P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
         "w4a16_read_device_status": (_I, [_P, ctypes.POINTER(_I), _P]),
         "w4a16_moe_indexed_gemm_noalloc": (_I, [_I, _P, _I, _I, _I, _P, _I, _I, _P, _P, _P, _I,
                                                 _P, _P, _I, ctypes.POINTER(Plan), _P]),
@@ -241,6 +245,28 @@ def w4a16_moe_grouped_gemm(kind: int, packed: torch.Tensor, num_experts: int, n:
         flags, None if plan is None else ctypes.byref(plan), _ptr(workspace), workspace.numel(),
         _stream(stream)))
     return out
+
+
+def w4a16_topk_softmax(logits: torch.Tensor, topk: int, renormalize: bool = True,
+                       expert_offset: int = 0, num_local_experts: Optional[int] = None,
+                       out=None, stream=None):
+    """logits fp32/BF16 [T, E] -> (topk_ids int32 [T, topk] local or -1,
+    topk_weights fp32 [T, topk])."""
+    tokens, e = logits.shape
+    if num_local_experts is None:
+        num_local_experts = e
+    dtype = {torch.float32: W4A16_DTYPE_F32, torch.bfloat16: W4A16_DTYPE_BF16}.get(logits.dtype)
+    if dtype is None:
+        raise W4A16Error("w4a16_topk_softmax", W4A16_ERR_INVALID_ARG,
+                         f"logits of dtype {logits.dtype}")
+    if out is None:
+        out = (torch.empty((tokens, topk), dtype=torch.int32, device=logits.device),
+               torch.empty((tokens, topk), dtype=torch.float32, device=logits.device))
+    ids, w = out
+    _check("w4a16_topk_softmax", load_library().w4a16_topk_softmax(
+        _ptr(logits.contiguous()), dtype, tokens, e, topk, int(bool(renormalize)), expert_offset,
+        num_local_experts, _ptr(ids), _ptr(w), _stream(stream)))
+    return ids, w
 
 
 def w4a16_silu_and_mul(x: torch.Tensor, out: Optional[torch.Tensor] = None, stream=None):
