@@ -16,7 +16,8 @@ weight stream (1.19 GB at the EP8 decode shard) is larger than L2 anyway.
 on a bounded sample of the same workload scaled to a whole layer.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                       [--workload ep8_decode|ep8_decode_e12|tp8_16|tp8_64|tp8_256|ep8_prefill|tiny]
+                       [--workload ep8_decode|ep8_decode_e12|tp8_16|tp8_64|tp8_256|ep8_prefill|tiny
+                                   |grouped_contig_{128,256,512,1024}|grouped_masked_32]
 """
 
 from __future__ import annotations
@@ -446,6 +447,116 @@ def run_ours(args):
     print(json.dumps(line))
 
 
+def make_grouped(name):
+    """Grouped-layout workloads on the EP8 shard: the gate_up-shaped and the
+    down-shaped GEMM over the same per-expert rows (random activations)."""
+    from w4a16_int4_moe_gb300 import workloads as wl
+    if name.startswith("grouped_contig_"):
+        m = int(name.split("_")[-1])
+        gu = wl.grouped_contiguous_problem(m, 48, 4096, 7168, seed=1)
+        dn = wl.grouped_contiguous_problem(m, 48, 7168, 2048, seed=2)
+        return gu, dn, f"grouped_contiguous_E48_m{m}_H7168_I2048"
+    if name == "grouped_masked_32":
+        gu = wl.grouped_masked_problem(48, 32, 4096, 7168, seed=1)
+        dn = wl.grouped_masked_problem(48, 32, 7168, 2048, seed=2)
+        dn.layout[:] = gu.layout          # the same rows in both GEMMs
+        return gu, dn, "grouped_masked_E48_budget32_H7168_I2048"
+    raise SystemExit(f"unknown workload {name}")
+
+
+def run_grouped(args):
+    """One step = the grouped gate_up GEMM then the grouped down GEMM (the
+    activation between them untimed), L2 flushed before each step."""
+    import torch
+    from w4a16_int4_moe_gb300 import ops
+    torch.cuda.set_device(0)
+    device = torch.device("cuda", 0)
+    ops.load_library()
+    gu, dn, wname = make_grouped(args.workload)
+
+    def to_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+    calls = []
+    for gp in (gu, dn):
+        pk = ops.w4a16_prepack(to_dev(gp.q), to_dev(gp.s.view(np.int16)))
+        a = to_dev(gp.a.view(np.int16)).view(torch.bfloat16)
+        lay = to_dev(gp.layout)
+        kind = ops.W4A16_GROUPED_CONTIGUOUS if gp.kind == "contiguous" else ops.W4A16_GROUPED_MASKED
+        m = gp.a.shape[0] if gp.kind == "contiguous" else gp.a.shape[1]
+        shape = (m, gp.n) if gp.kind == "contiguous" else (gp.num_experts, m, gp.n)
+        out = torch.empty(shape, dtype=torch.bfloat16, device=device)
+        ws = torch.zeros(256, dtype=torch.uint8, device=device)
+        calls.append((gp, kind, pk, a, m, lay, ws, out))
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream()
+
+    def run(c):
+        gp, kind, pk, a, m, lay, ws, out = c
+        ops.w4a16_moe_grouped_gemm(kind, pk, gp.num_experts, gp.n, gp.k, a, m, lay, ws,
+                                   expected_m=gp.expected_m, out=out)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        run(calls[0])
+        run(calls[1])
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = ClockSampler()
+    clocks.start()
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        run(calls[0])
+        ev[i][1].record(stream)
+        run(calls[1])
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    clocks.mark(time.time() - wall, time.time())
+    clk = clocks.stop()
+    for c in calls:
+        st, word = ops.w4a16_read_device_status(c[6])
+        if st != ops.W4A16_OK:
+            raise SystemExit(f"device status {word:#x}")
+    gu_us = statistics.mean(e[0].elapsed_time(e[1]) * 1e3 for e in ev)
+    dn_us = statistics.mean(e[1].elapsed_time(e[2]) * 1e3 for e in ev)
+    rows = gu.valid_rows()
+    wb = 0.5 + 2.0 / 32
+    act_e = 48 if gu.kind == "contiguous" else int((gu.layout > 0).sum())
+    gu_bytes = act_e * 4096 * 7168 * wb + rows * 7168 * 2 + rows * 4096 * 2
+    dn_bytes = act_e * 7168 * 2048 * wb + rows * 2048 * 2 + rows * 7168 * 2
+    gu_flops, dn_flops = 2.0 * rows * 4096 * 7168, 2.0 * rows * 7168 * 2048
+    hbm, tflops_peak, peak_src = measured_peaks()
+    layer_us = gu_us + dn_us
+    tensor = gu.kind == "contiguous"
+    if tensor:
+        ach = gu_flops / (gu_us * 1e-6) / 1e12
+        roof = {"bound": "tensor", "kernel": "w4a16_moe_gemm_kernel (grouped gate_up)",
+                "achieved": ach, "peak": tflops_peak, "unit": "TFLOP/s", "frac": ach / tflops_peak,
+                "peak_source": f"{peak_src} bf16_tflops", "traffic": None}
+    else:
+        ach = gu_bytes / (gu_us * 1e-6) / 1e9
+        roof = {"bound": "hbm", "kernel": "w4a16_moe_gemm_kernel (grouped gate_up)",
+                "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                "peak_source": f"{peak_src} hbm_gbs", "traffic": None,
+                "algorithmic_bytes": gu_bytes}
+    line = {
+        "metric": METRIC, "value": layer_us, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": wall / args.steps * 1e3,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; random uint4 weights, N(0,1) activations)",
+        "config": {"workload": wname, "valid_rows": rows, "experts": 48,
+                   "l2": "flushed before every step (256 MiB write)"},
+        "gate_up_us": gu_us, "down_us": dn_us,
+        "achieved": {"tflops": (gu_flops + dn_flops) / (layer_us * 1e-6) / 1e12,
+                     "hbm_gbs": (gu_bytes + dn_bytes) / (layer_us * 1e-6) / 1e9},
+        "roofline": roof, "gpu_launches": 2 * args.steps, "clocks": clk,
+    }
+    print(json.dumps(line))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -461,6 +572,8 @@ def main():
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload.startswith("grouped_"):
+        run_grouped(args)
     else:
         run_ours(args)
 

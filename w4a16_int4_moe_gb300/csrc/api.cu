@@ -336,6 +336,7 @@ w4a16_status w4a16_moe_indexed_gemm(int mode, const void* packed, int num_expert
   g.out = out;
   g.status = static_cast<int*>(workspace);
   fill_pipeline(pl, &g);
+  g.raster_rows = 0;
   g.timeout_cycles = wait_timeout_cycles();
   long long grid = plan->grid > 0 ? plan->grid : static_cast<long long>(sms) * plan->ctas_per_sm;
   const long long max_items = static_cast<long long>(capacity / bm) * g.n_tiles;
@@ -422,6 +423,8 @@ w4a16_status w4a16_moe_grouped_gemm(int kind, const void* packed, int num_expert
   g.out = out;
   g.status = static_cast<int*>(workspace);
   fill_pipeline(pl, &g);
+  // group the item order once all token rows are a good part of L2 (129 MB)
+  g.raster_rows = static_cast<double>(rows_total) * k * 2.0 > 64.0 * (1 << 20) ? 1 : 0;
   g.timeout_cycles = wait_timeout_cycles();
   const int sms = current_sm_count();
   if (sms <= 0) return W4A16_ERR_CUDA;

@@ -86,6 +86,7 @@ struct GemmArgs {
   // multiple of 4), activation ring stages (even), partial accumulators (MMA
   // issuers), accumulator slots and the TMEM columns of one accumulator
   int w_stages, b_stages, n_parts, d_slots, d_cols;
+  int raster_rows;  // 1: grouped item order (see decode_item), 0: tile-major
   long long timeout_cycles;
 };
 

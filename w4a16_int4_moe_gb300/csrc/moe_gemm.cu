@@ -202,11 +202,31 @@ struct ItemDesc {
 };
 
 // Which routing block and weight tile item `it` is, and its expert (-1: skip).
+// Item order. Plain: tile-major (all blocks for tile 0, then tile 1, ...),
+// so the CTAs working at one time stream different experts' weights and
+// every block's token rows are read once per tile. Rastered (kRaster, for
+// grouped GEMMs whose token rows are too many for L2): blocks in groups of
+// kRasterBlocks consecutive blocks, tile-major inside a group, so a group's
+// token rows stay in L2 across the tiles. The rastered order is a separate
+// kernel instantiation: its integer divisions, even untaken, cost the plain
+// kernel measurable time on short items (instruction footprint).
+constexpr int kRasterBlocks = 8;
+
+template <bool kRaster>
 __device__ __forceinline__ ItemDesc decode_item(const GemmArgs& a, int it, int num_blocks,
                                                 int blocks_per_expert) {
   ItemDesc d;
-  d.tile = it / num_blocks;
-  d.blk = it - d.tile * num_blocks;
+  if constexpr (kRaster) {
+    const int per_group = kRasterBlocks * a.n_tiles;
+    const int group = it / per_group;
+    const int rem = it - group * per_group;
+    const int gsize = min(kRasterBlocks, num_blocks - group * kRasterBlocks);
+    d.tile = rem / gsize;
+    d.blk = group * kRasterBlocks + (rem - d.tile * gsize);
+  } else {
+    d.tile = it / num_blocks;
+    d.blk = it - d.tile * num_blocks;
+  }
   int e = -1;
   if (a.family == kIndexed) {
     e = __ldg(a.expert_ids + d.blk);
@@ -290,10 +310,11 @@ __device__ __forceinline__ void dequant_group(const uint4 q, uint32_t scale_bits
 // item. Global stage u -> A slot u % 4 (dequant warpgroup u % 4), B slot
 // u % BS, weight slot u % WS (WS % 4 == 0, BS even).
 
-// kGlu: the fused-activation epilogue (out_mode kOutGluBf16) is compiled
-// into its own instantiation so that it cannot change the register
-// allocation of the plain kernel.
-template <bool kGlu>
+// kGlu: the fused-activation epilogue (out_mode kOutGluBf16) and kRaster:
+// the grouped item order are compiled into their own instantiations so that
+// they cannot change the register allocation or the instruction footprint
+// of the plain kernel.
+template <bool kGlu, bool kRaster>
 __global__ void __launch_bounds__(kThreads, 1)
     w4a16_moe_gemm_kernel(const __grid_constant__ GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
@@ -428,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       RingPos wp;
       bool ok = true;
       for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
-        const ItemDesc d = decode_item(args, it, num_blocks, bpe);
+        const ItemDesc d = decode_item<kRaster>(args, it, num_blocks, bpe);
         if (d.e < 0) continue;
         const uint8_t* src = args.wpack + static_cast<long long>(d.e) * args.expert_bytes +
                              static_cast<long long>(d.tile) * args.k_steps * kStepBytes;
@@ -470,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       const uint64_t b_desc0 = smem_desc_sw128_kmajor(smem_u32(sm.b_ring));
       for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
-        const ItemDesc d = decode_item(args, it, num_blocks, bpe);
+        const ItemDesc d = decode_item<kRaster>(args, it, num_blocks, bpe);
         if (d.e < 0) continue;
         if (!wait_phase(B.itf(ip.slot), ip.phase, abort_flag, status, kWhereMmaItem, tmo)) {
           ok = false;
@@ -526,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // loads of the routing tensors stay off the copy and MMA critical path.
     RingPos ip;
     for (int it = blockIdx.x; it < items; it += gridDim.x) {
-      const ItemDesc d = decode_item(args, it, num_blocks, bpe);
+      const ItemDesc d = decode_item<kRaster>(args, it, num_blocks, bpe);
       if (d.e < 0) continue;
       if (!warp_wait_phase(B.ite(ip.slot), ip.phase ^ 1, abort_flag, status, kWhereRouter, tmo))
         break;
@@ -569,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t issued = 0;  // stages whose b_full phase this thread started
       bool ok = true;
       for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
-        const ItemDesc d = decode_item(args, it, num_blocks, bpe);
+        const ItemDesc d = decode_item<kRaster>(args, it, num_blocks, bpe);
         if (d.e < 0) continue;
         const int box_row = (args.family == kMasked) ? d.e * args.m + (d.blk - d.e * bpe) * bm
                                                      : d.blk * bm;
@@ -616,7 +637,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int u = 0;             // global stage index of this CTA
     bool ok = true;
     for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
-      const ItemDesc d = decode_item(args, it, num_blocks, bpe);
+      const ItemDesc d = decode_item<kRaster>(args, it, num_blocks, bpe);
       if (d.e < 0) continue;
       // item-local stages of this warpgroup: st = wg - u (mod 4), step 4
       for (int st = (wg - u) & 3; st < n_stp; st += 4) {
@@ -680,7 +701,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     grid_dependency_wait();  // the previous grid may zero the output this one adds into
     RingPos ip, dp;
     for (int it = blockIdx.x; it < items; it += gridDim.x) {
-      const ItemDesc d = decode_item(args, it, num_blocks, bpe);
+      const ItemDesc d = decode_item<kRaster>(args, it, num_blocks, bpe);
       if (d.e < 0) continue;
       const int islot = ip.slot;
       const int dslot = dp.slot;
@@ -906,7 +927,9 @@ cudaError_t launch_moe_gemm(const GemmArgs& args, int grid, bool dependent, cuda
   size_t smem = gemm_smem_bytes(args.block_m, args.w_stages, args.b_stages);
   if (smem < 118 * 1024) smem = 118 * 1024;
   const bool glu = args.out_mode == kOutGluBf16;
-  auto kernel = glu ? w4a16_moe_gemm_kernel<true> : w4a16_moe_gemm_kernel<false>;
+  auto kernel = glu                ? w4a16_moe_gemm_kernel<true, false>
+                : args.raster_rows ? w4a16_moe_gemm_kernel<false, true>
+                                   : w4a16_moe_gemm_kernel<false, false>;
   cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
