@@ -107,9 +107,17 @@ def _check_pair(p, device, bm, cols_gu=None, cols_dn=None, what=""):
 
 # ------------------------------------------------------------ small shapes --
 
-@pytest.mark.parametrize("bm", [16, 32, 48, 64])
+@pytest.mark.parametrize("bm", [16, 32, 48, 64, 128])
 def test_tiny_all_block_sizes(cuda_dev, bm):
     _check_pair(wl.tiny(), cuda_dev, bm, what=f"tiny bm={bm}")
+
+
+@pytest.mark.parametrize("bm", [64, 128])
+def test_blocks_of_mixed_fill(cuda_dev, bm):
+    # 50..73 rows per expert: at block_m 64 an expert fills one block and
+    # part of a second, at block_m 128 a block is between 39% and 57% full
+    p = wl.uniform_problem(256, 1024, 512, 16, 4, seed=61)
+    _check_pair(p, cuda_dev, bm, what=f"mixed fill bm={bm}")
 
 
 @pytest.mark.parametrize("tokens,hidden,inter,experts,topk,bm", [
@@ -157,7 +165,7 @@ def test_schedules_are_bitwise_identical(cuda_dev):
     pk = _pack(p.q_gu, p.s_gu, cuda_dev)
     ref = None
     for bm, st, bst, grid in [(16, 8, 8, 0), (32, 4, 16, 0), (64, 8, 8, 3), (64, 4, 12, 1),
-                              (16, 12, 12, 5), (48, 7, 8, 7)]:
+                              (16, 12, 12, 5), (48, 7, 8, 7), (128, 8, 8, 0)]:
         routing = _routing(p.topk_ids, p.num_experts, bm, cuda_dev)
         g = _gate_up(p, pk, routing, _plan(bm, 2 * p.inter, p.hidden, st, bst, grid), cuda_dev)
         bits = bf16_bits(g)[_routed(p)]
