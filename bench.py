@@ -29,6 +29,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -112,12 +113,19 @@ class ClockSampler:
 
     def __init__(self):
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", "clocks_bench.csv")
+        # the raw samples go to W4A16_CLOCKS_CSV when it is set, else to a
+        # temporary file that is removed once summarised
+        self.keep = "W4A16_CLOCKS_CSV" in os.environ
+        self.path = os.environ.get("W4A16_CLOCKS_CSV", "")
         self.window = None
 
     def start(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            if self.keep:
+                os.makedirs(os.path.dirname(os.path.abspath(self.path)), exist_ok=True)
+            else:
+                fd, self.path = tempfile.mkstemp(suffix="_clocks.csv")
+                os.close(fd)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
@@ -161,6 +169,8 @@ class ClockSampler:
                     continue
                 active = [n for n, v in zip(names, parts[6:10]) if v.lower() == "active"]
                 samples.append((ts, sm, mx, active))
+        if not self.keep:
+            os.remove(self.path)
         if not samples:
             return None
         inside = samples
