@@ -876,10 +876,12 @@ size_t gemm_smem_bytes(int block_m, int w_stages, int b_stages) {
 bool tmem_accumulators(int block_m, int k_steps, int* d_cols, int* parts, int* d_slots) {
   const int dcols = (block_m + 31) / 32 * 32;
   const int free_cols = kTmemCols - kASlots * kAColsPerSlot;
-  // Four issuers by default; short reductions (a few stages per item) take
-  // two, so that more items fit in TMEM at once and the epilogue reads half
-  // as many partial accumulators per item.
-  int p = k_steps <= 8 ? 2 : kMaxIssuers;
+  // Four issuers while their accumulators fit: one thread issues a
+  // tcgen05.mma only every hundred-odd cycles, so even short reductions
+  // (TP8 down, k = 256) gain more from four parallel MMA chains (measured 3-7%)
+  // than from holding more items in TMEM at once with two.
+  (void)k_steps;
+  int p = kMaxIssuers;
   while (p > 1 && p * dcols > free_cols) p >>= 1;
   if (p * dcols > free_cols) return false;
   *d_cols = dcols;
