@@ -208,7 +208,7 @@ size_t w4a16_workspace_size(const w4a16_plan_t* plan, int rows, int k);
  *   GATE_UP_SILU: as GATE_UP with n = 2*inter (gate rows, then up rows), but
  *            out BF16 [tokens*topk, n/2] receives
  *            bf16( silu(g) * u ), g = bf16(x . Wgate^T), u = bf16(x . Wup^T),
- *            silu(g) = g / (1 + exp(-g)) in fp32: the same values as GATE_UP
+ *            silu(g) as in w4a16_silu_and_mul: the same values as GATE_UP
  *            followed by w4a16_silu_and_mul, in one pass (the activation is
  *            this library's reading, see w4a16_silu_and_mul). Requires
  *            packed with W4A16_LAYOUT_KTILE64_GLU16, plan->layout equal to
@@ -278,7 +278,9 @@ w4a16_status w4a16_topk_softmax(const void* logits, int logits_dtype, int tokens
  * Activation between gate_up and down (the pages leave it out of the timed
  * pair, [P-arex] "六个场景的逐层测量与限定条件"; its form is this library's
  * reading): in BF16 [rows, 2*inter] = [gate | up]; out BF16 [rows, inter]
- * = bf16(silu(gate) * up), computed in fp32. inter % 8 == 0.
+ * = bf16(silu(gate) * up) with silu(g) = g / (1 + e^-g), computed in fp32
+ * with the fast exponential and division (a few fp32 ulps before the BF16
+ * rounding). inter % 8 == 0.
  */
 w4a16_status w4a16_silu_and_mul(const uint16_t* in, int rows, int inter, uint16_t* out,
                                 void* stream);

@@ -767,17 +767,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if constexpr (kGlu) {
           // Fused activation: lanes 0..15 hold gate columns, lanes 16..31 the
-          // matching up columns (W4A16_LAYOUT_KTILE64_GLU16). Both are rounded
-          // to BF16 as the unfused gate_up output would be, then combined as
-          // silu(g) * u in FP32; the 16 x 16 results are staged transposed and
-          // written 4 columns of one token row at a time.
+          // matching up columns (W4A16_LAYOUT_KTILE64_GLU16). Per pair of
+          // token columns, lane l < 16 computes column 2m and lane l + 16
+          // column 2m + 1: one exchange gives each the other half of its
+          // (gate, up) pair. Both are rounded to BF16 as the unfused gate_up
+          // output would be, then combined as in w4a16_silu_and_mul; the
+          // 16 x 16 results are staged transposed and written 4 columns of
+          // one token row at a time.
+          const bool hi_lane = lane >= 16;
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) {
-            const float mine = __uint_as_float(v[jj]);
-            const float other = __shfl_xor_sync(0xffffffffu, mine, 16);
-            const float g = __bfloat162float(__float2bfloat16_rn(mine));
-            const float u = __bfloat162float(__float2bfloat16_rn(other));
-            if (lane < 16) tile[jj * 16 + lane] = g / (1.0f + expf(-g)) * u;
+          for (int m = 0; m < 8; ++m) {
+            const float v0 = __uint_as_float(v[2 * m]);
+            const float v1 = __uint_as_float(v[2 * m + 1]);
+            const float recv = __shfl_xor_sync(0xffffffffu, hi_lane ? v0 : v1, 16);
+            const float g = __bfloat162float(__float2bfloat16_rn(hi_lane ? recv : v0));
+            const float u = __bfloat162float(__float2bfloat16_rn(hi_lane ? v1 : recv));
+            tile[(2 * m + (hi_lane ? 1 : 0)) * 16 + (lane & 15)] =
+                __fdividef(g, 1.0f + __expf(-g)) * u;
           }
           __syncwarp();
           const int inter = args.n >> 1;
