@@ -60,7 +60,16 @@ constexpr int kItemSlots = 8;                 // routing-info ring depth (items)
 constexpr int kMaxDSlots = 4;                 // accumulator slots (items in flight in TMEM)
 constexpr int kMaxIssuers = 4;
 constexpr int kTmemCols = 512;
-constexpr int kEpiTileBytes = 4 * 16 * 32 * 4;  // epilogue transpose staging
+// Epilogue staging rows per warp: the whole block for blocks of 48 or 64 rows
+// (so that the accumulator slot is freed before the stores), else 16 rows: a
+// block of up to 32 rows mostly holds at most 16 (decode), and the shared
+// memory of blocks above 64 rows goes to the activation ring.
+__host__ __device__ constexpr int epi_stage_rows(int block_m) {
+  return (block_m > 32 && block_m <= 64) ? (block_m + 15) / 16 * 16 : 16;
+}
+__host__ __device__ constexpr int epi_tile_bytes(int block_m) {
+  return 4 * epi_stage_rows(block_m) * 32 * 4;  // 4 epilogue warps x rows x 32 FP32
+}
 
 // Warp roles. The dequant and epilogue warpgroups start at multiples of 4
 // warps, so that warp % 4 selects the TMEM lane quarter each warp may access.
@@ -86,7 +95,7 @@ struct Smem {
   float* info_wt;       // [kItemSlots][block_m]: top-k weight (down pass)
   int* info_n16;        // [kItemSlots]: MMA N of the item
   int* info_rows;       // [kItemSlots]: real rows (last real row + 1)
-  float* epi_tile;      // [4 epilogue warps][16 token rows][32 weight rows]
+  float* epi_tile;      // [4 epilogue warps][stage rows][32 weight rows]
   uint64_t* bars;
   uint32_t* tmem_base;
   volatile int* abort_flag;
@@ -338,11 +347,13 @@ __device__ __forceinline__ void dequant_group(const uint4 q, uint32_t scale_bits
 // item. Global stage u -> A slot u % 4 (dequant warpgroup u % 4), B slot
 // u % BS, weight slot u % WS (WS % 4 == 0, BS even).
 
-// kGlu: the fused-activation epilogue (out_mode kOutGluBf16) and kRaster:
-// the grouped item order are compiled into their own instantiations so that
-// they cannot change the register allocation or the instruction footprint
-// of the plain kernel.
-template <bool kGlu, bool kRaster>
+// kGlu: the fused-activation epilogue (out_mode kOutGluBf16), kRaster: the
+// grouped item order, and kEarly: the epilogue that frees the accumulator
+// slot before its stores (blocks of 48 or 64 rows, whose accumulators fill
+// TMEM's single slot) are compiled into their own instantiations so that they
+// cannot change the register allocation or the instruction footprint of the
+// plain kernel.
+template <bool kGlu, bool kRaster, bool kEarly>
 __global__ void __launch_bounds__(kThreads, 1)
     w4a16_moe_gemm_kernel(const __grid_constant__ GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
@@ -375,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   off += kItemSlots * sizeof(int);
   off = align_up(off, 16);
   sm.epi_tile = reinterpret_cast<float*>(base + off);
-  off += kEpiTileBytes;
+  off += epi_tile_bytes(bm);
   off = align_up(off, 8);
   sm.bars = reinterpret_cast<uint64_t*>(base + off);
   off += (2 * WS + 2 * BS + kNumBarsFixed) * 8;
@@ -717,14 +728,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ======================= epilogue =======================================
     // Warp q reads TMEM lanes 32q..32q+31 (weight rows of the tile = output
     // columns tile*128 + 32q + lane): per 16 token columns it adds the
-    // partial accumulators in a fixed order, stages the 32 x 16 values
-    // transposed in shared memory, and then writes 4 consecutive output
-    // columns of one token row per operation (an 8-byte BF16 store, or a
-    // float4 atomic add of the top-k weighted values in the down pass).
+    // partial accumulators in a fixed order, stages the values transposed in
+    // shared memory, and then writes 4 consecutive output columns of one
+    // token row per operation (an 8-byte BF16 store, or a float4 atomic add
+    // of the top-k weighted values in the down pass).
     const int quarter = warp & 3;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const int live_parts = min(parts, args.k_steps);  // partial q holds k step q first
-    float* tile = sm.epi_tile + quarter * (16 * 32);    // [16 token rows][32 weight rows]
+    // this warp's staging tile: [stage_rows token rows][32 weight rows]
+    const int stage_rows = epi_stage_rows(bm);
+    float* tile = sm.epi_tile + quarter * (stage_rows * 32);
     const int c4 = lane & 7;                            // 4-column group of this lane
     const int jr0 = lane >> 3;                          // first token row of this lane
     const bool vec4 = (args.n & 3) == 0;
@@ -745,112 +758,241 @@ __global__ void __launch_bounds__(kThreads, 1)
       // first output column of this lane's 4-column group
       const int ng = d.tile * kTileRows + quarter * 32 + 4 * c4;
       const uint32_t dcol0 = tmem + lane_base + d_col_base + dslot * parts * args.d_cols;
-      for (int j0 = 0; j0 < rows; j0 += 16) {
-        // the first two partial accumulators with one TMEM round trip, any
-        // further ones one by one; summed in the fixed order
-        // ((p0 + p1) + p2) + p3
-        uint32_t v[16], w[16];
-        tmem_ld_32x32b_x16(dcol0 + j0, v);
-        if (live_parts > 1) tmem_ld_32x32b_x16(dcol0 + args.d_cols + j0, w);
-        tmem_ld_wait();
-        if (live_parts > 1) {
+      if constexpr (kEarly) {
+        // Token rows go through the warp's staging tile in passes. When the
+        // whole block fits (stage_rows), one pass first moves every partial sum
+        // out of TMEM and frees the accumulator slot, so that the next item's
+        // MMAs overlap this item's stores; otherwise each 16-row pass is staged
+        // and written, and the slot is freed at the end.
+        const bool early = rows <= stage_rows;  // (kEarly launches only)
+        const int pass_rows = early ? stage_rows : 16;
+        for (int p0 = 0; p0 < rows; p0 += pass_rows) {
+          const int p1 = min(rows, p0 + pass_rows);
+          for (int j0 = p0; j0 < p1; j0 += 16) {
+            float* slab = tile + (j0 - p0) * 32;  // 16 token rows x 32
+            // the first two partial accumulators with one TMEM round trip, any
+            // further ones one by one; summed in the fixed order
+            // ((p0 + p1) + p2) + p3
+            uint32_t v[16], w[16];
+            tmem_ld_32x32b_x16(dcol0 + j0, v);
+            if (live_parts > 1) tmem_ld_32x32b_x16(dcol0 + args.d_cols + j0, w);
+            tmem_ld_wait();
+            if (live_parts > 1) {
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj)
-            v[jj] = __float_as_uint(__uint_as_float(v[jj]) + __uint_as_float(w[jj]));
-        }
-        for (int p = 2; p < live_parts; ++p) {
-          tmem_ld_32x32b_x16(dcol0 + p * args.d_cols + j0, w);
-          tmem_ld_wait();
+              for (int jj = 0; jj < 16; ++jj)
+                v[jj] = __float_as_uint(__uint_as_float(v[jj]) + __uint_as_float(w[jj]));
+            }
+            for (int p = 2; p < live_parts; ++p) {
+              tmem_ld_32x32b_x16(dcol0 + p * args.d_cols + j0, w);
+              tmem_ld_wait();
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj)
-            v[jj] = __float_as_uint(__uint_as_float(v[jj]) + __uint_as_float(w[jj]));
-        }
-        if constexpr (kGlu) {
-          // Fused activation: lanes 0..15 hold gate columns, lanes 16..31 the
-          // matching up columns (W4A16_LAYOUT_KTILE64_GLU16). Per pair of
-          // token columns, lane l < 16 computes column 2m and lane l + 16
-          // column 2m + 1: one exchange gives each the other half of its
-          // (gate, up) pair. Both are rounded to BF16 as the unfused gate_up
-          // output would be, then combined as in w4a16_silu_and_mul; the
-          // 16 x 16 results are staged transposed and written 4 columns of
-          // one token row at a time.
-          const bool hi_lane = lane >= 16;
+              for (int jj = 0; jj < 16; ++jj)
+                v[jj] = __float_as_uint(__uint_as_float(v[jj]) + __uint_as_float(w[jj]));
+            }
+            if constexpr (kGlu) {
+              // Fused activation: lanes 0..15 hold gate columns, lanes 16..31 the
+              // matching up columns (W4A16_LAYOUT_KTILE64_GLU16). Per pair of
+              // token columns, lane l < 16 computes column 2m and lane l + 16
+              // column 2m + 1: one exchange gives each the other half of its
+              // (gate, up) pair. Both are rounded to BF16 as the unfused gate_up
+              // output would be, then combined as in w4a16_silu_and_mul; the
+              // 16 x 16 results are staged transposed ([token row][16]).
+              const bool hi_lane = lane >= 16;
 #pragma unroll
-          for (int m = 0; m < 8; ++m) {
-            const float v0 = __uint_as_float(v[2 * m]);
-            const float v1 = __uint_as_float(v[2 * m + 1]);
-            const float recv = __shfl_xor_sync(0xffffffffu, hi_lane ? v0 : v1, 16);
-            const float g = __bfloat162float(__float2bfloat16_rn(hi_lane ? recv : v0));
-            const float u = __bfloat162float(__float2bfloat16_rn(hi_lane ? v1 : recv));
-            tile[(2 * m + (hi_lane ? 1 : 0)) * 16 + (lane & 15)] =
-                __fdividef(g, 1.0f + __expf(-g)) * u;
-          }
-          __syncwarp();
-          const int inter = args.n >> 1;
-          const int gcol = d.tile * 64 + quarter * 16 + 4 * (lane & 3);
-          for (int jr = lane >> 2; jr < 16 && j0 + jr < rows; jr += 8) {
-            const int dr = idst[j0 + jr];
-            if (dr < 0) continue;
-            const float4 x = *reinterpret_cast<const float4*>(tile + jr * 16 + 4 * (lane & 3));
-            const __nv_bfloat162 lo = __floats2bfloat162_rn(x.x, x.y);
-            const __nv_bfloat162 hi = __floats2bfloat162_rn(x.z, x.w);
-            uint2 pk;
-            pk.x = *reinterpret_cast<const uint32_t*>(&lo);
-            pk.y = *reinterpret_cast<const uint32_t*>(&hi);
-            *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(args.out) +
-                                      static_cast<long long>(dr) * inter + gcol) = pk;
-          }
-          __syncwarp();  // the tile is rewritten by the next 16 token columns
-        } else {
-          // transpose through shared memory: tile[jj][lane] = value of token
-          // column j0 + jj for weight row lane
-#pragma unroll
-          for (int jj = 0; jj < 16; ++jj) tile[jj * 32 + lane] = __uint_as_float(v[jj]);
-          __syncwarp();
-          // lane (jr, c4) writes token row j0 + jr, columns ng..ng+3
-          for (int jr = jr0; jr < 16 && j0 + jr < rows; jr += 4) {
-            const int j = j0 + jr;
-            const int dr = idst[j];
-            if (dr < 0 || ng >= args.n) continue;
-            const float4 x = *reinterpret_cast<const float4*>(tile + jr * 32 + 4 * c4);
-            if (args.out_mode == kOutF32WeightedAdd) {
-              float* o = static_cast<float*>(args.out) + static_cast<long long>(dr) * args.n + ng;
-              const float wt = iwt[j];
-              if (vec4) {
-                atomicAdd(reinterpret_cast<float4*>(o),
-                          make_float4(wt * x.x, wt * x.y, wt * x.z, wt * x.w));
-              } else {
-                atomicAdd(o, wt * x.x);
-                if (ng + 1 < args.n) atomicAdd(o + 1, wt * x.y);
-                if (ng + 2 < args.n) atomicAdd(o + 2, wt * x.z);
-                if (ng + 3 < args.n) atomicAdd(o + 3, wt * x.w);
+              for (int m = 0; m < 8; ++m) {
+                const float v0 = __uint_as_float(v[2 * m]);
+                const float v1 = __uint_as_float(v[2 * m + 1]);
+                const float recv = __shfl_xor_sync(0xffffffffu, hi_lane ? v0 : v1, 16);
+                const float g = __bfloat162float(__float2bfloat16_rn(hi_lane ? recv : v0));
+                const float u = __bfloat162float(__float2bfloat16_rn(hi_lane ? v1 : recv));
+                slab[(2 * m + (hi_lane ? 1 : 0)) * 16 + (lane & 15)] =
+                    __fdividef(g, 1.0f + __expf(-g)) * u;
               }
             } else {
-              __nv_bfloat16* o =
-                  static_cast<__nv_bfloat16*>(args.out) + static_cast<long long>(dr) * args.n + ng;
-              const __nv_bfloat162 lo = __floats2bfloat162_rn(x.x, x.y);
-              const __nv_bfloat162 hi = __floats2bfloat162_rn(x.z, x.w);
-              if (vec4) {
+              // transposed: slab[jj][lane] = value of token column j0 + jj for
+              // weight row lane
+#pragma unroll
+              for (int jj = 0; jj < 16; ++jj) slab[jj * 32 + lane] = __uint_as_float(v[jj]);
+            }
+          }
+          __syncwarp();
+          if (early) {
+            tc_fence_before();
+            if (lane == 0) mbar_arrive(B.acce(dslot));
+          }
+          for (int j0 = p0; j0 < p1; j0 += 16) {
+            const float* slab = tile + (j0 - p0) * 32;
+            if constexpr (kGlu) {
+              const int inter = args.n >> 1;
+              const int gcol = d.tile * 64 + quarter * 16 + 4 * (lane & 3);
+              for (int jr = lane >> 2; jr < 16 && j0 + jr < rows; jr += 8) {
+                const int dr = idst[j0 + jr];
+                if (dr < 0) continue;
+                const float4 x = *reinterpret_cast<const float4*>(slab + jr * 16 + 4 * (lane & 3));
+                const __nv_bfloat162 lo = __floats2bfloat162_rn(x.x, x.y);
+                const __nv_bfloat162 hi = __floats2bfloat162_rn(x.z, x.w);
                 uint2 pk;
                 pk.x = *reinterpret_cast<const uint32_t*>(&lo);
                 pk.y = *reinterpret_cast<const uint32_t*>(&hi);
-                *reinterpret_cast<uint2*>(o) = pk;
-              } else {
-                o[0] = lo.x;
-                if (ng + 1 < args.n) o[1] = lo.y;
-                if (ng + 2 < args.n) o[2] = hi.x;
-                if (ng + 3 < args.n) o[3] = hi.y;
+                *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(args.out) +
+                                          static_cast<long long>(dr) * inter + gcol) = pk;
+              }
+            } else {
+              // lane (jr, c4) writes token row j0 + jr, columns ng..ng+3
+              for (int jr = jr0; jr < 16 && j0 + jr < rows; jr += 4) {
+                const int j = j0 + jr;
+                const int dr = idst[j];
+                if (dr < 0 || ng >= args.n) continue;
+                const float4 x = *reinterpret_cast<const float4*>(slab + jr * 32 + 4 * c4);
+                if (args.out_mode == kOutF32WeightedAdd) {
+                  float* o =
+                      static_cast<float*>(args.out) + static_cast<long long>(dr) * args.n + ng;
+                  const float wt = iwt[j];
+                  if (vec4) {
+                    atomicAdd(reinterpret_cast<float4*>(o),
+                              make_float4(wt * x.x, wt * x.y, wt * x.z, wt * x.w));
+                  } else {
+                    atomicAdd(o, wt * x.x);
+                    if (ng + 1 < args.n) atomicAdd(o + 1, wt * x.y);
+                    if (ng + 2 < args.n) atomicAdd(o + 2, wt * x.z);
+                    if (ng + 3 < args.n) atomicAdd(o + 3, wt * x.w);
+                  }
+                } else {
+                  __nv_bfloat16* o = static_cast<__nv_bfloat16*>(args.out) +
+                                     static_cast<long long>(dr) * args.n + ng;
+                  const __nv_bfloat162 lo = __floats2bfloat162_rn(x.x, x.y);
+                  const __nv_bfloat162 hi = __floats2bfloat162_rn(x.z, x.w);
+                  if (vec4) {
+                    uint2 pk;
+                    pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+                    pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+                    *reinterpret_cast<uint2*>(o) = pk;
+                  } else {
+                    o[0] = lo.x;
+                    if (ng + 1 < args.n) o[1] = lo.y;
+                    if (ng + 2 < args.n) o[2] = hi.x;
+                    if (ng + 3 < args.n) o[3] = hi.y;
+                  }
+                }
               }
             }
           }
-          __syncwarp();  // the tile is rewritten by the next 16 token columns
+          __syncwarp();  // the tile is rewritten by the next pass
         }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(B.acce(dslot));
-        mbar_arrive(B.ite(islot));
+        if (!early) tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (!early) mbar_arrive(B.acce(dslot));
+          mbar_arrive(B.ite(islot));
+        }
+      } else {
+        for (int j0 = 0; j0 < rows; j0 += 16) {
+          // the first two partial accumulators with one TMEM round trip, any
+          // further ones one by one; summed in the fixed order
+          // ((p0 + p1) + p2) + p3
+          uint32_t v[16], w[16];
+          tmem_ld_32x32b_x16(dcol0 + j0, v);
+          if (live_parts > 1) tmem_ld_32x32b_x16(dcol0 + args.d_cols + j0, w);
+          tmem_ld_wait();
+          if (live_parts > 1) {
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj)
+              v[jj] = __float_as_uint(__uint_as_float(v[jj]) + __uint_as_float(w[jj]));
+          }
+          for (int p = 2; p < live_parts; ++p) {
+            tmem_ld_32x32b_x16(dcol0 + p * args.d_cols + j0, w);
+            tmem_ld_wait();
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj)
+              v[jj] = __float_as_uint(__uint_as_float(v[jj]) + __uint_as_float(w[jj]));
+          }
+          if constexpr (kGlu) {
+            // Fused activation: lanes 0..15 hold gate columns, lanes 16..31 the
+            // matching up columns (W4A16_LAYOUT_KTILE64_GLU16). Per pair of
+            // token columns, lane l < 16 computes column 2m and lane l + 16
+            // column 2m + 1: one exchange gives each the other half of its
+            // (gate, up) pair. Both are rounded to BF16 as the unfused gate_up
+            // output would be, then combined as in w4a16_silu_and_mul; the
+            // 16 x 16 results are staged transposed and written 4 columns of
+            // one token row at a time.
+            const bool hi_lane = lane >= 16;
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+              const float v0 = __uint_as_float(v[2 * m]);
+              const float v1 = __uint_as_float(v[2 * m + 1]);
+              const float recv = __shfl_xor_sync(0xffffffffu, hi_lane ? v0 : v1, 16);
+              const float g = __bfloat162float(__float2bfloat16_rn(hi_lane ? recv : v0));
+              const float u = __bfloat162float(__float2bfloat16_rn(hi_lane ? v1 : recv));
+              tile[(2 * m + (hi_lane ? 1 : 0)) * 16 + (lane & 15)] =
+                  __fdividef(g, 1.0f + __expf(-g)) * u;
+            }
+            __syncwarp();
+            const int inter = args.n >> 1;
+            const int gcol = d.tile * 64 + quarter * 16 + 4 * (lane & 3);
+            for (int jr = lane >> 2; jr < 16 && j0 + jr < rows; jr += 8) {
+              const int dr = idst[j0 + jr];
+              if (dr < 0) continue;
+              const float4 x = *reinterpret_cast<const float4*>(tile + jr * 16 + 4 * (lane & 3));
+              const __nv_bfloat162 lo = __floats2bfloat162_rn(x.x, x.y);
+              const __nv_bfloat162 hi = __floats2bfloat162_rn(x.z, x.w);
+              uint2 pk;
+              pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+              pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+              *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(args.out) +
+                                        static_cast<long long>(dr) * inter + gcol) = pk;
+            }
+            __syncwarp();  // the tile is rewritten by the next 16 token columns
+          } else {
+            // transpose through shared memory: tile[jj][lane] = value of token
+            // column j0 + jj for weight row lane
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) tile[jj * 32 + lane] = __uint_as_float(v[jj]);
+            __syncwarp();
+            // lane (jr, c4) writes token row j0 + jr, columns ng..ng+3
+            for (int jr = jr0; jr < 16 && j0 + jr < rows; jr += 4) {
+              const int j = j0 + jr;
+              const int dr = idst[j];
+              if (dr < 0 || ng >= args.n) continue;
+              const float4 x = *reinterpret_cast<const float4*>(tile + jr * 32 + 4 * c4);
+              if (args.out_mode == kOutF32WeightedAdd) {
+                float* o = static_cast<float*>(args.out) + static_cast<long long>(dr) * args.n + ng;
+                const float wt = iwt[j];
+                if (vec4) {
+                  atomicAdd(reinterpret_cast<float4*>(o),
+                            make_float4(wt * x.x, wt * x.y, wt * x.z, wt * x.w));
+                } else {
+                  atomicAdd(o, wt * x.x);
+                  if (ng + 1 < args.n) atomicAdd(o + 1, wt * x.y);
+                  if (ng + 2 < args.n) atomicAdd(o + 2, wt * x.z);
+                  if (ng + 3 < args.n) atomicAdd(o + 3, wt * x.w);
+                }
+              } else {
+                __nv_bfloat16* o = static_cast<__nv_bfloat16*>(args.out) +
+                                   static_cast<long long>(dr) * args.n + ng;
+                const __nv_bfloat162 lo = __floats2bfloat162_rn(x.x, x.y);
+                const __nv_bfloat162 hi = __floats2bfloat162_rn(x.z, x.w);
+                if (vec4) {
+                  uint2 pk;
+                  pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+                  pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+                  *reinterpret_cast<uint2*>(o) = pk;
+                } else {
+                  o[0] = lo.x;
+                  if (ng + 1 < args.n) o[1] = lo.y;
+                  if (ng + 2 < args.n) o[2] = hi.x;
+                  if (ng + 3 < args.n) o[3] = hi.y;
+                }
+              }
+            }
+            __syncwarp();  // the tile is rewritten by the next 16 token columns
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(B.acce(dslot));
+          mbar_arrive(B.ite(islot));
+        }
       }
       ip.next(kItemSlots);
       dp.next(args.d_slots);
@@ -872,7 +1014,7 @@ size_t gemm_smem_bytes(int block_m, int w_stages, int b_stages) {
   off += static_cast<size_t>(b_stages) * 2 * block_m * 128;
   off += static_cast<size_t>(w_stages) * kWStageBytes;
   off += static_cast<size_t>(kItemSlots) * block_m * (4 + 4) + 2 * kItemSlots * 4;
-  off = (off + 15) / 16 * 16 + kEpiTileBytes;
+  off = (off + 15) / 16 * 16 + epi_tile_bytes(block_m);
   off = (off + 7) / 8 * 8;
   off += (2 * w_stages + 2 * b_stages + kNumBarsFixed) * 8;
   off += 8;
@@ -965,9 +1107,14 @@ cudaError_t launch_moe_gemm(const GemmArgs& args, int grid, bool dependent, cuda
   size_t smem = gemm_smem_bytes(args.block_m, args.w_stages, args.b_stages);
   if (smem < 118 * 1024) smem = 118 * 1024;
   const bool glu = args.out_mode == kOutGluBf16;
-  auto kernel = glu                ? w4a16_moe_gemm_kernel<true, false>
-                : args.raster_rows ? w4a16_moe_gemm_kernel<false, true>
-                                   : w4a16_moe_gemm_kernel<false, false>;
+  // the whole-block staging tile exists for exactly these block sizes
+  const bool early = epi_stage_rows(args.block_m) > 16;
+  auto kernel = glu ? (early ? w4a16_moe_gemm_kernel<true, false, true>
+                             : w4a16_moe_gemm_kernel<true, false, false>)
+                : args.raster_rows ? (early ? w4a16_moe_gemm_kernel<false, true, true>
+                                            : w4a16_moe_gemm_kernel<false, true, false>)
+                                   : (early ? w4a16_moe_gemm_kernel<false, false, true>
+                                            : w4a16_moe_gemm_kernel<false, false, false>);
   cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
