@@ -61,6 +61,19 @@ def test_plan_follows_tok_e(lib):
         assert 8 <= p.b_stages <= 32 and p.b_stages % 4 == 0
 
 
+def test_plan_ring_depths():
+    # The deepest rings that fit in 227 KB of shared memory, an activation
+    # ring of at least six stages first: blocks of up to 32 rows get 8
+    # activation stages (16 k steps) and 16 weight stages; 64-row blocks,
+    # whose epilogue stages the whole block (32 KB), get 6 and 8.
+    decode = ops.w4a16_plan(576, 8, 48, 4096, 7168, 12.0)
+    assert (decode.block_m, decode.b_stages, decode.stages) == (32, 16, 16)
+    tp8 = ops.w4a16_plan(16, 8, 384, 512, 7168)
+    assert (tp8.block_m, tp8.b_stages, tp8.stages) == (16, 16, 16)
+    prefill = ops.w4a16_plan(8192, 8, 48, 4096, 7168, 81.3)
+    assert (prefill.block_m, prefill.b_stages, prefill.stages) == (64, 12, 8)
+
+
 def test_plan_rejects_bad_sizes(lib):
     p = ops.Plan()
     assert lib.w4a16_plan(0, 8, 0, 1, 1, 0.0, ctypes.byref(p)) == ops.W4A16_ERR_INVALID_ARG
