@@ -197,17 +197,23 @@ def cpu_oracle_sample(p, n_experts_sample=None):
         n_experts_sample = active.size
     rng = np.random.default_rng(0)
     chosen = np.sort(rng.choice(active, size=n_experts_sample, replace=False))
-    sub_ids = np.where(np.isin(p.topk_ids, chosen), p.topk_ids, -1)
+    # the tokens routed to the sampled experts, with their other picks masked,
+    # so that the per-token work also scales with the sample
+    picked = np.isin(p.topk_ids, chosen)
+    rows = picked.any(axis=1)
+    sub_ids = np.where(picked, p.topk_ids, -1)[rows]
+    x_sub, w_sub = p.x[rows], p.topk_weights[rows]
     t0 = time.perf_counter()
-    g = oracle.indexed_gate_up(p.x, sub_ids, p.q_gu, p.s_gu)
+    g = oracle.indexed_gate_up(x_sub, sub_ids, p.q_gu, p.s_gu)
     g_bits = oracle.f64_to_bf16_bits(np.nan_to_num(g))
     a_bits = oracle.silu_and_mul(g_bits)
-    oracle.indexed_down(a_bits, sub_ids, p.topk_weights, p.q_dn, p.s_dn)
+    oracle.indexed_down(a_bits, sub_ids, w_sub, p.q_dn, p.s_dn)
     dt = time.perf_counter() - t0
     scale = active.size / n_experts_sample
     return {"value": dt * scale * 1e6, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
             "sample": f"{n_experts_sample} of {active.size} active experts (all their routed rows, "
-                      f"gate_up+silu+down, float64 numpy), {dt:.2f} s, scaled x{scale:.2f}"}
+                      f"{int(rows.sum())} tokens; gate_up+silu+down, float64 numpy), {dt:.2f} s, "
+                      f"scaled x{scale:.2f}"}
 
 
 def dist_setup(n_gpus):
