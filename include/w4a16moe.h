@@ -68,8 +68,11 @@ enum {
                                       not graph-capturable ([P-lens]
                                       "ランタイムの考慮事項": trusted routing
                                       validation off = capturable)          */
-  W4A16_FLAG_ACCUMULATE = 2        /* DOWN: add into `out` instead of first
+  W4A16_FLAG_ACCUMULATE = 2,       /* DOWN: add into `out` instead of first
                                       zeroing it                            */
+  W4A16_FLAG_DETERMINISTIC = 8     /* DOWN: sum each token's top-k rows in a
+                                      fixed order (see
+                                      w4a16_moe_indexed_gemm)               */
 };
 /* Packed weight layouts (w4a16_prepack). One layout serves every family. */
 enum {
@@ -191,6 +194,14 @@ w4a16_status w4a16_unpack(const void* packed, int num_experts, int n, int k, int
 size_t w4a16_workspace_size(const w4a16_plan_t* plan, int rows, int k);
 
 /*
+ * Extra workspace bytes of a DOWN call with W4A16_FLAG_DETERMINISTIC, placed
+ * after the w4a16_workspace_size part: the weighted rows, capacity x n FP32,
+ * then the routing position of each of the numel = tokens * topk flattened
+ * rows (int32); each part rounded up to 256 bytes. 0 on bad sizes.
+ */
+size_t w4a16_deterministic_bytes(int capacity, int n, int numel);
+
+/*
  * Indexed W4A16 MoE GEMM ([P-arex] "调度由每个专家收到的 token 数决定",
  * "六个场景的逐层测量与限定条件"; [P-lens] "コア貢献").
  * Weights: `packed` from w4a16_prepack with [num_experts, n, k].
@@ -204,7 +215,14 @@ size_t w4a16_workspace_size(const w4a16_plan_t* plan, int rows, int k);
  *            topk_weights fp32 [tokens, topk]; out fp32 [tokens, n]:
  *            out[i / topk, :] += topk_weights.flat[i] * ( a[i, :] . W_e^T ).
  *            `out` is zeroed first unless W4A16_FLAG_ACCUMULATE. Summation
- *            order across the top-k rows of a token is not fixed.
+ *            order across the top-k rows of a token is not fixed, unless
+ *            W4A16_FLAG_DETERMINISTIC: then the GEMM stores every weighted
+ *            row (FP32) in the workspace and a second kernel sets
+ *            out[t, :] (+)= the sum of token t's rows in ascending top-k
+ *            slot order, so the result does not depend on the grid, the
+ *            block size or the timing. That needs ws_bytes >=
+ *            w4a16_workspace_size(plan, capacity, k) +
+ *            w4a16_deterministic_bytes(capacity, n, tokens * topk).
  *   GATE_UP_SILU: as GATE_UP with n = 2*inter (gate rows, then up rows), but
  *            out BF16 [tokens*topk, n/2] receives
  *            bf16( silu(g) * u ), g = bf16(x . Wgate^T), u = bf16(x . Wup^T),

@@ -123,6 +123,14 @@ def test_gemm_argument_checks_before_any_launch(lib):
     assert call(wsb=need - 1) == ops.W4A16_ERR_WORKSPACE
     assert call(cap=250) == ops.W4A16_ERR_INVALID_ARG          # not a multiple of block_m
     assert call(flags=64) == ops.W4A16_ERR_INVALID_ARG
+    # the deterministic sum is a DOWN option, and needs its own workspace part
+    assert call(flags=ops.W4A16_FLAG_DETERMINISTIC) == ops.W4A16_ERR_INVALID_ARG
+    det_w = ctypes.c_void_p(1 << 20)
+    assert call(mode=ops.W4A16_DOWN, w=det_w, flags=ops.W4A16_FLAG_DETERMINISTIC,
+                wsb=need) == ops.W4A16_ERR_WORKSPACE
+    det = ops.w4a16_deterministic_bytes(256, 1024, 128)
+    assert det == 256 * 1024 * 4 + 512   # rows, then 128 int32 positions (256-byte units)
+    assert ops.w4a16_deterministic_bytes(-1, 1024, 128) == 0
     assert call(out=ctypes.c_void_p((1 << 20) + 2)) == ops.W4A16_ERR_INVALID_ARG  # misaligned
     bad = ops.Plan.from_buffer_copy(plan)
     bad.block_m = 24

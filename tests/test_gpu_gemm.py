@@ -203,6 +203,69 @@ def test_over_allocated_routing_and_validation(cuda_dev):
     assert ops.w4a16_read_device_status(ws)[0] == ops.W4A16_OK
 
 
+def _down_det(p, packed, routing, plan, act_bits, device, out=None, accumulate=False):
+    sid, eid, ntp = routing
+    ws = ops.new_workspace(plan, device, sid.numel(), p.inter, det_n=p.hidden,
+                           det_numel=p.numel)
+    a = bf16_tensor(act_bits, device)
+    w = dev(p.topk_weights, device)
+    if out is None:
+        out = torch.full((p.tokens, p.hidden), float("nan"), dtype=torch.float32, device=device)
+    flags = ops.W4A16_FLAG_DETERMINISTIC | (ops.W4A16_FLAG_ACCUMULATE if accumulate else 0)
+    ops.w4a16_moe_indexed_gemm(ops.W4A16_DOWN, packed, p.num_experts, p.hidden, p.inter, a,
+                               p.tokens, p.topk, sid, eid, ntp, plan, ws, topk_weights=w,
+                               out=out, flags=flags)
+    st, word = ops.w4a16_read_device_status(ws)
+    assert st == ops.W4A16_OK, hex(word)
+    return out
+
+
+def test_down_deterministic(cuda_dev):
+    # W4A16_FLAG_DETERMINISTIC: each weighted row goes to the workspace and a
+    # second kernel adds every token's rows in top-k slot order. The output
+    # bits are then the same for every block size and grid, the values match
+    # the oracle, tokens without a local expert get 0, and ACCUMULATE adds.
+    p = wl.uniform_problem(256, 1024, 512, 16, 4, seed=63)
+    p.topk_ids[::7, 1] = -1          # some rows routed elsewhere
+    p.topk_ids[5, :] = -1            # a token with no local expert
+    pk = _pack(p.q_dn, p.s_dn, cuda_dev)
+    a_bits = wl.random_activations(np.random.default_rng(64), p.numel, p.inter)
+    a_bits[~_routed(p)] = 0
+    ref = oracle.indexed_down(a_bits, p.topk_ids, p.topk_weights, p.q_dn, p.s_dn)
+    outs = []
+    for bm, grid in ((16, 0), (32, 7), (48, 0), (64, 13)):
+        routing = _routing(p.topk_ids, p.num_experts, bm, cuda_dev)
+        y = _down_det(p, pk, routing, _plan(bm, p.hidden, p.inter, grid=grid), a_bits, cuda_dev)
+        outs.append(y.cpu().numpy())
+    for y in outs[1:]:
+        np.testing.assert_array_equal(y.view(np.uint32), outs[0].view(np.uint32))
+    assert np.all(outs[0][5] == 0.0)
+    assert_close(outs[0], ref, "deterministic down")
+    routing = _routing(p.topk_ids, p.num_experts, 32, cuda_dev)
+    prior = torch.full((p.tokens, p.hidden), 0.5, dtype=torch.float32, device=cuda_dev)
+    y2 = _down_det(p, pk, routing, _plan(32, p.hidden, p.inter), a_bits, cuda_dev, out=prior,
+                   accumulate=True)
+    np.testing.assert_array_equal(y2.cpu().numpy(), np.float32(0.5) + outs[1])
+
+
+def test_layer_deterministic_matches_oracle(cuda_dev):
+    p = wl.tiny(seed=65)
+
+    def t(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(cuda_dev)
+
+    gu = moe_mod.PackedExperts.from_checkpoint(t(p.q_gu), t(p.s_gu.view(np.int16)))
+    dn = moe_mod.PackedExperts.from_checkpoint(t(p.q_dn), t(p.s_dn.view(np.int16)))
+    layer = moe_mod.W4A16MoE(gu, dn, p.topk, p.tokens, device=cuda_dev, deterministic=True)
+    x, ids, w = bf16_tensor(p.x, cuda_dev), t(p.topk_ids), t(p.topk_weights)
+    y1 = layer.forward(x, ids, w).cpu().numpy()
+    y2 = layer.forward(x, ids, w).cpu().numpy()
+    np.testing.assert_array_equal(y1.view(np.uint32), y2.view(np.uint32))
+    _, _, _, y_ref = oracle.moe_layer(p.x, p.topk_ids, p.topk_weights, p.q_gu, p.s_gu,
+                                      p.q_dn, p.s_dn)
+    assert_close(y1, y_ref, "deterministic layer")
+
+
 def test_down_accumulate_flag(cuda_dev):
     p = wl.tiny(seed=7)
     pk = _pack(p.q_dn, p.s_dn, cuda_dev)

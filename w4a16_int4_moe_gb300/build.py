@@ -20,7 +20,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libw4a16moe.so")
 
-SOURCES = ["api.cu", "moe_gemm.cu", "align.cu", "prepack.cu", "act.cu", "noalloc.cu", "permute.cu", "topk.cu"]
+SOURCES = ["api.cu", "moe_gemm.cu", "align.cu", "prepack.cu", "act.cu", "noalloc.cu", "permute.cu",
+           "topk.cu", "det.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

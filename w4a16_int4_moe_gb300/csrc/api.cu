@@ -216,6 +216,11 @@ w4a16_status w4a16_unpack(const void* packed, int num_experts, int n, int k, int
                                    q, scales, static_cast<cudaStream_t>(stream)));
 }
 
+size_t w4a16_deterministic_bytes(int capacity, int n, int numel) {
+  if (capacity < 0 || n <= 0 || numel < 0) return 0;
+  return det_rows_bytes(capacity, n) + (static_cast<size_t>(numel) * 4 + 255) / 256 * 256;
+}
+
 size_t w4a16_workspace_size(const w4a16_plan_t* plan, int rows, int k) {
   (void)plan;
   if (rows <= 0 || k <= 0) return kStatusBytes;
@@ -239,12 +244,19 @@ w4a16_status w4a16_moe_indexed_gemm(int mode, const void* packed, int num_expert
     return W4A16_ERR_INVALID_ARG;
   if (tokens > 0 && a == nullptr) return W4A16_ERR_INVALID_ARG;
   if (mode == W4A16_DOWN && tokens > 0 && topk_weights == nullptr) return W4A16_ERR_INVALID_ARG;
-  if ((flags & ~(W4A16_FLAG_VALIDATE_ROUTING | W4A16_FLAG_ACCUMULATE)) != 0)
+  if ((flags & ~(W4A16_FLAG_VALIDATE_ROUTING | W4A16_FLAG_ACCUMULATE |
+                 W4A16_FLAG_DETERMINISTIC)) != 0)
     return W4A16_ERR_INVALID_ARG;
+  const bool det = (flags & W4A16_FLAG_DETERMINISTIC) != 0;
+  if (det && mode != W4A16_DOWN) return W4A16_ERR_INVALID_ARG;
   if (!aligned16(packed) || !aligned16(out) || (a != nullptr && !aligned16(a)))
     return W4A16_ERR_INVALID_ARG;
-  if (workspace == nullptr || ws_bytes < w4a16_workspace_size(plan, capacity, k))
-    return W4A16_ERR_WORKSPACE;
+  const size_t ws_base = w4a16_workspace_size(plan, capacity, k);
+  const long long numel_all = static_cast<long long>(tokens) * topk;
+  if (numel_all >= (1LL << 30)) return W4A16_ERR_UNSUPPORTED;
+  const size_t ws_det =
+      det ? w4a16_deterministic_bytes(capacity, n, static_cast<int>(numel_all)) : 0;
+  if (workspace == nullptr || ws_bytes < ws_base + ws_det) return W4A16_ERR_WORKSPACE;
   Pipeline pl;
   if (!plan_pipeline(*plan, k, &pl)) return W4A16_ERR_INVALID_ARG;
   // the fused activation needs the interleaved gate/up packing, and only it
@@ -292,6 +304,17 @@ w4a16_status w4a16_moe_indexed_gemm(int mode, const void* packed, int num_expert
       return W4A16_ERR_CUDA;
     return W4A16_OK;
   }
+  // deterministic down pass: the GEMM stores the weighted rows in the
+  // workspace (after the routed rows) and a per-token ordered sum writes
+  // every element of `out`, so nothing is zeroed first
+  float* det_rows = nullptr;
+  int32_t* det_inv = nullptr;
+  if (det) {
+    det_rows = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + ws_base);
+    det_inv = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(det_rows) +
+                                         det_rows_bytes(capacity, n));
+  }
+  const size_t zero_now = det ? 0 : zero_bytes;
 
   GemmArgs g;
   std::memset(&g, 0, sizeof(g));
@@ -312,10 +335,13 @@ w4a16_status w4a16_moe_indexed_gemm(int mode, const void* packed, int num_expert
     return W4A16_ERR_CUDA;
   // (n * 4 bytes per row is a multiple of 16 when n % 4 == 0; otherwise the
   // tail is cleared separately)
-  const size_t zero_vec_bytes = zero_bytes / 16 * 16;
-  if (zero_bytes != zero_vec_bytes &&
-      cudaMemsetAsync(static_cast<uint8_t*>(out) + zero_vec_bytes, 0, zero_bytes - zero_vec_bytes,
+  const size_t zero_vec_bytes = zero_now / 16 * 16;
+  if (zero_now != zero_vec_bytes &&
+      cudaMemsetAsync(static_cast<uint8_t*>(out) + zero_vec_bytes, 0, zero_now - zero_vec_bytes,
                       s) != cudaSuccess)
+    return W4A16_ERR_CUDA;
+  if (det && launch_det_inverse(sorted_ids, num_tokens_padded, capacity, static_cast<int>(numel),
+                                det_inv, sms, s) != cudaSuccess)
     return W4A16_ERR_CUDA;
   if (launch_permute_rows(a, k, a_div, static_cast<int>(numel), sorted_ids, num_tokens_padded,
                           capacity, permuted, out, zero_vec_bytes, sms, s) != cudaSuccess)
@@ -324,7 +350,9 @@ w4a16_status w4a16_moe_indexed_gemm(int mode, const void* packed, int num_expert
   g.gather_rows = 1;
   g.act_rows = capacity;
   g.family = kIndexed;
-  g.out_mode = mode == W4A16_DOWN ? kOutF32WeightedAdd : (glu ? kOutGluBf16 : kOutBf16);
+  g.out_mode = det                  ? kOutF32Rows
+               : mode == W4A16_DOWN ? kOutF32WeightedAdd
+               : (glu ? kOutGluBf16 : kOutBf16);
   g.sorted_ids = sorted_ids;
   g.expert_ids = expert_ids;
   g.num_tokens_padded = num_tokens_padded;
@@ -334,7 +362,7 @@ w4a16_status w4a16_moe_indexed_gemm(int mode, const void* packed, int num_expert
   g.o_div = mode == W4A16_DOWN ? topk : 1;
   g.topk_weights = topk_weights;
   g.block_m = bm;
-  g.out = out;
+  g.out = det ? static_cast<void*>(det_rows) : out;
   g.status = static_cast<int*>(workspace);
   fill_pipeline(pl, &g);
   g.raster_rows = 0;
@@ -342,7 +370,12 @@ w4a16_status w4a16_moe_indexed_gemm(int mode, const void* packed, int num_expert
   long long grid = plan->grid > 0 ? plan->grid : static_cast<long long>(sms) * plan->ctas_per_sm;
   const long long max_items = static_cast<long long>(capacity / bm) * g.n_tiles;
   grid = std::max<long long>(1, std::min(grid, max_items));
-  return cuda_status(launch_moe_gemm(g, static_cast<int>(grid), true, s));
+  if (launch_moe_gemm(g, static_cast<int>(grid), true, s) != cudaSuccess) return W4A16_ERR_CUDA;
+  if (det && launch_det_reduce(det_rows, det_inv, tokens, topk, n,
+                               (flags & W4A16_FLAG_ACCUMULATE) != 0, static_cast<float*>(out), sms,
+                               s) != cudaSuccess)
+    return W4A16_ERR_CUDA;
+  return W4A16_OK;
 }
 
 w4a16_status w4a16_moe_grouped_gemm(int kind, const void* packed, int num_experts, int n, int k,

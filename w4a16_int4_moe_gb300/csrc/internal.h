@@ -34,6 +34,12 @@ inline size_t permuted_bytes(long long rows, int k) {
   return static_cast<size_t>(rows) * permuted_row_elems(k) * 2;
 }
 
+// Weighted FP32 rows of the deterministic down pass, [capacity][n], rounded
+// up to 256 bytes (in the workspace after the routed rows).
+inline size_t det_rows_bytes(int capacity, int n) {
+  return (static_cast<size_t>(capacity) * n * 4 + 255) / 256 * 256;
+}
+
 inline int packed_tiles(int n) { return ceil_div(n, kTileRows); }
 inline int packed_ksteps(int k) { return ceil_div(k, kKStep); }
 inline size_t packed_expert_bytes(int n, int k) {
@@ -41,7 +47,9 @@ inline size_t packed_expert_bytes(int n, int k) {
 }
 
 enum Family { kIndexed = 0, kContiguous = 1, kMasked = 2 };
-enum OutMode { kOutBf16 = 0, kOutF32WeightedAdd = 1, kOutGluBf16 = 2 };
+// kOutF32Rows (the deterministic down pass): top-k weighted FP32 rows, each
+// at its routing position, for a separate ordered sum per token.
+enum OutMode { kOutBf16 = 0, kOutF32WeightedAdd = 1, kOutGluBf16 = 2, kOutF32Rows = 3 };
 
 // Source row (of the [n, k] weight matrix) of row `row` of packed tile `tile`.
 // W4A16_LAYOUT_KTILE64_GLU16 interleaves gate rows [0, n/2) and up rows
@@ -123,6 +131,15 @@ cudaError_t launch_permute_rows(const uint16_t* a, int k, int a_div, int numel,
                                 const int32_t* sorted_ids, const int32_t* num_tokens_padded,
                                 int capacity, uint16_t* dst, void* zero, size_t zero_bytes,
                                 int sms, cudaStream_t stream);
+
+// Deterministic down pass: inv[id] = routing position of flattened row id
+// (-1 when not routed here), then out[t] (+)= the top-k weighted rows of
+// token t added in ascending top-k slot order.
+cudaError_t launch_det_inverse(const int32_t* sorted_ids, const int32_t* num_tokens_padded,
+                               int capacity, int numel, int32_t* inv, int sms,
+                               cudaStream_t stream);
+cudaError_t launch_det_reduce(const float* rows, const int32_t* inv, int tokens, int topk, int n,
+                              bool accumulate, float* out, int sms, cudaStream_t stream);
 
 cudaError_t launch_topk_softmax(const void* logits, int bf16_logits, int tokens, int num_experts,
                                 int topk, int renormalize, int expert_offset, int num_local,

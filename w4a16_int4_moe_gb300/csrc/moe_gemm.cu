@@ -282,15 +282,24 @@ __device__ __forceinline__ ItemDesc decode_item(const GemmArgs& a, int it, int n
 
 // Row j of block `blk`: output row (-1 = not a real row) and the top-k
 // weight of the down pass.
+// kRows (the deterministic down pass): the output row is the routing
+// position itself.
+template <bool kRows>
 __device__ __forceinline__ void row_info(const GemmArgs& a, const ItemDesc& d, int j, int& dst,
                                          float& wt) {
   dst = -1;
   wt = 0.f;
   if (a.family == kIndexed) {
-    const int id = __ldg(a.sorted_ids + static_cast<long long>(d.blk) * a.block_m + j);
+    const long long pos = static_cast<long long>(d.blk) * a.block_m + j;
+    const int id = __ldg(a.sorted_ids + pos);
     if (id >= 0 && id < a.numel) {
-      dst = id / a.o_div;
-      wt = (a.out_mode == kOutF32WeightedAdd) ? __ldg(a.topk_weights + id) : 1.f;
+      if constexpr (kRows) {
+        dst = static_cast<int>(pos);
+        wt = __ldg(a.topk_weights + id);
+      } else {
+        dst = id / a.o_div;
+        wt = (a.out_mode == kOutF32WeightedAdd) ? __ldg(a.topk_weights + id) : 1.f;
+      }
     }
   } else if (a.family == kContiguous) {
     const int r = d.blk * a.block_m + j;
@@ -350,10 +359,11 @@ __device__ __forceinline__ void dequant_group(const uint4 q, uint32_t scale_bits
 // kGlu: the fused-activation epilogue (out_mode kOutGluBf16), kRaster: the
 // grouped item order, and kEarly: the epilogue that frees the accumulator
 // slot before its stores (blocks of 48 or 64 rows, whose accumulators fill
-// TMEM's single slot) are compiled into their own instantiations so that they
-// cannot change the register allocation or the instruction footprint of the
-// plain kernel.
-template <bool kGlu, bool kRaster, bool kEarly>
+// TMEM's single slot), and kRows: the deterministic down pass (out_mode
+// kOutF32Rows) are compiled into their own instantiations so that they cannot
+// change the register allocation or the instruction footprint of the plain
+// kernel.
+template <bool kGlu, bool kRaster, bool kEarly, bool kRows>
 __global__ void __launch_bounds__(kThreads, 1)
     w4a16_moe_gemm_kernel(const __grid_constant__ GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
@@ -596,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = lane; j < bm; j += 32) {
         int dd;
         float w;
-        row_info(args, d, j, dd, w);
+        row_info<kRows>(args, d, j, dd, w);
         idst[j] = dd;
         iwt[j] = w;
         if (dd >= 0) maxj = j;
@@ -844,7 +854,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int dr = idst[j];
                 if (dr < 0 || ng >= args.n) continue;
                 const float4 x = *reinterpret_cast<const float4*>(slab + jr * 32 + 4 * c4);
-                if (args.out_mode == kOutF32WeightedAdd) {
+                if constexpr (kRows) {
+                  // deterministic down pass: the weighted row at its routing position
+                  float* o =
+                      static_cast<float*>(args.out) + static_cast<long long>(dr) * args.n + ng;
+                  const float wt = iwt[j];
+                  if (vec4) {
+                    *reinterpret_cast<float4*>(o) =
+                        make_float4(wt * x.x, wt * x.y, wt * x.z, wt * x.w);
+                  } else {
+                    o[0] = wt * x.x;
+                    if (ng + 1 < args.n) o[1] = wt * x.y;
+                    if (ng + 2 < args.n) o[2] = wt * x.z;
+                    if (ng + 3 < args.n) o[3] = wt * x.w;
+                  }
+                } else if (args.out_mode == kOutF32WeightedAdd) {
                   float* o =
                       static_cast<float*>(args.out) + static_cast<long long>(dr) * args.n + ng;
                   const float wt = iwt[j];
@@ -954,7 +978,21 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int dr = idst[j];
               if (dr < 0 || ng >= args.n) continue;
               const float4 x = *reinterpret_cast<const float4*>(tile + jr * 32 + 4 * c4);
-              if (args.out_mode == kOutF32WeightedAdd) {
+              if constexpr (kRows) {
+                // deterministic down pass: the weighted row at its routing position
+                float* o =
+                    static_cast<float*>(args.out) + static_cast<long long>(dr) * args.n + ng;
+                const float wt = iwt[j];
+                if (vec4) {
+                  *reinterpret_cast<float4*>(o) =
+                      make_float4(wt * x.x, wt * x.y, wt * x.z, wt * x.w);
+                } else {
+                  o[0] = wt * x.x;
+                  if (ng + 1 < args.n) o[1] = wt * x.y;
+                  if (ng + 2 < args.n) o[2] = wt * x.z;
+                  if (ng + 3 < args.n) o[3] = wt * x.w;
+                }
+              } else if (args.out_mode == kOutF32WeightedAdd) {
                 float* o = static_cast<float*>(args.out) + static_cast<long long>(dr) * args.n + ng;
                 const float wt = iwt[j];
                 if (vec4) {
@@ -1107,14 +1145,18 @@ cudaError_t launch_moe_gemm(const GemmArgs& args, int grid, bool dependent, cuda
   size_t smem = gemm_smem_bytes(args.block_m, args.w_stages, args.b_stages);
   if (smem < 118 * 1024) smem = 118 * 1024;
   const bool glu = args.out_mode == kOutGluBf16;
+  const bool rows = args.out_mode == kOutF32Rows;
   // the whole-block staging tile exists for exactly these block sizes
   const bool early = epi_stage_rows(args.block_m) > 16;
-  auto kernel = glu ? (early ? w4a16_moe_gemm_kernel<true, false, true>
-                             : w4a16_moe_gemm_kernel<true, false, false>)
-                : args.raster_rows ? (early ? w4a16_moe_gemm_kernel<false, true, true>
-                                            : w4a16_moe_gemm_kernel<false, true, false>)
-                                   : (early ? w4a16_moe_gemm_kernel<false, false, true>
-                                            : w4a16_moe_gemm_kernel<false, false, false>);
+  auto kernel =
+      rows ? (early ? w4a16_moe_gemm_kernel<false, false, true, true>
+                    : w4a16_moe_gemm_kernel<false, false, false, true>)
+      : glu ? (early ? w4a16_moe_gemm_kernel<true, false, true, false>
+                     : w4a16_moe_gemm_kernel<true, false, false, false>)
+      : args.raster_rows ? (early ? w4a16_moe_gemm_kernel<false, true, true, false>
+                                  : w4a16_moe_gemm_kernel<false, true, false, false>)
+                         : (early ? w4a16_moe_gemm_kernel<false, false, true, false>
+                                  : w4a16_moe_gemm_kernel<false, false, false, false>);
   cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;

@@ -39,9 +39,13 @@ class W4A16MoE:
     """One MoE layer's expert pair on one GPU (gate_up [E, 2I, H], down [E, H, I])."""
 
     def __init__(self, gate_up: PackedExperts, down: PackedExperts, topk: int,
-                 max_tokens: int, tok_e_hint: float = 0.0, device=None):
+                 max_tokens: int, tok_e_hint: float = 0.0, device=None,
+                 deterministic: bool = False):
         """With gate_up packed as W4A16_LAYOUT_KTILE64_GLU16 the activation is
-        fused into the gate_up call (forward skips the separate pass)."""
+        fused into the gate_up call (forward skips the separate pass). With
+        deterministic=True the down pass adds each token's top-k rows in a
+        fixed order (W4A16_FLAG_DETERMINISTIC): the output bits do not depend
+        on the schedule."""
         assert gate_up.num_experts == down.num_experts
         assert gate_up.n == 2 * down.k and gate_up.k == down.n
         self.gate_up, self.down = gate_up, down
@@ -51,6 +55,7 @@ class W4A16MoE:
         self.device = device or gate_up.packed.device
         self.max_tokens = max_tokens
         self.tok_e_hint = tok_e_hint
+        self.deterministic = deterministic
         self._plan_for(max_tokens)
 
     def _plan_for(self, tokens: int):
@@ -74,8 +79,9 @@ class W4A16MoE:
         self.act_buf = torch.empty((numel, self.inter), dtype=torch.bfloat16, device=dev)
         # one workspace for both GEMMs (ordered on one stream): status words
         # and the routed rows of the wider activation (x, k = hidden)
-        self.workspace = ops.new_workspace(self.plan_gu, dev, self.capacity,
-                                           max(self.hidden, self.inter))
+        self.workspace = ops.new_workspace(
+            self.plan_gu, dev, self.capacity, max(self.hidden, self.inter),
+            det_n=self.hidden if self.deterministic else 0, det_numel=numel)
 
     def align(self, topk_ids: torch.Tensor, stream=None):
         return ops.w4a16_moe_align_block_size(
@@ -107,7 +113,8 @@ class W4A16MoE:
         return ops.w4a16_moe_indexed_gemm(
             ops.W4A16_DOWN, self.down.packed, self.num_experts, self.down.n, self.down.k,
             self.act_buf[:numel], tokens, self.topk, self.sorted_ids, self.expert_ids, self.ntp,
-            self.plan_dn, self.workspace, topk_weights=topk_weights, out=out, stream=stream)
+            self.plan_dn, self.workspace, topk_weights=topk_weights, out=out,
+            flags=ops.W4A16_FLAG_DETERMINISTIC if self.deterministic else 0, stream=stream)
 
     def route(self, router_logits: torch.Tensor, expert_offset: int = 0,
               renormalize: bool = True, stream=None):

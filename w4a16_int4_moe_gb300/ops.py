@@ -31,6 +31,7 @@ W4A16_GROUPED_CONTIGUOUS = 0
 W4A16_GROUPED_MASKED = 1
 W4A16_FLAG_VALIDATE_ROUTING = 1
 W4A16_FLAG_ACCUMULATE = 2
+W4A16_FLAG_DETERMINISTIC = 8
 W4A16_LAYOUT_KTILE64 = 0
 W4A16_LAYOUT_KTILE64_GLU16 = 1
 W4A16_DTYPE_F32 = 0
@@ -43,7 +44,7 @@ EXPORTED = (
     "w4a16_moe_align_block_size", "w4a16_prepack_size", "w4a16_prepack", "w4a16_unpack",
     "w4a16_workspace_size", "w4a16_moe_indexed_gemm", "w4a16_moe_grouped_gemm",
     "w4a16_silu_and_mul", "w4a16_read_device_status", "w4a16_moe_indexed_gemm_noalloc",
-    "w4a16_topk_softmax",
+    "w4a16_topk_softmax", "w4a16_deterministic_bytes",
 )
 
 
@@ -92,6 +93,7 @@ def load_library(path: Optional[str] = None):
         "w4a16_prepack": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _Z, _P]),
         "w4a16_unpack": (_I, [_P, _I, _I, _I, _I, _P, _P, _P]),
         "w4a16_workspace_size": (_Z, [ctypes.POINTER(Plan), _I, _I]),
+        "w4a16_deterministic_bytes": (_Z, [_I, _I, _I]),
         "w4a16_moe_indexed_gemm": (_I, [_I, _P, _I, _I, _I, _P, _I, _I, _P, _P, _P, _I, _P, _P,
                                         _I, ctypes.POINTER(Plan), _P, _Z, _P]),
         "w4a16_moe_grouped_gemm": (_I, [_I, _P, _I, _I, _I, _P, _I, _P, _I, _P, _I,
@@ -205,8 +207,19 @@ def w4a16_unpack(packed: torch.Tensor, num_experts: int, n: int, k: int,
     return q, s
 
 
-def new_workspace(plan: Plan, device, rows: int = 0, k: int = 0) -> torch.Tensor:
-    return torch.zeros(w4a16_workspace_size(plan, rows, k), dtype=torch.uint8, device=device)
+def w4a16_deterministic_bytes(capacity: int, n: int, numel: int) -> int:
+    """Extra workspace of a W4A16_FLAG_DETERMINISTIC down call."""
+    return int(load_library().w4a16_deterministic_bytes(capacity, n, numel))
+
+
+def new_workspace(plan: Plan, device, rows: int = 0, k: int = 0, det_n: int = 0,
+                  det_numel: int = 0) -> torch.Tensor:
+    """det_n, det_numel: room for a deterministic down pass of width det_n
+    over det_numel flattened rows (0: none)."""
+    size = w4a16_workspace_size(plan, rows, k)
+    if det_n > 0:
+        size += w4a16_deterministic_bytes(rows, det_n, det_numel)
+    return torch.zeros(size, dtype=torch.uint8, device=device)
 
 
 def w4a16_moe_indexed_gemm(mode: int, packed: torch.Tensor, num_experts: int, n: int, k: int,
