@@ -17,8 +17,9 @@
 //   tcgen05.mma kind::f16, M = 128 weight rows, N = the block's tokens
 //     (rounded to 16, chosen per block at run time), K = 16 per instruction,
 //     FP32 accumulators in TMEM (D)
-//   epilogue warps: tcgen05.ld --> BF16 row stores, or the top-k weighted
-//     FP32 scatter-add of the down pass.
+//   epilogue warps: tcgen05.ld --> BF16 row stores, the top-k weighted FP32
+//     scatter-add of the down pass, or (deterministic down pass) the
+//     weighted FP32 rows at their routing positions.
 //
 // Writing the dequantised weights to TMEM instead of shared memory keeps the
 // shared-memory port free for the token operand: at decode (N = 16) a
@@ -28,8 +29,9 @@
 // The pipeline moves in stages of two 64-k steps (9216 bytes of packed
 // weights): every handshake is paid once per stage, four dequant warpgroups
 // work on four consecutive stages, and up to four MMA issuers split the k
-// steps (each tcgen05.mma holds its issuing thread for tens of cycles, so at
-// small N the issue rate, not the tensor core, sets the pace). Each issuer
+// steps (one thread issues a tcgen05.mma only every 100-125 cycles whatever N
+// is, measured on GB300, so at small N the issue rate, not the tensor core,
+// sets the pace). Each issuer
 // owns a partial FP32 accumulator; the epilogue adds them in a fixed order,
 // so results do not depend on the schedule.
 //
