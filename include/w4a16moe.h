@@ -338,9 +338,11 @@ w4a16_status w4a16_read_device_status(void* workspace, int* detail, void* stream
  *   word on `stream` first, so calls that overlap on the GPU (different
  *   streams without ordering) race on it: order them, or use
  *   w4a16_moe_indexed_gemm with one workspace per stream.
- * - flags: those of w4a16_moe_indexed_gemm, plus W4A16_FLAG_SYNC_STATUS to
- *   synchronise `stream` after the launch and return W4A16_ERR_TIMEOUT if a
- *   device-side wait gave up (without it such a failure is not reported).
+ * - flags: those of w4a16_moe_indexed_gemm except W4A16_FLAG_DETERMINISTIC
+ *   (refused with W4A16_ERR_INVALID_ARG: its row buffer needs a workspace
+ *   sized by the caller), plus W4A16_FLAG_SYNC_STATUS to synchronise
+ *   `stream` after the launch and return W4A16_ERR_TIMEOUT if a device-side
+ *   wait gave up (without it such a failure is not reported).
  */
 enum { W4A16_FLAG_SYNC_STATUS = 4 };
 w4a16_status w4a16_moe_indexed_gemm_noalloc(int mode, const void* packed, int num_experts, int n,

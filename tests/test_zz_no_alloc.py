@@ -66,3 +66,8 @@ def test_noalloc_rejects_unknown_flags(cuda_dev, lib):
     assert lib.w4a16_moe_indexed_gemm_noalloc(0, fake, 8, 1024, 512, fake, 64, 2, fake, fake,
                                               fake, 256, None, fake, 64, ctypes.byref(plan),
                                               None) == ops.W4A16_ERR_INVALID_ARG
+    # so is the deterministic down pass, whose row buffer needs a sized workspace
+    assert lib.w4a16_moe_indexed_gemm_noalloc(ops.W4A16_DOWN, fake, 8, 1024, 512, fake, 64, 2,
+                                              fake, fake, fake, 256, fake, fake,
+                                              ops.W4A16_FLAG_DETERMINISTIC, ctypes.byref(plan),
+                                              None) == ops.W4A16_ERR_INVALID_ARG
