@@ -202,3 +202,17 @@ def test_product_path_has_no_cpu_fallback():
             ops.load_library("/nonexistent/libw4a16moe.so")
     finally:
         ops._lib = saved
+
+
+def test_header_is_plain_c():
+    # the boundary header compiles as C (and C++) on its own
+    import shutil
+    import subprocess
+    header = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                          "include", "w4a16moe.h")
+    for cc, lang in (("gcc", "c"), ("g++", "c++")):
+        if shutil.which(cc) is None:
+            pytest.skip(f"{cc} not installed")
+        r = subprocess.run([cc, "-fsyntax-only", "-Wall", "-Werror", "-x", lang, header],
+                           capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr
