@@ -6,16 +6,27 @@ Chord 内核 …", section "六个场景的逐层测量与限定条件"): micros
 layer, lower is better, plus achieved HBM GB/s and TFLOP/s against the
 measured roofline.
 
-One step = one pass of the whole path over one batch: routing alignment,
-gate_up, silu_and_mul, down. The reported value is the mean over the timed
-steps of the CUDA-event time of gate_up plus down, with inputs already
-resident in HBM; L2 is flushed (a 256 MiB write) before every step and the
-weight stream (1.19 GB at the EP8 decode shard) is larger than L2 anyway.
+One step = one decode step through `--layers` MoE layers of the headline
+shard shape (EP8 decode by default): per layer routing alignment, gate_up,
+silu_and_mul and down over the same batch. Before every layer L2 is flushed
+(a 256 MiB write), so each layer streams its 1.19 GB of weights from HBM as a
+distinct layer would. The reported value is the mean over all timed layers
+of the CUDA-event time of gate_up plus down, with inputs already resident in
+HBM.
 
-`--impl reference` times the float64 CPU oracle on the host cores instead,
-on a bounded sample of the same workload scaled to a whole layer.
+The same run then measures every other configuration of the shard shapes
+(TP8 T=16/64/256, EP8 prefill, grouped contiguous 128 and 1024 rows per
+expert, grouped masked with a 32-row budget) and reports them in the
+`configs` object of the JSON line, each with its roofline fraction against
+the bound that applies (HBM for the weight-bound shapes, BF16 tensor peak for
+the compute-bound ones).
+
+`--impl reference` times the float64 CPU oracle on the host cores instead:
+each step one whole layer of the same workload (every active expert, all its
+routed rows).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                       [--layers L] [--no-configs]
                        [--workload ep8_decode|ep8_decode_e12|tp8_16|tp8_64|tp8_256|ep8_prefill|tiny
                                    |grouped_contig_{128,256,512,1024}|grouped_masked_32]
 """
@@ -41,9 +52,15 @@ METRIC = "MoE W4A16 gate_up+down µs/layer; achieved HBM GB/s or TFLOPS vs roofl
 UNIT = "us/layer"
 L2_FLUSH_BYTES = 256 << 20
 PROFILES = os.path.join(ROOT, "profiles")
+# nominal GB300 figures, reported beside the measured-peak fractions
+NOMINAL_HBM_GBS = 8000.0
+NOMINAL_BF16_TFLOPS = 2250.0
+WEIGHT_BYTES = 0.5 + 2.0 / 32  # uint4 code + BF16 scale per 32 elements
+CONFIG_SET = ("tp8_16", "tp8_64", "tp8_256", "ep8_prefill", "grouped_contig_128",
+              "grouped_contig_1024", "grouped_masked_32")
 
 
-def make_workload(name):
+def make_workload(name, weights=True):
     from w4a16_int4_moe_gb300 import workloads as wl
     if name == "ep8_decode":
         return wl.ep8_decode()
@@ -52,9 +69,9 @@ def make_workload(name):
         # that detailed profiler captures run on
         return wl.ep8_decode(tokens=144, local_experts=12)
     if name.startswith("tp8_"):
-        return wl.tp8(int(name.split("_")[1]))
+        return wl.tp8(int(name.split("_")[1]), weights=weights)
     if name == "ep8_prefill":
-        return wl.ep8_prefill()
+        return wl.ep8_prefill(weights=weights)
     if name == "tiny":
         return wl.tiny()
     raise SystemExit(f"unknown workload {name}")
@@ -70,13 +87,25 @@ def algorithmic_work(p):
     rows = int(local.sum())
     tokens_used = int(np.any((p.topk_ids >= 0) & (p.topk_ids < p.num_experts), axis=1).sum())
     h, i2, i = p.hidden, 2 * p.inter, p.inter
-    wb = 0.5 + 2.0 / 32
-    gu_bytes = active * i2 * h * wb + tokens_used * h * 2 + rows * i2 * 2
-    dn_bytes = active * h * i * wb + rows * i * 2 + p.tokens * h * 4
+    gu_bytes = active * i2 * h * WEIGHT_BYTES + tokens_used * h * 2 + rows * i2 * 2
+    dn_bytes = active * h * i * WEIGHT_BYTES + rows * i * 2 + p.tokens * h * 4
     return {
         "gate_up": {"bytes": gu_bytes, "flops": 2.0 * rows * i2 * h},
         "down": {"bytes": dn_bytes, "flops": 2.0 * rows * h * i},
         "active_experts": active, "rows": rows,
+    }
+
+
+def workload_config(p, world):
+    """The `config` object of both arms (identical for the same workload)."""
+    flat = p.topk_ids.reshape(-1)
+    local = (flat >= 0) & (flat < p.num_experts)
+    return {
+        "workload": p.name, "tokens": p.tokens, "hidden": p.hidden, "inter": p.inter,
+        "local_experts": p.num_experts, "topk": p.topk, "routed_rows": int(local.sum()),
+        "active_experts": int(np.unique(flat[local]).size),
+        "l2": "flushed before every layer (256 MiB write); the weight stream exceeds L2",
+        "parallelism": f"replicas x{world}",
     }
 
 
@@ -186,14 +215,15 @@ class ClockSampler:
 
 
 def cpu_oracle_sample(p, n_experts_sample=None):
-    """Time the float64 oracle (as it stands) on a bounded sample: all routed
-    rows of a subset of experts through gate_up -> act -> down; scale to a
-    whole layer by the fraction of active experts sampled."""
+    """Time the float64 oracle (as it stands) on all routed rows of
+    `n_experts_sample` active experts (default: every active expert, i.e. one
+    whole layer) through gate_up -> act -> down; a partial sample is scaled
+    to a whole layer by the fraction of active experts sampled."""
     import oracle
     flat = p.topk_ids.reshape(-1)
     local = (flat >= 0) & (flat < p.num_experts)
     active = np.unique(flat[local])
-    if n_experts_sample is None:
+    if n_experts_sample is None or n_experts_sample >= active.size:
         n_experts_sample = active.size
     rng = np.random.default_rng(0)
     chosen = np.sort(rng.choice(active, size=n_experts_sample, replace=False))
@@ -210,10 +240,12 @@ def cpu_oracle_sample(p, n_experts_sample=None):
     oracle.indexed_down(a_bits, sub_ids, w_sub, p.q_dn, p.s_dn)
     dt = time.perf_counter() - t0
     scale = active.size / n_experts_sample
+    whole = n_experts_sample == active.size
     return {"value": dt * scale * 1e6, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"{n_experts_sample} of {active.size} active experts (all their routed rows, "
-                      f"{int(rows.sum())} tokens; gate_up+silu+down, float64 numpy), {dt:.2f} s, "
-                      f"scaled x{scale:.2f}"}
+            "sample": (f"the whole layer: all {active.size} active experts" if whole else
+                       f"{n_experts_sample} of {active.size} active experts, scaled x{scale:.2f}")
+                      + f" (all their routed rows, {int(rows.sum())} tokens; gate_up+silu+down, "
+                        f"float64 numpy), {dt:.2f} s"}
 
 
 def dist_setup(n_gpus):
@@ -243,23 +275,252 @@ def run_reference(args):
     p = make_workload(args.workload)
     for _ in range(args.warmup):
         cpu_oracle_sample(p, n_experts_sample=1)
-    vals, samples = [], None
+    vals, rec = [], None
+    t0 = time.perf_counter()
     for _ in range(args.steps):
         rec = cpu_oracle_sample(p, n_experts_sample=args.ref_experts)
         vals.append(rec["value"])
-        samples = rec
+    wall = time.perf_counter() - t0
     value = statistics.mean(vals)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": value / 1e3, "higher_is_better": False, "scaling": "weak",
+        "ms_per_step": wall / args.steps * 1e3, "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": p.name},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": samples["cores"],
-                         "kind": "oracle", "sample": samples["sample"]},
+        "config": workload_config(p, world),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": rec["cores"],
+                         "kind": "oracle", "sample": rec["sample"]},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
+
+
+def to_device(a, device):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+
+def device_weights(num_experts, n, k, seed, device):
+    """Seeded synthetic checkpoint tensors drawn on the device (same recipe
+    as the workloads: uniform codes, |N(0,1)| * 0.02 BF16 scales)."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    q = torch.randint(0, 256, (num_experts, n, k // 2), dtype=torch.uint8, device=device,
+                      generator=g)
+    s = (torch.randn((num_experts, n, k // 32), device=device, generator=g).abs() * 0.02)
+    return q, s.to(torch.bfloat16).view(torch.int16)
+
+
+def time_indexed_layer(layer, x, tokens, ids, w, out, flush, steps, warmup, layers=1):
+    """gate_up and down CUDA-event times (µs) of `steps` steps of `layers`
+    layers each, L2 flushed before every layer. Returns the per-layer lists
+    and the wall time of the timed steps."""
+    import torch
+    stream = torch.cuda.current_stream()
+
+    def one(ev=None):
+        flush.zero_()
+        layer.align(ids)
+        if ev is not None:
+            ev[0].record(stream)
+        layer.gate_up_gemm(x, tokens)
+        if ev is not None:
+            ev[1].record(stream)
+        layer.activation(tokens)
+        if ev is not None:
+            ev[2].record(stream)
+        layer.down_gemm(tokens, w, out)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(warmup * layers):
+        one()
+    torch.cuda.synchronize()
+    n = steps * layers
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(n):
+        one(events[i])
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    gu = [e[0].elapsed_time(e[1]) * 1e3 for e in events]
+    dn = [e[2].elapsed_time(e[3]) * 1e3 for e in events]
+    return gu, dn, wall
+
+
+def roofline_entry(bound, kernel, achieved, peak, nominal, peak_src, extra=None):
+    unit = "GB/s" if bound == "hbm" else "TFLOP/s"
+    d = {"bound": bound, "kernel": kernel, "achieved": achieved, "peak": peak, "unit": unit,
+         "frac": achieved / peak, "peak_source": peak_src,
+         "nominal_peak": nominal, "frac_of_nominal": achieved / nominal}
+    if extra:
+        d.update(extra)
+    return d
+
+
+def indexed_config(name, packed, device, flush, steps, warmup, peaks):
+    """One indexed configuration (TP8 or EP8 prefill) with the given packed
+    weights {(n, k): PackedExperts}: gate_up and down µs, roofline."""
+    import torch
+    from w4a16_int4_moe_gb300 import moe as moe_mod
+    p = make_workload(name, weights=False)
+    work = algorithmic_work(p)
+    gu = packed[(2 * p.inter, p.hidden)]
+    dn = packed[(p.hidden, p.inter)]
+    layer = moe_mod.W4A16MoE(gu, dn, p.topk, p.tokens, tok_e_hint=p.tok_e_hint(), device=device)
+    x = to_device(p.x.view(np.int16), device).view(torch.bfloat16)
+    ids = to_device(p.topk_ids, device)
+    w = to_device(p.topk_weights, device)
+    out = torch.empty((p.tokens, p.hidden), dtype=torch.float32, device=device)
+    gu_us, dn_us, _ = time_indexed_layer(layer, x, p.tokens, ids, w, out, flush, steps, warmup)
+    torch.cuda.synchronize()
+    from w4a16_int4_moe_gb300 import ops
+    st, word = ops.w4a16_read_device_status(layer.workspace)
+    if st != ops.W4A16_OK:
+        raise SystemExit(f"device status {word:#x} in configuration {name}")
+    g, d_ = statistics.mean(gu_us), statistics.mean(dn_us)
+    hbm, tf, src = peaks
+    tensor = name == "ep8_prefill"
+    layer_us = g + d_
+    total_b = work["gate_up"]["bytes"] + work["down"]["bytes"]
+    total_f = work["gate_up"]["flops"] + work["down"]["flops"]
+    if tensor:
+        roof = roofline_entry("tensor", "w4a16_moe_gemm_kernel (gate_up + down)",
+                              total_f / (layer_us * 1e-6) / 1e12, tf, NOMINAL_BF16_TFLOPS,
+                              f"{src} bf16_tflops")
+    else:
+        roof = roofline_entry("hbm", "w4a16_moe_gemm_kernel (gate_up + down)",
+                              total_b / (layer_us * 1e-6) / 1e9, hbm, NOMINAL_HBM_GBS,
+                              f"{src} hbm_gbs", {"algorithmic_bytes": total_b})
+    return {"workload": p.name, "layer_us": layer_us, "gate_up_us": g, "down_us": d_,
+            "steps": steps, "block_m": layer.block_m, "routed_rows": work["rows"],
+            "active_experts": work["active_experts"],
+            "gate_up_gbs": work["gate_up"]["bytes"] / (g * 1e-6) / 1e9,
+            "tflops": total_f / (layer_us * 1e-6) / 1e12, "roofline": roof}
+
+
+def grouped_inputs(name, device, packed):
+    """(calls, label, rows, active experts) of a grouped workload on the EP8
+    shard: the gate_up-shaped then the down-shaped grouped GEMM over the same
+    per-expert rows, activations drawn on the device."""
+    import torch
+    from w4a16_int4_moe_gb300 import ops
+    from w4a16_int4_moe_gb300 import workloads as wl
+    g = torch.Generator(device=device)
+    g.manual_seed(3)
+    calls = []
+    if name.startswith("grouped_contig_"):
+        m = int(name.split("_")[-1])
+        lay_np = wl.contiguous_layout(m, 48)
+        rows = int((lay_np >= 0).sum())
+        active = 48
+        label = f"grouped_contiguous_E48_m{m}_H7168_I2048"
+        kind = ops.W4A16_GROUPED_CONTIGUOUS
+        for (n, k) in ((4096, 7168), (7168, 2048)):
+            a = torch.randn((lay_np.size, k), device=device, generator=g).to(torch.bfloat16)
+            out = torch.empty((lay_np.size, n), dtype=torch.bfloat16, device=device)
+            calls.append((kind, packed[(n, k)], n, k, a, lay_np.size, to_device(lay_np, device),
+                          m, out))
+    elif name == "grouped_masked_32":
+        counts = wl.masked_counts(48, 32, seed=1)
+        rows = int(counts.sum())
+        active = int((counts > 0).sum())
+        label = "grouped_masked_E48_budget32_H7168_I2048"
+        kind = ops.W4A16_GROUPED_MASKED
+        for (n, k) in ((4096, 7168), (7168, 2048)):
+            a = torch.randn((48, 32, k), device=device, generator=g).to(torch.bfloat16)
+            out = torch.empty((48, 32, n), dtype=torch.bfloat16, device=device)
+            calls.append((kind, packed[(n, k)], n, k, a, 32, to_device(counts, device), 16, out))
+    else:
+        raise SystemExit(f"unknown workload {name}")
+    return calls, label, rows, active
+
+
+def grouped_config(name, packed, device, flush, steps, warmup, peaks):
+    """One step = the grouped gate_up GEMM then the grouped down GEMM (the
+    activation between them untimed), L2 flushed before each step."""
+    import torch
+    from w4a16_int4_moe_gb300 import ops
+    calls, label, rows, active = grouped_inputs(name, device, packed)
+    ws = torch.zeros(256, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream()
+
+    def run(c):
+        kind, pk, n, k, a, m, lay, exp_m, out = c
+        ops.w4a16_moe_grouped_gemm(kind, pk.packed, 48, n, k, a, m, lay, ws, expected_m=exp_m,
+                                   out=out)
+
+    for _ in range(warmup):
+        flush.zero_()
+        run(calls[0])
+        run(calls[1])
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        run(calls[0])
+        ev[i][1].record(stream)
+        run(calls[1])
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    st, word = ops.w4a16_read_device_status(ws)
+    if st != ops.W4A16_OK:
+        raise SystemExit(f"device status {word:#x} in configuration {name}")
+    gu_us = statistics.mean(e[0].elapsed_time(e[1]) * 1e3 for e in ev)
+    dn_us = statistics.mean(e[1].elapsed_time(e[2]) * 1e3 for e in ev)
+    gu_bytes = active * 4096 * 7168 * WEIGHT_BYTES + rows * 7168 * 2 + rows * 4096 * 2
+    dn_bytes = active * 7168 * 2048 * WEIGHT_BYTES + rows * 2048 * 2 + rows * 7168 * 2
+    flops = 2.0 * rows * 4096 * 7168 + 2.0 * rows * 7168 * 2048
+    layer_us = gu_us + dn_us
+    hbm, tf, src = peaks
+    if name.startswith("grouped_contig_"):
+        roof = roofline_entry("tensor", "w4a16_moe_gemm_kernel (grouped gate_up + down)",
+                              flops / (layer_us * 1e-6) / 1e12, tf, NOMINAL_BF16_TFLOPS,
+                              f"{src} bf16_tflops")
+    else:
+        roof = roofline_entry("hbm", "w4a16_moe_gemm_kernel (grouped gate_up + down)",
+                              (gu_bytes + dn_bytes) / (layer_us * 1e-6) / 1e9, hbm,
+                              NOMINAL_HBM_GBS, f"{src} hbm_gbs",
+                              {"algorithmic_bytes": gu_bytes + dn_bytes})
+    return {"workload": label, "layer_us": layer_us, "gate_up_us": gu_us, "down_us": dn_us,
+            "steps": steps, "valid_rows": rows, "tflops": flops / (layer_us * 1e-6) / 1e12,
+            "wall_s": wall, "roofline": roof}
+
+
+def run_configs(args, packed_ep8, device, flush, peaks):
+    """The `configs` block: every other configuration, measured in this run."""
+    import torch
+    from w4a16_int4_moe_gb300 import moe as moe_mod
+    steps = max(3, min(args.steps, 20))
+    warmup = max(3, min(args.warmup, 5))
+    res = {}
+    packed = dict(packed_ep8)
+    tp8_packed = None
+    for name in CONFIG_SET:
+        t0 = time.perf_counter()
+        if name.startswith("tp8_"):
+            if tp8_packed is None:
+                q, s = device_weights(384, 512, 7168, 11, device)
+                gu = moe_mod.PackedExperts.from_checkpoint(q, s)
+                del q, s
+                q, s = device_weights(384, 7168, 256, 12, device)
+                dn = moe_mod.PackedExperts.from_checkpoint(q, s)
+                del q, s
+                tp8_packed = {(512, 7168): gu, (7168, 256): dn}
+            r = indexed_config(name, tp8_packed, device, flush, steps, warmup, peaks)
+        elif name == "ep8_prefill":
+            r = indexed_config(name, packed, device, flush, steps, warmup, peaks)
+        else:
+            r = grouped_config(name, packed, device, flush, steps, warmup, peaks)
+        r["setup_and_run_s"] = time.perf_counter() - t0
+        res[name] = r
+        torch.cuda.empty_cache()
+    return res
 
 
 def run_ours(args):
@@ -276,77 +537,49 @@ def run_ours(args):
     p = make_workload(args.workload)
     work = algorithmic_work(p)
 
-    def to_dev(a):
-        return torch.from_numpy(np.ascontiguousarray(a)).to(device)
-
-    gu = moe_mod.PackedExperts.from_checkpoint(to_dev(p.q_gu), to_dev(p.s_gu.view(np.int16)))
-    dn = moe_mod.PackedExperts.from_checkpoint(to_dev(p.q_dn), to_dev(p.s_dn.view(np.int16)))
+    gu = moe_mod.PackedExperts.from_checkpoint(to_device(p.q_gu, device),
+                                               to_device(p.s_gu.view(np.int16), device))
+    dn = moe_mod.PackedExperts.from_checkpoint(to_device(p.q_dn, device),
+                                               to_device(p.s_dn.view(np.int16), device))
     layer = moe_mod.W4A16MoE(gu, dn, p.topk, p.tokens, tok_e_hint=p.tok_e_hint(), device=device)
-    x = to_dev(p.x.view(np.int16)).view(torch.bfloat16)
-    ids = to_dev(p.topk_ids)
-    w = to_dev(p.topk_weights)
+    x = to_device(p.x.view(np.int16), device).view(torch.bfloat16)
+    ids = to_device(p.topk_ids, device)
+    w = to_device(p.topk_weights, device)
     out = torch.empty((p.tokens, p.hidden), dtype=torch.float32, device=device)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream()
-
-    def step(ev=None):
-        flush.zero_()
-        layer.align(ids)
-        if ev is not None:
-            ev[0].record(stream)
-        layer.gate_up_gemm(x, p.tokens)
-        if ev is not None:
-            ev[1].record(stream)
-        layer.activation(p.tokens)
-        if ev is not None:
-            ev[2].record(stream)
-        layer.down_gemm(p.tokens, w, out)
-        if ev is not None:
-            ev[3].record(stream)
+    L = max(1, args.layers)
 
     clocks = ClockSampler()
     clocks.start()
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    st, word = ops.w4a16_read_device_status(layer.workspace)
-    if st != ops.W4A16_OK:
-        raise SystemExit(f"device status {word:#x} after warm-up")
-
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     if dist is not None:
         dist.barrier()
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for i in range(args.steps):
-        step(events[i])
-    torch.cuda.synchronize()
-    wall = time.perf_counter() - t0
+    gu_us, dn_us, wall = time_indexed_layer(layer, x, p.tokens, ids, w, out, flush, args.steps,
+                                            args.warmup, layers=L)
     t_end_wall = time.time()
     clocks.mark(t_end_wall - wall, t_end_wall)
     if dist is not None:
         dist.barrier()
     clk = clocks.stop()
-    gu_us = [events[i][0].elapsed_time(events[i][1]) * 1e3 for i in range(args.steps)]
-    dn_us = [events[i][2].elapsed_time(events[i][3]) * 1e3 for i in range(args.steps)]
     st, word = ops.w4a16_read_device_status(layer.workspace)
     if st != ops.W4A16_OK:
         raise SystemExit(f"device status {word:#x} after the timed steps")
     layer_us = statistics.mean(a + b for a, b in zip(gu_us, dn_us))
     layer_us = reduce_max(layer_us, dist)
     wall = reduce_max(wall, dist)
-    value = layer_us / world   # replicas: world layers per step
+    value = layer_us / world   # replicas: world layers per layer time
 
     # ---- the layer with the activation fused into gate_up (reported
     # beside the metric; the metric itself keeps the activation untimed) ----
     fused = None
+    layer_f = None
     if not args.no_fused:
         gu_glu = moe_mod.PackedExperts.from_checkpoint(
-            to_dev(p.q_gu), to_dev(p.s_gu.view(np.int16)),
+            to_device(p.q_gu, device), to_device(p.s_gu.view(np.int16), device),
             layout=ops.W4A16_LAYOUT_KTILE64_GLU16)
         layer_f = moe_mod.W4A16MoE(gu_glu, dn, p.topk, p.tokens, tok_e_hint=p.tok_e_hint(),
                                    device=device)
-        nf = max(20, args.steps // 4)
+        nf = max(20, args.steps)
         ev_f = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(nf)]
         for i in range(args.warmup + nf):
             e = ev_f[i - args.warmup] if i >= args.warmup else None
@@ -384,7 +617,7 @@ def run_ours(args):
 
     # ---- end to end through the public call, host buffers: the layer a user
     # builds, with the activation fused into gate_up when measured above ----
-    e2e_layer = layer_f if fused is not None else layer
+    e2e_layer = layer_f if layer_f is not None else layer
     x_h = torch.from_numpy(p.x.view(np.int16)).view(torch.bfloat16).pin_memory()
     ids_h = torch.from_numpy(p.topk_ids).pin_memory()
     w_h = torch.from_numpy(p.topk_weights).pin_memory()
@@ -403,7 +636,7 @@ def run_ours(args):
         e2e_step()
     torch.cuda.synchronize()
     e2e_times = []
-    for _ in range(args.steps):
+    for _ in range(max(20, args.steps)):
         flush.zero_()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
@@ -416,15 +649,22 @@ def run_ours(args):
     h2d = p.x.nbytes + p.topk_ids.nbytes + p.topk_weights.nbytes
     d2h = p.tokens * p.hidden * 4
 
+    peaks = measured_peaks()
+    configs = None
+    if not args.no_configs and rank == 0 and args.workload == "ep8_decode":
+        configs = run_configs(args, {(2 * p.inter, p.hidden): gu, (p.hidden, p.inter): dn},
+                              device, flush, peaks)
+
     if rank != 0:
         return
-    hbm, tflops_peak, peak_src = measured_peaks()
+    hbm, tflops_peak, peak_src = peaks
     gu_mean = statistics.mean(gu_us)
     dn_mean = statistics.mean(dn_us)
     gu_gbs = work["gate_up"]["bytes"] / (gu_mean * 1e-6) / 1e9
     dn_gbs = work["down"]["bytes"] / (dn_mean * 1e-6) / 1e9
     total_bytes = work["gate_up"]["bytes"] + work["down"]["bytes"]
     total_flops = work["gate_up"]["flops"] + work["down"]["flops"]
+    layer_gbs = total_bytes / (layer_us * 1e-6) / 1e9
     traffic = traffic_record(os.path.join(ROOT, "w4a16_int4_moe_gb300", "csrc", "moe_gemm.cu"),
                              args.workload)
     line = {
@@ -432,143 +672,67 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": wall / args.steps * 1e3,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; random uint4 weights, N(0,1) activations)",
-        "config": {
-            "workload": p.name, "tokens": p.tokens, "hidden": p.hidden, "inter": p.inter,
-            "local_experts": p.num_experts, "topk": p.topk, "routed_rows": work["rows"],
-            "active_experts": work["active_experts"], "block_m": layer.block_m,
-            "l2": "flushed before every step (256 MiB write); the weight stream exceeds L2",
-            "parallelism": f"replicas x{world}",
-        },
+        "config": workload_config(p, world),
+        "layers_per_step": L,
+        "plan": {"block_m": layer.block_m, "gate_up": layer.plan_gu.as_dict(),
+                 "down": layer.plan_dn.as_dict()},
         "gate_up_us": gu_mean, "down_us": dn_mean,
-        "achieved": {"hbm_gbs": total_bytes / (layer_us * 1e-6) / 1e9,
-                     "tflops": total_flops / (layer_us * 1e-6) / 1e12,
+        "achieved": {"hbm_gbs": layer_gbs, "tflops": total_flops / (layer_us * 1e-6) / 1e12,
                      "gate_up_gbs": gu_gbs, "down_gbs": dn_gbs},
-        "roofline": {
-            "bound": "hbm", "kernel": "w4a16_moe_gemm_kernel (gate_up)",
-            "achieved": gu_gbs, "peak": hbm, "unit": "GB/s", "frac": gu_gbs / hbm,
-            "peak_source": f"{peak_src} hbm_gbs",
-            "traffic": None if traffic is None else traffic["dram_bytes_per_launch"],
-            "algorithmic_bytes": work["gate_up"]["bytes"],
-        },
-        "gpu_launches": 6 * args.steps,  # align, permute + gate_up, silu, permute + down
+        "roofline": roofline_entry(
+            "hbm", "w4a16_moe_gemm_kernel (gate_up)", gu_gbs, hbm, NOMINAL_HBM_GBS,
+            f"{peak_src} hbm_gbs",
+            {"traffic": None if traffic is None else traffic["dram_bytes_per_launch"],
+             "algorithmic_bytes": work["gate_up"]["bytes"]}),
+        "layer_roofline": roofline_entry(
+            "hbm", "w4a16_moe_gemm_kernel (gate_up + down)", layer_gbs, hbm, NOMINAL_HBM_GBS,
+            f"{peak_src} hbm_gbs", {"algorithmic_bytes": total_bytes}),
+        # per layer: align, permute + gate_up, silu, permute + down
+        "gpu_launches": 6 * L * args.steps,
         "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "call": "W4A16MoE.forward (align, gate_up with fused activation, down)"
-                        if fused is not None else "W4A16MoE.forward (align, gate_up, act, down)"},
+                        if layer_f is not None else "W4A16MoE.forward (align, gate_up, act, down)"},
         "clocks": clk,
         "fused_activation": fused,
+        "configs": configs,
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_oracle_sample(p)
     print(json.dumps(line))
 
 
-def make_grouped(name):
-    """Grouped-layout workloads on the EP8 shard: the gate_up-shaped and the
-    down-shaped GEMM over the same per-expert rows (random activations)."""
-    from w4a16_int4_moe_gb300 import workloads as wl
-    if name.startswith("grouped_contig_"):
-        m = int(name.split("_")[-1])
-        gu = wl.grouped_contiguous_problem(m, 48, 4096, 7168, seed=1)
-        dn = wl.grouped_contiguous_problem(m, 48, 7168, 2048, seed=2)
-        return gu, dn, f"grouped_contiguous_E48_m{m}_H7168_I2048"
-    if name == "grouped_masked_32":
-        gu = wl.grouped_masked_problem(48, 32, 4096, 7168, seed=1)
-        dn = wl.grouped_masked_problem(48, 32, 7168, 2048, seed=2)
-        dn.layout[:] = gu.layout          # the same rows in both GEMMs
-        return gu, dn, "grouped_masked_E48_budget32_H7168_I2048"
-    raise SystemExit(f"unknown workload {name}")
-
-
 def run_grouped(args):
-    """One step = the grouped gate_up GEMM then the grouped down GEMM (the
-    activation between them untimed), L2 flushed before each step."""
+    """A grouped workload as the headline (weights drawn on the device)."""
     import torch
+    from w4a16_int4_moe_gb300 import moe as moe_mod
     from w4a16_int4_moe_gb300 import ops
     torch.cuda.set_device(0)
     device = torch.device("cuda", 0)
     ops.load_library()
-    gu, dn, wname = make_grouped(args.workload)
-
-    def to_dev(a):
-        return torch.from_numpy(np.ascontiguousarray(a)).to(device)
-
-    calls = []
-    for gp in (gu, dn):
-        pk = ops.w4a16_prepack(to_dev(gp.q), to_dev(gp.s.view(np.int16)))
-        a = to_dev(gp.a.view(np.int16)).view(torch.bfloat16)
-        lay = to_dev(gp.layout)
-        kind = ops.W4A16_GROUPED_CONTIGUOUS if gp.kind == "contiguous" else ops.W4A16_GROUPED_MASKED
-        m = gp.a.shape[0] if gp.kind == "contiguous" else gp.a.shape[1]
-        shape = (m, gp.n) if gp.kind == "contiguous" else (gp.num_experts, m, gp.n)
-        out = torch.empty(shape, dtype=torch.bfloat16, device=device)
-        ws = torch.zeros(256, dtype=torch.uint8, device=device)
-        calls.append((gp, kind, pk, a, m, lay, ws, out))
+    packed = {}
+    for (n, k), seed in (((4096, 7168), 1), ((7168, 2048), 2)):
+        q, s = device_weights(48, n, k, seed, device)
+        packed[(n, k)] = moe_mod.PackedExperts.from_checkpoint(q, s)
+        del q, s
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
-    stream = torch.cuda.current_stream()
-
-    def run(c):
-        gp, kind, pk, a, m, lay, ws, out = c
-        ops.w4a16_moe_grouped_gemm(kind, pk, gp.num_experts, gp.n, gp.k, a, m, lay, ws,
-                                   expected_m=gp.expected_m, out=out)
-
-    for _ in range(args.warmup):
-        flush.zero_()
-        run(calls[0])
-        run(calls[1])
-    torch.cuda.synchronize()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     clocks = ClockSampler()
     clocks.start()
-    t0 = time.perf_counter()
-    for i in range(args.steps):
-        flush.zero_()
-        ev[i][0].record(stream)
-        run(calls[0])
-        ev[i][1].record(stream)
-        run(calls[1])
-        ev[i][2].record(stream)
-    torch.cuda.synchronize()
-    wall = time.perf_counter() - t0
-    clocks.mark(time.time() - wall, time.time())
+    r = grouped_config(args.workload, packed, device, flush, args.steps, args.warmup,
+                       measured_peaks())
+    t_end = time.time()
+    clocks.mark(t_end - r["wall_s"], t_end)
     clk = clocks.stop()
-    for c in calls:
-        st, word = ops.w4a16_read_device_status(c[6])
-        if st != ops.W4A16_OK:
-            raise SystemExit(f"device status {word:#x}")
-    gu_us = statistics.mean(e[0].elapsed_time(e[1]) * 1e3 for e in ev)
-    dn_us = statistics.mean(e[1].elapsed_time(e[2]) * 1e3 for e in ev)
-    rows = gu.valid_rows()
-    wb = 0.5 + 2.0 / 32
-    act_e = 48 if gu.kind == "contiguous" else int((gu.layout > 0).sum())
-    gu_bytes = act_e * 4096 * 7168 * wb + rows * 7168 * 2 + rows * 4096 * 2
-    dn_bytes = act_e * 7168 * 2048 * wb + rows * 2048 * 2 + rows * 7168 * 2
-    gu_flops, dn_flops = 2.0 * rows * 4096 * 7168, 2.0 * rows * 7168 * 2048
-    hbm, tflops_peak, peak_src = measured_peaks()
-    layer_us = gu_us + dn_us
-    tensor = gu.kind == "contiguous"
-    if tensor:
-        ach = gu_flops / (gu_us * 1e-6) / 1e12
-        roof = {"bound": "tensor", "kernel": "w4a16_moe_gemm_kernel (grouped gate_up)",
-                "achieved": ach, "peak": tflops_peak, "unit": "TFLOP/s", "frac": ach / tflops_peak,
-                "peak_source": f"{peak_src} bf16_tflops", "traffic": None}
-    else:
-        ach = gu_bytes / (gu_us * 1e-6) / 1e9
-        roof = {"bound": "hbm", "kernel": "w4a16_moe_gemm_kernel (grouped gate_up)",
-                "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
-                "peak_source": f"{peak_src} hbm_gbs", "traffic": None,
-                "algorithmic_bytes": gu_bytes}
     line = {
-        "metric": METRIC, "value": layer_us, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": wall / args.steps * 1e3,
-        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "metric": METRIC, "value": r["layer_us"], "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": r["wall_s"] / args.steps * 1e3, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; random uint4 weights, N(0,1) activations)",
-        "config": {"workload": wname, "valid_rows": rows, "experts": 48,
+        "config": {"workload": r["workload"], "valid_rows": r["valid_rows"], "experts": 48,
                    "l2": "flushed before every step (256 MiB write)"},
-        "gate_up_us": gu_us, "down_us": dn_us,
-        "achieved": {"tflops": (gu_flops + dn_flops) / (layer_us * 1e-6) / 1e12,
-                     "hbm_gbs": (gu_bytes + dn_bytes) / (layer_us * 1e-6) / 1e9},
-        "roofline": roof, "gpu_launches": 2 * args.steps, "clocks": clk,
+        "gate_up_us": r["gate_up_us"], "down_us": r["down_us"], "tflops": r["tflops"],
+        "roofline": r["roofline"], "gpu_launches": 2 * args.steps, "clocks": clk,
     }
     print(json.dumps(line))
 
@@ -576,15 +740,20 @@ def run_grouped(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--layers", type=int, default=32,
+                    help="MoE layers per step (each streams the weights after an L2 flush)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="ep8_decode")
-    ap.add_argument("--ref-experts", type=int, default=2,
-                    help="experts per reference step (bounded CPU sample)")
+    ap.add_argument("--ref-experts", type=int, default=None,
+                    help="reference arm: experts per step (default: every active expert, "
+                         "the whole layer)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fused", action="store_true",
                     help="skip the fused-activation layer measurement")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other configurations (the `configs` object)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

@@ -156,7 +156,8 @@ w4a16_status w4a16_moe_align_block_size(const int32_t* topk_ids, int tokens, int
  * Bytes of the packed weights of `num_experts` experts of shape [n, k].
  * Schema ([P-arex] "接入方式"): uint4, group 32, BF16 scales. group must be
  * 32 and k a positive multiple of 32, else W4A16_ERR_UNSUPPORTED; layout
- * must be W4A16_LAYOUT_KTILE64. Host only.
+ * must be W4A16_LAYOUT_KTILE64, or W4A16_LAYOUT_KTILE64_GLU16 with n a
+ * multiple of 128 (else W4A16_ERR_UNSUPPORTED). Host only.
  */
 w4a16_status w4a16_prepack_size(int num_experts, int n, int k, int group, int layout,
                                 size_t* bytes);
@@ -332,12 +333,14 @@ w4a16_status w4a16_read_device_status(void* workspace, int* detail, void* stream
  *   exceeds 32 MiB (for k = 7168 that is a routing capacity above 2340
  *   rows).
  * - The first call on each device looks up the array's device address
- *   (cudaGetSymbolAddress, with that device current); make that first call
- *   before any stream capture begins.
- * - Every call on a device shares the array and the call clears its status
- *   word on `stream` first, so calls that overlap on the GPU (different
- *   streams without ordering) race on it: order them, or use
- *   w4a16_moe_indexed_gemm with one workspace per stream.
+ *   (cudaGetSymbolAddress, with that device current), and so does the first
+ *   call after the device's context changed (cudaDeviceReset); make that
+ *   first call before any stream capture begins.
+ * - Every call on a device shares the array. Once every argument check has
+ *   passed, the call clears the array's status word on `stream`, then
+ *   launches; a refused call enqueues nothing. Calls that overlap on the GPU
+ *   (different streams without ordering) race on the array: order them, or
+ *   use w4a16_moe_indexed_gemm with one workspace per stream.
  * - flags: those of w4a16_moe_indexed_gemm except W4A16_FLAG_DETERMINISTIC
  *   (refused with W4A16_ERR_INVALID_ARG: its row buffer needs a workspace
  *   sized by the caller), plus W4A16_FLAG_SYNC_STATUS to synchronise

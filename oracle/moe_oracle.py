@@ -285,24 +285,31 @@ def topk_softmax(logits, topk: int, renormalize: bool = True, expert_offset: int
       on the input values themselves;
     * weights = p of the chosen experts, divided by their sum if `renormalize`;
     * ids become local: g - expert_offset when that lies in
-      [0, num_local_experts), else -1 (an expert of another GPU).
+      [0, num_local_experts), else -1 (an expert of another GPU);
+    * an expert whose logit is -inf is masked: it is never chosen (its
+      softmax probability is 0). When fewer than k experts can be chosen, the
+      remaining slots hold id -1 and weight 0.
 
     logits float [T, E]. Returns (ids int32 [T, k], weights float64 [T, k])."""
     lg = np.asarray(logits, dtype=np.float64)
     t, e = lg.shape
     if num_local_experts is None:
         num_local_experts = e
-    ids = np.empty((t, topk), dtype=np.int32)
-    w = np.empty((t, topk), dtype=np.float64)
+    ids = np.full((t, topk), -1, dtype=np.int32)
+    w = np.zeros((t, topk), dtype=np.float64)
     for i in range(t):
         row = lg[i]
-        p = np.exp(row - row.max())
+        cand = np.flatnonzero(row > -np.inf)              # the experts that can be chosen
+        if cand.size == 0:
+            continue
+        p = np.where(row > -np.inf, np.exp(row - row[cand].max()), 0.0)
         p /= p.sum()
-        order = np.lexsort((np.arange(e), -row))[:topk]   # by logit desc, then id asc
+        order = cand[np.lexsort((cand, -row[cand]))][:topk]   # by logit desc, then id asc
         sel = p[order]
         if renormalize:
             sel = sel / sel.sum()
         loc = order - expert_offset
-        ids[i] = np.where((loc >= 0) & (loc < num_local_experts), loc, -1)
-        w[i] = sel
+        n = order.size
+        ids[i, :n] = np.where((loc >= 0) & (loc < num_local_experts), loc, -1)
+        w[i, :n] = sel
     return ids, w

@@ -216,3 +216,24 @@ def test_header_is_plain_c():
         r = subprocess.run([cc, "-fsyntax-only", "-Wall", "-Werror", "-x", lang, header],
                            capture_output=True, text=True)
         assert r.returncode == 0, r.stderr
+
+
+def test_noalloc_refuses_a_workspace_beyond_its_array(lib):
+    # the built-in array holds 32 MiB: at k = 7168 (14336 B per routed row
+    # after the 256 status bytes) a routing capacity of 2340 rows fits and
+    # 2341 does not. Capacity 2340 is not a multiple of block_m 32, so the
+    # call that passes the size check is refused right after it, before any
+    # CUDA call; nothing is launched with these fake pointers.
+    import ctypes
+    plan = ops.w4a16_plan(64, 8, 48, 4096, 7168)
+    plan.block_m = 32
+    fake = ctypes.c_void_p(1 << 20)
+
+    def call(capacity):
+        return lib.w4a16_moe_indexed_gemm_noalloc(0, fake, 48, 4096, 7168, fake, 64, 8, fake,
+                                                  fake, fake, capacity, None, fake, 0,
+                                                  ctypes.byref(plan), None)
+    assert ops.w4a16_workspace_size(plan, 2340, 7168) <= 32 << 20
+    assert ops.w4a16_workspace_size(plan, 2341, 7168) > 32 << 20
+    assert call(2341) == ops.W4A16_ERR_WORKSPACE
+    assert call(2340) == ops.W4A16_ERR_INVALID_ARG

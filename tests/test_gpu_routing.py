@@ -45,6 +45,20 @@ def test_topk_softmax_bf16_ties(cuda_dev):
     _check(bf16_tensor(bits, cuda_dev), oracle.bf16_bits_to_f64(bits), 8, True, 0, 384)
 
 
+def test_topk_softmax_masked_experts(cuda_dev):
+    # -inf logits mask experts; rows with fewer than k unmasked experts get
+    # id -1 and weight 0 in the remaining slots, also when every expert is masked
+    rng = np.random.default_rng(5)
+    lg = rng.standard_normal((40, 64)).astype(np.float32)
+    for t in range(40):
+        keep = rng.choice(64, size=t % 12, replace=False)   # 0..11 experts left
+        row = np.full(64, -np.inf, dtype=np.float32)
+        row[keep] = lg[t, keep]
+        lg[t] = row
+    for renorm in (True, False):
+        _check(torch.from_numpy(lg).to(cuda_dev), lg, 8, renorm, 0, 64)
+
+
 def test_unsupported_sizes_are_refused(cuda_dev):
     lg = torch.zeros((4, 1025), device=cuda_dev)
     with pytest.raises(ops.W4A16Error) as ei:

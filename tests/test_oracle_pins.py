@@ -415,6 +415,21 @@ def test_topk_softmax_brute_force_over_subsets():
         assert np.all(np.diff(w[0]) <= 1e-15)            # larger logit, larger weight first
 
 
+def test_topk_softmax_masked_experts_golden():
+    # hand-derived: logits 0, -inf, 1, -inf with k = 3: only experts 2 and 0
+    # can be chosen (larger logit first); their softmax weights are e/(1+e)
+    # and 1/(1+e) (the masked experts have probability 0), already summing to
+    # 1; the third slot finds no expert: id -1, weight 0
+    lg = np.array([[0.0, -np.inf, 1.0, -np.inf]])
+    ids, w = oracle.topk_softmax(lg, 3)
+    assert ids.tolist() == [[2, 0, -1]]
+    e = np.e
+    np.testing.assert_allclose(w, [[e / (1 + e), 1 / (1 + e), 0.0]], rtol=1e-15, atol=0)
+    # every expert masked: no slot is routed
+    ids, w = oracle.topk_softmax(np.full((1, 4), -np.inf), 2)
+    assert ids.tolist() == [[-1, -1]] and w.tolist() == [[0.0, 0.0]]
+
+
 def test_planted_ascending_topk_is_caught(monkeypatch):
     import oracle.moe_oracle as om
     real = om.np.lexsort

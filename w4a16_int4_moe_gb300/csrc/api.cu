@@ -234,6 +234,21 @@ w4a16_status w4a16_moe_indexed_gemm(int mode, const void* packed, int num_expert
                                     const float* topk_weights, void* out, int flags,
                                     const w4a16_plan_t* plan, void* workspace, size_t ws_bytes,
                                     void* stream) {
+  return w4a16::indexed_gemm(mode, packed, num_experts, n, k, a, tokens, topk, sorted_ids,
+                             expert_ids, num_tokens_padded, capacity, topk_weights, out, flags,
+                             plan, workspace, ws_bytes, stream, false);
+}
+
+}  // extern "C"
+
+namespace w4a16 {
+
+w4a16_status indexed_gemm(int mode, const void* packed, int num_experts, int n, int k,
+                          const uint16_t* a, int tokens, int topk, const int32_t* sorted_ids,
+                          const int32_t* expert_ids, const int32_t* num_tokens_padded,
+                          int capacity, const float* topk_weights, void* out, int flags,
+                          const w4a16_plan_t* plan, void* workspace, size_t ws_bytes,
+                          void* stream, bool noalloc) {
   if (mode != W4A16_GATE_UP && mode != W4A16_DOWN && mode != W4A16_GATE_UP_SILU)
     return W4A16_ERR_INVALID_ARG;
   if (num_experts <= 0 || n <= 0 || k <= 0 || tokens < 0 || topk <= 0 || capacity < 0)
@@ -256,7 +271,8 @@ w4a16_status w4a16_moe_indexed_gemm(int mode, const void* packed, int num_expert
   if (numel_all >= (1LL << 30)) return W4A16_ERR_UNSUPPORTED;
   const size_t ws_det =
       det ? w4a16_deterministic_bytes(capacity, n, static_cast<int>(numel_all)) : 0;
-  if (workspace == nullptr || ws_bytes < ws_base + ws_det) return W4A16_ERR_WORKSPACE;
+  if ((!noalloc && workspace == nullptr) || ws_bytes < ws_base + ws_det)
+    return W4A16_ERR_WORKSPACE;
   Pipeline pl;
   if (!plan_pipeline(*plan, k, &pl)) return W4A16_ERR_INVALID_ARG;
   // the fused activation needs the interleaved gate/up packing, and only it
@@ -292,6 +308,14 @@ w4a16_status w4a16_moe_indexed_gemm(int mode, const void* packed, int num_expert
         if (id < 0 || id > numel) return W4A16_ERR_ROUTING;
       }
     }
+  }
+  // every check passed: only now may anything be enqueued. The library's
+  // own scratch array keeps what the previous call left: its status word is
+  // cleared first.
+  if (noalloc) {
+    workspace = noalloc_scratch_address();
+    if (workspace == nullptr) return W4A16_ERR_CUDA;
+    if (cudaMemsetAsync(workspace, 0, kStatusBytes, s) != cudaSuccess) return W4A16_ERR_CUDA;
   }
 
   // the down pass adds into `out`: zeroed first unless ACCUMULATE (by the
@@ -377,6 +401,10 @@ w4a16_status w4a16_moe_indexed_gemm(int mode, const void* packed, int num_expert
     return W4A16_ERR_CUDA;
   return W4A16_OK;
 }
+
+}  // namespace w4a16
+
+extern "C" {
 
 w4a16_status w4a16_moe_grouped_gemm(int kind, const void* packed, int num_experts, int n, int k,
                                     const uint16_t* a, int m, const int32_t* layout,

@@ -99,6 +99,20 @@ struct GemmArgs {
 };
 
 int device_sm_count(int device);
+
+// w4a16_moe_indexed_gemm. With noalloc the workspace is the library's own
+// scratch array of ws_bytes (noalloc.cu; `workspace` is ignored): its device
+// address is looked up and its status words are zeroed on `stream` only once
+// every host-side check has passed (a refused call makes no CUDA call).
+w4a16_status indexed_gemm(int mode, const void* packed, int num_experts, int n, int k,
+                          const uint16_t* a, int tokens, int topk, const int32_t* sorted_ids,
+                          const int32_t* expert_ids, const int32_t* num_tokens_padded,
+                          int capacity, const float* topk_weights, void* out, int flags,
+                          const w4a16_plan_t* plan, void* workspace, size_t ws_bytes,
+                          void* stream, bool noalloc);
+// Device address of the no-allocation scratch array on the current device
+// (nullptr on a CUDA error).
+void* noalloc_scratch_address();
 size_t gemm_smem_bytes(int block_m, int w_stages, int b_stages);
 // TMEM split for a block of block_m rows and a reduction of k_steps 64-k
 // steps: columns of one accumulator, the number of partial accumulators (MMA

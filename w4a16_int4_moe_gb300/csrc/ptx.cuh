@@ -1,4 +1,4 @@
-// ptx.cuh -- inline-PTX helpers for sm_103a: mbarriers, bulk copies, cp.async,
+// ptx.cuh -- inline-PTX helpers for sm_103a: mbarriers, bulk and tensor copies,
 // tcgen05 (TMEM allocation, MMA, loads/stores, commits and fences).
 //
 // Only hand-written PTX from the public ISA lives here; nothing is taken
@@ -81,19 +81,6 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
 
 // ------------------------------------------------ tensor copies (TMA) ---
 
-// Four rows (given by their row coordinates) of a 2-D tensor map whose box
-// is one row high, written as four consecutive rows at `dst` with the map's
-// swizzle; completion counted in bytes on `bar`. Out-of-range rows read the
-// fill value (zero).
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* map, int col, int r0, int r1,
-                                            int r2, int r3, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(map), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
-      : "memory");
-}
-
 // One box of a 2-D tensor map at (col, row).
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* map, int col, int row,
                                             uint32_t bar) {
@@ -114,21 +101,8 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, int c
       : "memory");
 }
 
-// ---------------------------------------------------- cp.async (gather) ---
+// ------------------------------------------------------- proxy fences ---
 
-// 16-byte copy; src_bytes == 0 writes 16 zero bytes and reads nothing.
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-               "r"(src_bytes)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
 // Make this thread's generic-proxy shared-memory writes visible to the async
 // proxy (the tensor core reads its shared-memory operand through it).
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -184,21 +158,6 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
       : "memory");
 }
 
-// Warp-collective: thread t of the warp writes 32 consecutive 32-bit columns
-// starting at `taddr` of TMEM lane (lane field of taddr) + t.
-__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&v)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
-      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(
-          taddr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
-      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
-      "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
-      "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
-      "r"(v[29]), "r"(v[30]), "r"(v[31])
-      : "memory");
-}
 // Warp-collective: thread t writes 16 consecutive 32-bit columns.
 __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&v)[16]) {
   asm volatile(

@@ -7,7 +7,8 @@
 // the serving stack's. Reading taken here: softmax over all experts, the k
 // largest logits (ties to the lower expert id), the chosen probabilities
 // optionally renormalised to sum to 1, and global ids mapped to this GPU's
-// local experts (-1 for another GPU's).
+// local experts (-1 for another GPU's). Experts with a -inf logit are masked:
+// never chosen; slots that find no expert hold id -1 and weight 0.
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -79,19 +80,22 @@ __global__ void __launch_bounds__(kTopkWarps * 32)
           be = oe;
         }
       }
-      if (be < num_experts && (be & 31) == lane) taken |= 1u << (be >> 5);
-      const float p = expf(bv - mx) / sum;
+      // no expert left to choose (the rest are masked with -inf logits):
+      // the slot holds id -1 and weight 0
+      const bool found = be < num_experts;
+      if (found && (be & 31) == lane) taken |= 1u << (be >> 5);
+      const float p = found ? expf(bv - mx) / sum : 0.f;
       sel_sum += p;
       if (lane == s) {
         my_p = p;
-        my_id = be;
+        my_id = found ? be : -1;
       }
     }
     if (lane < topk) {
       const int loc = my_id - expert_offset;
       const long long at = static_cast<long long>(t) * topk + lane;
-      topk_ids[at] = (loc >= 0 && loc < num_local) ? loc : -1;
-      topk_weights[at] = renormalize ? my_p / sel_sum : my_p;
+      topk_ids[at] = (my_id >= 0 && loc >= 0 && loc < num_local) ? loc : -1;
+      topk_weights[at] = renormalize ? (sel_sum > 0.f ? my_p / sel_sum : 0.f) : my_p;
     }
   }
 }

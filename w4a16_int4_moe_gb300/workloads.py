@@ -111,9 +111,14 @@ def _draw_expert_tokens(rng, tokens, topk, counts):
             return lists
 
 
-def make_problem(name, rng, tokens, hidden, inter, num_experts, topk, topk_ids, meta=None):
-    q_gu, s_gu = random_weights(rng, num_experts, 2 * inter, hidden)
-    q_dn, s_dn = random_weights(rng, num_experts, hidden, inter)
+def make_problem(name, rng, tokens, hidden, inter, num_experts, topk, topk_ids, meta=None,
+                 weights=True):
+    """weights=False leaves the four weight arrays None (routing and
+    activations only, for callers that draw the weights elsewhere)."""
+    q_gu = s_gu = q_dn = s_dn = None
+    if weights:
+        q_gu, s_gu = random_weights(rng, num_experts, 2 * inter, hidden)
+        q_dn, s_dn = random_weights(rng, num_experts, hidden, inter)
     x = random_activations(rng, tokens, hidden)
     w = softmax_weights(rng, tokens, topk)
     return MoEProblem(name, tokens, hidden, inter, num_experts, topk, x,
@@ -121,12 +126,12 @@ def make_problem(name, rng, tokens, hidden, inter, num_experts, topk, topk_ids, 
                       q_gu, s_gu, q_dn, s_dn, meta or {})
 
 
-def uniform_problem(tokens, hidden, inter, num_experts, topk, seed=0, name=None):
+def uniform_problem(tokens, hidden, inter, num_experts, topk, seed=0, name=None, weights=True):
     """Top-k uniform-random routing over all (local) experts."""
     rng = np.random.default_rng(seed)
     ids = _uniform_topk(rng, tokens, num_experts, topk)
     return make_problem(name or f"uniform_T{tokens}_H{hidden}_I{inter}_E{num_experts}_k{topk}",
-                        rng, tokens, hidden, inter, num_experts, topk, ids)
+                        rng, tokens, hidden, inter, num_experts, topk, ids, weights=weights)
 
 
 def tiny(seed=0):
@@ -153,10 +158,11 @@ def ep8_decode(seed=0, tokens=576, hidden=7168, inter=2048, local_experts=48, to
                         {"tok_e": counts.tolist()})
 
 
-def tp8(tokens, seed=0, hidden=7168, inter_shard=256, experts=384, topk=8):
+def tp8(tokens, seed=0, hidden=7168, inter_shard=256, experts=384, topk=8, weights=True):
     """TP8 single-instance shard: all 384 experts, intermediate 2048/8."""
     p = uniform_problem(tokens, hidden, inter_shard, experts, topk, seed,
-                        name=f"tp8_T{tokens}_H{hidden}_I{inter_shard}_E{experts}_top{topk}")
+                        name=f"tp8_T{tokens}_H{hidden}_I{inter_shard}_E{experts}_top{topk}",
+                        weights=weights)
     return p
 
 
@@ -169,14 +175,15 @@ def ep8_prefill_counts(local_experts=48, seed=0):
     return counts[rng.permutation(local_experts)]
 
 
-def ep8_prefill(seed=0, tokens=8192, hidden=7168, inter=2048, local_experts=48, topk=8):
+def ep8_prefill(seed=0, tokens=8192, hidden=7168, inter=2048, local_experts=48, topk=8,
+                weights=True):
     rng = np.random.default_rng(seed)
     counts = ep8_prefill_counts(local_experts, seed)
     lists = _draw_expert_tokens(rng, tokens, topk, counts)
     ids = _place_local_picks(rng, tokens, topk, lists)
     return make_problem(f"ep8_prefill_T{tokens}_H{hidden}_I{inter}_E{local_experts}_top{topk}",
                         rng, tokens, hidden, inter, local_experts, topk, ids,
-                        {"tok_e": counts.tolist()})
+                        {"tok_e": counts.tolist()}, weights=weights)
 
 
 @dataclass
@@ -217,6 +224,25 @@ def grouped_contiguous_problem(rows_per_expert, num_experts=48, n=4096, k=7168, 
     a = random_activations(rng, int(padded.sum()), k)
     return GroupedProblem(name or f"grouped_contiguous_E{num_experts}_N{n}_K{k}", "contiguous",
                           num_experts, n, k, a, m_expert, q, s, int(m_e.mean()))
+
+
+def contiguous_layout(rows_per_expert, num_experts=48, align=128):
+    """m_expert [M_pad] int32 of the contiguous layout: each expert's rows,
+    padded up to a multiple of ``align`` rows with -1."""
+    if np.isscalar(rows_per_expert):
+        m_e = np.full(num_experts, int(rows_per_expert), dtype=np.int64)
+    else:
+        m_e = np.asarray(rows_per_expert, dtype=np.int64)
+    padded = -(-m_e // align) * align
+    return np.concatenate([
+        np.concatenate([np.full(m, e), np.full(p - m, -1)]) for e, (m, p) in enumerate(zip(m_e, padded))
+    ]).astype(np.int32)
+
+
+def masked_counts(num_experts=48, max_m=32, seed=0):
+    """masked_m ~ U{1..max_m} per expert (the draw of grouped_masked_problem)."""
+    rng = np.random.default_rng(seed)
+    return rng.integers(1, max_m + 1, size=num_experts).astype(np.int32)
 
 
 def grouped_masked_problem(num_experts=48, max_m=32, n=4096, k=7168, seed=0, name=None,
