@@ -110,6 +110,12 @@ typedef struct {
   int swap_ab;     /* 1: weights are the MMA M operand, tokens the N one  */
   int layout;      /* W4A16_LAYOUT_KTILE64                                */
   int grid;        /* CTAs to launch; 0 = number of SMs x ctas_per_sm     */
+  int cta_pair;    /* 1: pairs of CTAs (2-CTA clusters) each work on 256
+                      weight rows, the pair's even CTA issuing M = 256
+                      tensor-core MMAs over both CTAs' operands; needs
+                      block_m % 32 == 0 (else the plan is refused); used
+                      when the weight tile count (n / 128, rounded up) is
+                      even, else the call runs unpaired. 0: unpaired      */
 } w4a16_plan_t;
 
 /*

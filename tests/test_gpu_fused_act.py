@@ -19,7 +19,7 @@ from helpers import assert_close, bf16_bits, bf16_tensor, dev
 pytestmark = pytest.mark.gpu
 
 
-def _fused_and_unfused(p, device, bm=None):
+def _fused_and_unfused(p, device, bm=None, cta_pair=0):
     q, s = dev(p.q_gu, device), dev(p.s_gu.view(np.int16), device)
     pk = ops.w4a16_prepack(q, s)
     pk_glu = ops.w4a16_prepack(q, s, layout=ops.W4A16_LAYOUT_KTILE64_GLU16)
@@ -28,6 +28,7 @@ def _fused_and_unfused(p, device, bm=None):
     if bm:
         plan.block_m = bm
         plan.stages, plan.b_stages = min(plan.stages, 8), 8   # fit larger token stages
+    plan.cta_pair = cta_pair
     sid, eid, ntp = ops.w4a16_moe_align_block_size(dev(p.topk_ids, device), p.num_experts,
                                                    plan.block_m)
     ws = ops.new_workspace(plan, device, sid.numel(), p.hidden)
@@ -58,8 +59,19 @@ def test_fused_activation_tiny(cuda_dev, bm):
     # against the float64 chain from the inputs: gate_up, BF16, then silu * up
     g_ref = oracle.indexed_gate_up(p.x, p.topk_ids, p.q_gu, p.s_gu)
     a_chain = oracle.silu_and_mul(oracle.f64_to_bf16_bits(np.nan_to_num(g_ref[routed])))
-    assert_close(oracle.bf16_bits_to_f64(act_bits[routed]), oracle.bf16_bits_to_f64(a_chain),
-                 f"fused act vs oracle chain bm={bm}", rel_l2=1e-2, max_abs_frac=2e-2)
+    # the activation of the BF16 gate and up values: the GEMM tolerance holds
+    # (measured rel-L2 3.8e-3 on GB300)
+    e = assert_close(oracle.bf16_bits_to_f64(act_bits[routed]), oracle.bf16_bits_to_f64(a_chain),
+                     f"fused act vs oracle chain bm={bm}")
+    print(f"fused act vs oracle chain bm={bm}: rel-L2 {e[0]:.3e} max-abs {e[1]:.3e}")
+
+
+@pytest.mark.parametrize("bm", [32, 64])
+def test_fused_activation_pair(cuda_dev, bm):
+    # CTA pairs: the fused epilogue of each CTA's tile gives the unfused bits
+    p = wl.tiny(seed=53)
+    g_bits, ref_bits, act_bits, routed = _fused_and_unfused(p, cuda_dev, bm, cta_pair=1)
+    np.testing.assert_array_equal(act_bits[routed], ref_bits[routed])
 
 
 def test_fused_activation_tp8_shape(cuda_dev):
@@ -81,7 +93,7 @@ def test_fused_activation_ep8_decode_full_size(cuda_dev):
     u = oracle.bf16_bits_to_f64(gb[:, len(cols):])
     a_ref = g / (1.0 + np.exp(-g)) * u
     assert_close(oracle.bf16_bits_to_f64(act_bits[routed][:, cols]), a_ref,
-                 "fused act EP8 sampled columns", rel_l2=1e-2, max_abs_frac=2e-2)
+                 "fused act EP8 sampled columns")
 
 
 def test_layer_forward_with_fused_activation(cuda_dev):

@@ -33,12 +33,13 @@ def _routing(ids, experts, bm, device):
     return ops.w4a16_moe_align_block_size(t, experts, bm, cap)
 
 
-def _plan(bm, n, k, stages=None, b_stages=None, grid=0):
+def _plan(bm, n, k, stages=None, b_stages=None, grid=0, pair=False):
     p = ops.w4a16_plan(64, 1, 1, n, k, float(bm))
     p.block_m = bm
     p.b_stages = b_stages or 8
     p.stages = stages or min(p.stages, 8)
     p.grid = grid
+    p.cta_pair = int(pair)
     return p
 
 
@@ -72,12 +73,12 @@ def _routed(p):
     return (flat >= 0) & (flat < p.num_experts)
 
 
-def _check_pair(p, device, bm, cols_gu=None, cols_dn=None, what=""):
+def _check_pair(p, device, bm, cols_gu=None, cols_dn=None, what="", cta_pair=False):
     """gate_up vs oracle, then down (on the GPU's activation) vs oracle."""
     pk_gu = _pack(p.q_gu, p.s_gu, device)
     pk_dn = _pack(p.q_dn, p.s_dn, device)
     routing = _routing(p.topk_ids, p.num_experts, bm, device)
-    g = _gate_up(p, pk_gu, routing, _plan(bm, 2 * p.inter, p.hidden), device)
+    g = _gate_up(p, pk_gu, routing, _plan(bm, 2 * p.inter, p.hidden, pair=cta_pair), device)
     g_bits = bf16_bits(g)
     routed = _routed(p)
     g_ref = oracle.indexed_gate_up(p.x, p.topk_ids, p.q_gu, p.s_gu, cols=cols_gu)
@@ -93,7 +94,8 @@ def _check_pair(p, device, bm, cols_gu=None, cols_dn=None, what=""):
                  rel_l2=4e-3, max_abs_frac=1e-2)
     a_bits_clean = a_bits.copy()
     a_bits_clean[~routed] = 0
-    y = _down(p, pk_dn, routing, _plan(bm, p.hidden, p.inter), a_bits_clean, device)
+    y = _down(p, pk_dn, routing, _plan(bm, p.hidden, p.inter, pair=cta_pair), a_bits_clean,
+              device)
     y_ref = oracle.indexed_down(a_bits_clean, p.topk_ids, p.topk_weights, p.q_dn, p.s_dn,
                                 cols=cols_dn)
     y_got = y.cpu().numpy()
@@ -410,3 +412,61 @@ def test_grouped_contiguous_full_size_ragged(cuda_dev):
     ref = oracle.grouped_contiguous(gp.a[rows], gp.layout[rows], gp.q, gp.s, cols=cols)
     valid = gp.layout[rows] >= 0
     assert_close(got[rows][:, cols][valid], ref[valid], "contiguous full size")
+
+
+# ------------------------------------------------------------- CTA pairs --
+# Pairs of CTAs (2-CTA clusters) issue M = 256 MMAs over two weight tiles, each
+# CTA holding one tile's dequantised rows and half of the block's token rows.
+
+@pytest.mark.parametrize("bm", [32, 64, 128])
+def test_pair_tiny_matches_oracle(cuda_dev, bm):
+    _check_pair(wl.tiny(seed=71), cuda_dev, bm, what=f"pair tiny bm={bm}", cta_pair=True)
+
+
+@pytest.mark.parametrize("tokens,hidden,inter,experts,topk,bm", [
+    (200, 320, 224, 6, 2, 64),   # gate_up 4 tiles (last one ragged); down 3 tiles: unpaired
+    (37, 96, 96, 5, 3, 32),      # k = 32 mod 64; 2 tiles / 1 tile (unpaired)
+    (5, 64, 32, 40, 4, 32),      # many empty experts
+])
+def test_pair_ragged_shapes(cuda_dev, tokens, hidden, inter, experts, topk, bm):
+    p = wl.uniform_problem(tokens, hidden, inter, experts, topk, seed=tokens + 1)
+    _check_pair(p, cuda_dev, bm, what=f"pair ragged {tokens}x{hidden}x{inter}", cta_pair=True)
+
+
+@pytest.mark.parametrize("bm", [32, 64])
+def test_pair_is_bitwise_the_unpaired_result(cuda_dev, bm):
+    # the pair MMA forms every output element from the same K slices in the
+    # same order as the one-CTA MMA: the bits agree
+    p = wl.uniform_problem(96, 512, 256, 8, 2, seed=72)
+    pk = _pack(p.q_gu, p.s_gu, cuda_dev)
+    routing = _routing(p.topk_ids, p.num_experts, bm, cuda_dev)
+    g1 = _gate_up(p, pk, routing, _plan(bm, 2 * p.inter, p.hidden), cuda_dev)
+    g2 = _gate_up(p, pk, routing, _plan(bm, 2 * p.inter, p.hidden, pair=True), cuda_dev)
+    routed = _routed(p)
+    np.testing.assert_array_equal(bf16_bits(g2)[routed], bf16_bits(g1)[routed])
+
+
+def test_pair_refuses_block_not_multiple_of_32(cuda_dev):
+    p = wl.tiny(seed=73)
+    pk = _pack(p.q_gu, p.s_gu, cuda_dev)
+    routing = _routing(p.topk_ids, p.num_experts, 16, cuda_dev)
+    with pytest.raises(ops.W4A16Error) as ei:
+        _gate_up(p, pk, routing, _plan(16, 2 * p.inter, p.hidden, pair=True), cuda_dev)
+    assert ei.value.status == ops.W4A16_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kind", ["contiguous", "masked"])
+def test_pair_grouped_matches_oracle(cuda_dev, kind):
+    if kind == "contiguous":
+        gp = wl.grouped_contiguous_problem([5, 128, 0, 77], num_experts=4, n=256, k=96, seed=74)
+        got = _grouped(gp, cuda_dev, _plan(32, gp.n, gp.k, pair=True))
+        ref = oracle.grouped_contiguous(gp.a, gp.layout, gp.q, gp.s)
+        valid = gp.layout >= 0
+    else:
+        gp = wl.grouped_masked_problem(num_experts=6, max_m=32, n=256, k=160, seed=75)
+        gp.layout[2] = 0
+        gp.layout[3] = 32
+        got = _grouped(gp, cuda_dev, _plan(32, gp.n, gp.k, pair=True))
+        ref = oracle.grouped_masked(gp.a, gp.layout, gp.q, gp.s)
+        valid = ~np.isnan(ref[..., 0])
+    assert_close(got[valid], ref[valid], f"pair grouped {kind}")

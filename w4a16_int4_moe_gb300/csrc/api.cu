@@ -56,7 +56,9 @@ bool plan_pipeline(const w4a16_plan_t& p, int k, Pipeline* out) {
     return false;
   pl.w_stages = p.stages / 4 * 4;
   pl.b_stages = p.b_stages / 2;
-  pl.smem = gemm_smem_bytes(p.block_m, pl.w_stages, pl.b_stages);
+  if (p.cta_pair != 0 && p.cta_pair != 1) return false;
+  if (p.cta_pair && p.block_m % 32 != 0) return false;
+  pl.smem = gemm_smem_bytes(p.block_m, pl.w_stages, pl.b_stages, p.cta_pair != 0);
   if (pl.smem > static_cast<size_t>(kMaxDynSmem)) return false;
   *out = pl;
   return true;
@@ -111,7 +113,7 @@ const char* w4a16_status_string(int status) {
   }
 }
 
-int w4a16_version(void) { return 110; }
+int w4a16_version(void) { return 120; }
 
 w4a16_status w4a16_plan(int tokens, int topk, int num_experts, int n, int k, float tok_e_hint,
                         w4a16_plan_t* out) {
@@ -355,7 +357,9 @@ w4a16_status indexed_gemm(int mode, const void* packed, int num_experts, int n, 
   uint16_t* permuted =
       reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(workspace) + kStatusBytes);
   const int a_div = mode == W4A16_DOWN ? 1 : topk;
-  if (!encode_permuted_tmap(&g.tmap, permuted, capacity, permuted_row_elems(k), bm))
+  // CTA pairs: each CTA of a pair loads half of a block's rows
+  const bool pair = plan->cta_pair != 0 && packed_tiles(n) % 2 == 0;
+  if (!encode_permuted_tmap(&g.tmap, permuted, capacity, permuted_row_elems(k), pair ? bm / 2 : bm))
     return W4A16_ERR_CUDA;
   // (n * 4 bytes per row is a multiple of 16 when n % 4 == 0; otherwise the
   // tail is cleared separately)
@@ -391,9 +395,15 @@ w4a16_status indexed_gemm(int mode, const void* packed, int num_experts, int n, 
   fill_pipeline(pl, &g);
   g.raster_rows = 0;
   g.timeout_cycles = wait_timeout_cycles();
+  g.pair = pair ? 1 : 0;
   long long grid = plan->grid > 0 ? plan->grid : static_cast<long long>(sms) * plan->ctas_per_sm;
   const long long max_items = static_cast<long long>(capacity / bm) * g.n_tiles;
   grid = std::max<long long>(1, std::min(grid, max_items));
+  if (pair) {
+    const int clusters = max_pair_clusters(g);
+    if (clusters <= 0) return W4A16_ERR_CUDA;
+    grid = 2 * std::max<long long>(1, std::min<long long>(grid / 2, clusters));
+  }
   if (launch_moe_gemm(g, static_cast<int>(grid), true, s) != cudaSuccess) return W4A16_ERR_CUDA;
   if (det && launch_det_reduce(det_rows, det_inv, tokens, topk, n,
                                (flags & W4A16_FLAG_ACCUMULATE) != 0, static_cast<float*>(out), sms,
@@ -476,7 +486,8 @@ w4a16_status w4a16_moe_grouped_gemm(int kind, const void* packed, int num_expert
   g.act = a;
   g.gather_rows = 0;
   g.act_rows = static_cast<int>(rows_total);
-  if (!encode_act_tmap(&g.tmap, a, rows_total, k, bm)) return W4A16_ERR_CUDA;
+  const bool pair = plan->cta_pair != 0 && g.n_tiles % 2 == 0;
+  if (!encode_act_tmap(&g.tmap, a, rows_total, k, pair ? bm / 2 : bm)) return W4A16_ERR_CUDA;
   g.family = kind == W4A16_GROUPED_CONTIGUOUS ? kContiguous : kMasked;
   g.out_mode = kOutBf16;
   g.layout = layout;
@@ -493,8 +504,14 @@ w4a16_status w4a16_moe_grouped_gemm(int kind, const void* packed, int num_expert
   const long long blocks = kind == W4A16_GROUPED_CONTIGUOUS
                                ? m / bm
                                : static_cast<long long>(num_experts) * ((m + bm - 1) / bm);
+  g.pair = pair ? 1 : 0;
   long long grid = plan->grid > 0 ? plan->grid : static_cast<long long>(sms) * plan->ctas_per_sm;
   grid = std::max<long long>(1, std::min(grid, blocks * g.n_tiles));
+  if (pair) {
+    const int clusters = max_pair_clusters(g);
+    if (clusters <= 0) return W4A16_ERR_CUDA;
+    grid = 2 * std::max<long long>(1, std::min<long long>(grid / 2, clusters));
+  }
   return cuda_status(launch_moe_gemm(g, static_cast<int>(grid), false, s));
 }
 

@@ -95,6 +95,9 @@ struct GemmArgs {
   // issuers), accumulator slots and the TMEM columns of one accumulator
   int w_stages, b_stages, n_parts, d_slots, d_cols;
   int raster_rows;  // 1: grouped item order (see decode_item), 0: tile-major
+  // 1: CTA pairs (clusters of 2) issue M = 256 MMAs over two weight tiles;
+  // needs an even tile count and block_m a multiple of 32; grid even
+  int pair;
   long long timeout_cycles;
 };
 
@@ -113,7 +116,10 @@ w4a16_status indexed_gemm(int mode, const void* packed, int num_experts, int n, 
 // Device address of the no-allocation scratch array on the current device
 // (nullptr on a CUDA error).
 void* noalloc_scratch_address();
-size_t gemm_smem_bytes(int block_m, int w_stages, int b_stages);
+size_t gemm_smem_bytes(int block_m, int w_stages, int b_stages, bool pair = false);
+// CTA pairs of the GEMM kernel for `args` that can be resident at once (0 on
+// error).
+int max_pair_clusters(const GemmArgs& args);
 // TMEM split for a block of block_m rows and a reduction of k_steps 64-k
 // steps: columns of one accumulator, the number of partial accumulators (MMA
 // issuers) and of accumulator slots.

@@ -49,6 +49,37 @@
 #include "internal.h"
 #include "ptx.cuh"
 
+// Role timing for development builds (-DW4A16_ROLE_PROFILE): each warp adds
+// the SM cycles between consecutive marks into per-category counters, stored
+// per CTA and warp when it finishes. Compiled out otherwise.
+#ifdef W4A16_ROLE_PROFILE
+__device__ long long g_w4a16_role_prof[256][32][8];
+#define W4A16_PROF_DECL                 \
+  long long prof_acc_[8] = {0};         \
+  long long prof_t_ = clock64();
+#define W4A16_PROF_MARK(i)              \
+  do {                                  \
+    const long long t_ = clock64();     \
+    prof_acc_[i] += t_ - prof_t_;       \
+    prof_t_ = t_;                       \
+  } while (0)
+#define W4A16_PROF_STORE()                                                        \
+  do {                                                                            \
+    if ((threadIdx.x & 31) == 0 && blockIdx.x < 256)                              \
+      for (int i_ = 0; i_ < 8; ++i_)                                              \
+        g_w4a16_role_prof[blockIdx.x][threadIdx.x >> 5][i_] = prof_acc_[i_];      \
+  } while (0)
+extern "C" int w4a16_debug_role_profile(long long* out, int bytes) {
+  const int n = bytes < static_cast<int>(sizeof(g_w4a16_role_prof))
+                    ? bytes : static_cast<int>(sizeof(g_w4a16_role_prof));
+  return cudaMemcpyFromSymbol(out, g_w4a16_role_prof, n) == cudaSuccess ? 0 : 1;
+}
+#else
+#define W4A16_PROF_DECL
+#define W4A16_PROF_MARK(i)
+#define W4A16_PROF_STORE()
+#endif
+
 namespace w4a16 {
 
 namespace {
@@ -87,7 +118,7 @@ constexpr int kWarpRouter = 26;     // per-item routing info, items ahead of the
 enum Where {
   kWhereProducer = 1, kWhereDequantW = 2, kWhereDequantA = 3, kWhereGatherItem = 4,
   kWhereGatherB = 5, kWhereMmaItem = 6, kWhereMmaAcc = 7, kWhereMmaA = 8, kWhereMmaB = 9,
-  kWhereEpiAcc = 10, kWhereEpiItem = 11, kWhereDrain = 12, kWhereRouter = 13
+  kWhereEpiAcc = 10, kWhereEpiItem = 11, kWhereDrain = 12, kWhereRouter = 13, kWhereRelay = 14
 };
 
 struct Smem {
@@ -125,13 +156,21 @@ __device__ __forceinline__ size_t align_up(size_t x, size_t a) { return (x + a -
 
 // Bounded wait: true when the phase of parity `parity` has completed; false
 // when the CTA is aborting or this wait ran out (then it starts the abort).
+// kCluster: the phase may be completed by arrivals from the other CTA of a
+// pair (remote arrives or multicast commits): acquire at cluster scope.
+template <bool kCluster = false>
+__device__ __forceinline__ bool try_wait_any(uint32_t bar, uint32_t parity, uint32_t suspend_ns) {
+  if constexpr (kCluster) return mbar_try_wait_cluster(bar, parity, suspend_ns);
+  return mbar_try_wait_sleep(bar, parity, suspend_ns);
+}
+template <bool kCluster = false>
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                         int* status, int where, long long timeout) {
   constexpr uint32_t kSuspendNs = 1000000;  // the thread sleeps until completion or 1 ms
-  if (mbar_try_wait_sleep(bar, parity, kSuspendNs)) return true;
+  if (try_wait_any<kCluster>(bar, parity, kSuspendNs)) return true;
   const long long t0 = clock64();
   while (true) {
-    if (mbar_try_wait_sleep(bar, parity, kSuspendNs)) return true;
+    if (try_wait_any<kCluster>(bar, parity, kSuspendNs)) return true;
     if (*abort_flag) return false;
     if (clock64() - t0 > timeout) {
       *abort_flag = 1;
@@ -144,10 +183,12 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
 // Warp-uniform bounded wait: every lane observes the phase itself (so each
 // lane's later reads are ordered after the completion it saw); the warp goes
 // on only if all lanes saw it.
+template <bool kCluster = false>
 __device__ __forceinline__ bool warp_wait_phase(uint32_t bar, uint32_t parity,
                                              volatile int* abort_flag, int* status, int where,
                                              long long timeout) {
-  return __all_sync(0xffffffffu, wait_phase(bar, parity, abort_flag, status, where, timeout));
+  return __all_sync(0xffffffffu,
+                    wait_phase<kCluster>(bar, parity, abort_flag, status, where, timeout));
 }
 
 // Bounded wait of the dequant warpgroups: polls without a suspend hint and
@@ -155,14 +196,20 @@ __device__ __forceinline__ bool warp_wait_phase(uint32_t bar, uint32_t parity,
 // instruction of the SM; a waiting warpgroup that backs off leaves the issue
 // slots to the three that work (measured 0.8% faster at EP8 decode than the
 // suspending wait, which the other roles keep: for them it was slower).
+template <bool kCluster = false>
+__device__ __forceinline__ bool try_wait_now(uint32_t bar, uint32_t parity) {
+  if constexpr (kCluster) return mbar_try_wait_cluster_now(bar, parity);
+  return mbar_try_wait(bar, parity);
+}
+template <bool kCluster = false>
 __device__ __forceinline__ bool wait_phase_backoff(uint32_t bar, uint32_t parity,
                                                    volatile int* abort_flag, int* status,
                                                    int where, long long timeout) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (try_wait_now<kCluster>(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     __nanosleep(128);
-    if (mbar_try_wait(bar, parity)) return true;
+    if (try_wait_now<kCluster>(bar, parity)) return true;
     if (*abort_flag) return false;
     if (clock64() - t0 > timeout) {
       *abort_flag = 1;
@@ -171,11 +218,12 @@ __device__ __forceinline__ bool wait_phase_backoff(uint32_t bar, uint32_t parity
     }
   }
 }
+template <bool kCluster = false>
 __device__ __forceinline__ bool warp_wait_phase_backoff(uint32_t bar, uint32_t parity,
                                                         volatile int* abort_flag, int* status,
                                                         int where, long long timeout) {
-  return __all_sync(0xffffffffu,
-                    wait_phase_backoff(bar, parity, abort_flag, status, where, timeout));
+  return __all_sync(0xffffffffu, wait_phase_backoff<kCluster>(bar, parity, abort_flag, status,
+                                                              where, timeout));
 }
 
 // Drain wait (abort path): wait for a phase that copies or MMAs already
@@ -251,12 +299,12 @@ struct ItemDesc {
 // kernel measurable time on short items (instruction footprint).
 constexpr int kRasterBlocks = 8;
 
-template <bool kRaster>
+template <bool kRaster, bool kPair>
 __device__ __forceinline__ ItemDesc decode_item(const GemmArgs& a, int it, int num_blocks,
-                                                int blocks_per_expert) {
+                                                int blocks_per_expert, uint32_t rank) {
   ItemDesc d;
   if constexpr (kRaster) {
-    const int per_group = kRasterBlocks * a.n_tiles;
+    const int per_group = kRasterBlocks * (kPair ? a.n_tiles >> 1 : a.n_tiles);
     const int group = it / per_group;
     const int rem = it - group * per_group;
     const int gsize = min(kRasterBlocks, num_blocks - group * kRasterBlocks);
@@ -266,6 +314,8 @@ __device__ __forceinline__ ItemDesc decode_item(const GemmArgs& a, int it, int n
     d.tile = it / num_blocks;
     d.blk = it - d.tile * num_blocks;
   }
+  // a CTA pair takes a pair of weight tiles: the even-ranked CTA the first
+  if constexpr (kPair) d.tile = d.tile * 2 + static_cast<int>(rank);
   int e = -1;
   if (a.family == kIndexed) {
     e = __ldg(a.expert_ids + d.blk);
@@ -365,12 +415,20 @@ __device__ __forceinline__ void dequant_group(const uint4 q, uint32_t scale_bits
 // kOutF32Rows) are compiled into their own instantiations so that they cannot
 // change the register allocation or the instruction footprint of the plain
 // kernel.
-template <bool kGlu, bool kRaster, bool kEarly, bool kRows>
+template <bool kGlu, bool kRaster, bool kEarly, bool kRows, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     w4a16_moe_gemm_kernel(const __grid_constant__ GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // A CTA pair (kPair, a cluster of 2) works on 256 weight rows at a time:
+  // each CTA dequantises its own 128 rows into its own TMEM and loads half of
+  // the block's token rows; the even-ranked CTA (the leader) issues M = 256
+  // MMAs over both. Otherwise every CTA works alone.
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  const int unit0 = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int units = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   // ---- shared-memory carve-up (base aligned to 1024 for the swizzle) ----
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -380,7 +438,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int BS = args.b_stages;
   const int parts = args.n_parts;
   const bool gather = args.gather_rows != 0;
-  const uint32_t b_step_bytes = static_cast<uint32_t>(bm) * 128u;
+  // token rows of a block held by this CTA (a pair splits them in halves)
+  const int bm_local = kPair ? bm >> 1 : bm;
+  const uint32_t b_step_bytes = static_cast<uint32_t>(bm_local) * 128u;
   const uint32_t b_stage_bytes = 2u * b_step_bytes;
   Smem sm;
   size_t off = 0;
@@ -440,11 +500,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(B.we(i), 4);  // the 4 warps of the warpgroup that read the stage
     }
     for (int i = 0; i < BS; ++i) {
-      mbar_init(B.bf(i), 1);        // the gather warp's arrival (+ tensor-copy bytes)
+      // the gather warp's arrival (+ tensor-copy bytes); the pair leader's
+      // also counts the peer's relayed arrival for its half of the rows
+      mbar_init(B.bf(i), (kPair && leader) ? 2 : 1);
       mbar_init(B.be(i), readers);  // tcgen05.commit of the stage's issuers
     }
     for (int i = 0; i < kASlots; ++i) {
-      mbar_init(B.af(i), 4);        // the 4 warps of the slot's dequant warpgroup
+      // the 4 warps of the slot's dequant warpgroup (of both CTAs of a pair)
+      mbar_init(B.af(i), kPair ? 8 : 4);
       mbar_init(B.ae(i), readers);
     }
     for (int i = 0; i < kItemSlots; ++i) {
@@ -453,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < kMaxDSlots; ++i) {
       mbar_init(B.accf(i), parts);  // one tcgen05.commit per MMA issuer
-      mbar_init(B.acce(i), 4);
+      mbar_init(B.acce(i), kPair ? 8 : 4);  // the epilogue warps (of both CTAs of a pair)
     }
     for (int i = 0; i < kMaxIssuers; ++i) mbar_init(B.fin(i), 1);
     *sm.abort_flag = 0;
@@ -461,11 +524,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_proxy_async_smem();
   }
   if (warp == kWarpMma0) {
-    tmem_alloc(smem_u32(sm.tmem_base), kTmemCols);
-    tmem_relinquish();
+    if constexpr (kPair) {
+      tmem_alloc_pair(smem_u32(sm.tmem_base), kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(sm.tmem_base), kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  // a pair's barriers must be initialised in both CTAs before either arrives
+  // on the other's
+  if constexpr (kPair) cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem = *sm.tmem_base;
 
@@ -481,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bpe = (args.m + bm - 1) / bm;
     num_blocks = args.num_experts * bpe;
   }
-  const int items = num_blocks * args.n_tiles;
+  const int items = num_blocks * (kPair ? args.n_tiles >> 1 : args.n_tiles);
   // TMEM columns: the kASlots A slots (64 columns each), then per accumulator
   // slot the `parts` partial accumulators, d_cols each.
   const int d_col_base = kASlots * kAColsPerSlot;
@@ -499,8 +570,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t issued = 0;  // stages whose w_full phase this thread started
       RingPos wp;
       bool ok = true;
-      for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
-        const ItemDesc d = decode_item<kRaster>(args, it, num_blocks, bpe);
+      for (int it = unit0; it < items && ok; it += units) {
+        const ItemDesc d = decode_item<kRaster, kPair>(args, it, num_blocks, bpe, rank);
         if (d.e < 0) continue;
         const uint8_t* src = args.wpack + static_cast<long long>(d.e) * args.expert_bytes +
                              static_cast<long long>(d.tile) * args.k_steps * kStepBytes;
@@ -532,37 +603,72 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if ((warp >= kWarpMma0 && warp < kWarpDequant0) || warp == kWarpMma3) {
     // ======================= MMA issuers ====================================
     // Issuer q takes the k steps ks % parts == q of every item and
-    // accumulates them into its own FP32 partial accumulator.
+    // accumulates them into its own FP32 partial accumulator. In a CTA pair
+    // the leader's issuers issue M = 256 MMAs over both CTAs' A slots and
+    // token halves; the peer issues none, and its warp of issuer 0 relays the
+    // completion of the peer's token-row copies to the leader instead.
     const int q = mma_q;
-    if (lane == 0 && q < parts) {
+    if (kPair && !leader && q == 0 && lane == 0) {
+      W4A16_PROF_DECL
+      RingPos bp;
+      const uint32_t leader_bf = map_to_cta(B.b_full, 0);
+      bool ok = true;
+      for (int it = unit0; it < items && ok; it += units) {
+        const ItemDesc d = decode_item<kRaster, kPair>(args, it, num_blocks, bpe, rank);
+        if (d.e < 0) continue;
+        for (int st = 0; st < n_stp; ++st, bp.next(BS)) {
+          W4A16_PROF_MARK(2);
+          if (!wait_phase(B.bf(bp.slot), bp.phase, abort_flag, status, kWhereRelay, tmo)) {
+            ok = false;
+            break;
+          }
+          W4A16_PROF_MARK(0);
+          mbar_arrive_remote_relaxed(leader_bf + 8u * bp.slot);
+          W4A16_PROF_MARK(1);
+        }
+      }
+      W4A16_PROF_MARK(2);
+      W4A16_PROF_STORE();
+    }
+    W4A16_PROF_DECL
+    if ((!kPair || leader) && lane == 0 && q < parts) {
       const IssuerPlan pl = issuer_plan(q, parts);
       RingPos ip, dp, ap, bp;
       ap.slot = pl.first;
       bp.slot = pl.first;
       bool ok = true;
       const uint64_t b_desc0 = smem_desc_sw128_kmajor(smem_u32(sm.b_ring));
-      for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
-        const ItemDesc d = decode_item<kRaster>(args, it, num_blocks, bpe);
+      for (int it = unit0; it < items && ok; it += units) {
+        const ItemDesc d = decode_item<kRaster, kPair>(args, it, num_blocks, bpe, rank);
         if (d.e < 0) continue;
         if (!wait_phase(B.itf(ip.slot), ip.phase, abort_flag, status, kWhereMmaItem, tmo)) {
           ok = false;
           break;
         }
         const int n16 = sm.info_n16[ip.slot];
-        if (!wait_phase(B.acce(dp.slot), dp.phase ^ 1, abort_flag, status, kWhereMmaAcc, tmo)) {
+        if (!wait_phase<kPair>(B.acce(dp.slot), dp.phase ^ 1, abort_flag, status, kWhereMmaAcc,
+                               tmo)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t idesc = idesc_bf16_m128(static_cast<uint32_t>(n16));
+        // a pair's MMA takes N/2 token rows from each CTA: N is the whole block
+        const uint32_t idesc = kPair ? idesc_bf16(256u, static_cast<uint32_t>(bm))
+                                     : idesc_bf16_m128(static_cast<uint32_t>(n16));
         const uint32_t d_tmem = tmem + d_col_base + (dp.slot * parts + q) * args.d_cols;
         uint32_t acc = 0;
         for (int st = pl.first; st < n_stp; st += pl.stride) {
-          if (!wait_phase(B.af(ap.slot), ap.phase, abort_flag, status, kWhereMmaA, tmo) ||
-              !wait_phase(B.bf(bp.slot), bp.phase, abort_flag, status, kWhereMmaB, tmo)) {
+          W4A16_PROF_MARK(5);
+          if (!wait_phase<kPair>(B.af(ap.slot), ap.phase, abort_flag, status, kWhereMmaA, tmo)) {
             ok = false;
             break;
           }
+          W4A16_PROF_MARK(2);
+          if (!wait_phase<kPair>(B.bf(bp.slot), bp.phase, abort_flag, status, kWhereMmaB, tmo)) {
+            ok = false;
+            break;
+          }
+          W4A16_PROF_MARK(3);
           tc_fence_after();
           for (int j = pl.j0; j <= pl.j1; ++j) {
             if (2 * st + j >= args.k_steps) break;
@@ -573,32 +679,54 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
               // +32 bytes of K per MMA inside the 128-byte swizzle row
-              mma_bf16_ts(d_tmem, a_tmem + kk * 8, b_desc + 2 * kk, idesc, acc);
+              if constexpr (kPair) {
+                mma_bf16_ts_pair(d_tmem, a_tmem + kk * 8, b_desc + 2 * kk, idesc, acc);
+              } else {
+                mma_bf16_ts(d_tmem, a_tmem + kk * 8, b_desc + 2 * kk, idesc, acc);
+              }
               acc = 1;
             }
           }
-          tc_commit(B.ae(ap.slot));
-          tc_commit(B.be(bp.slot));
+          W4A16_PROF_MARK(4);
+          if constexpr (kPair) {
+            // the slots are freed in both CTAs of the pair
+            tc_commit_pair_mc(B.ae(ap.slot), 0x3);
+            tc_commit_pair_mc(B.be(bp.slot), 0x3);
+          } else {
+            tc_commit(B.ae(ap.slot));
+            tc_commit(B.be(bp.slot));
+          }
           ap.advance(pl.stride, kASlots);
           bp.advance(pl.stride, BS);
+          W4A16_PROF_MARK(6);
         }
         if (!ok) break;
-        tc_commit(B.accf(dp.slot));
+        if constexpr (kPair) {
+          tc_commit_pair_mc(B.accf(dp.slot), 0x3);
+        } else {
+          tc_commit(B.accf(dp.slot));
+        }
         ip.next(kItemSlots);
         dp.next(args.d_slots);
       }
       // every MMA issued by this thread has finished once its final barrier flips
-      tc_commit(B.fin(q));
+      if constexpr (kPair) {
+        tc_commit_pair_mc(B.fin(q), 0x1);
+      } else {
+        tc_commit(B.fin(q));
+      }
       drain_phase(B.fin(q), 0, kDrainCycles);
     }
+    W4A16_PROF_MARK(5);
+    W4A16_PROF_STORE();
   } else if (warp == kWarpRouter) {
     // ======================= routing info, items ahead ======================
     // Resolves each item's rows (activation row, output row, top-k weight)
     // into the item ring up to kItemSlots items ahead, so that the global
     // loads of the routing tensors stay off the copy and MMA critical path.
     RingPos ip;
-    for (int it = blockIdx.x; it < items; it += gridDim.x) {
-      const ItemDesc d = decode_item<kRaster>(args, it, num_blocks, bpe);
+    for (int it = unit0; it < items; it += units) {
+      const ItemDesc d = decode_item<kRaster, kPair>(args, it, num_blocks, bpe, rank);
       if (d.e < 0) continue;
       if (!warp_wait_phase(B.ite(ip.slot), ip.phase ^ 1, abort_flag, status, kWhereRouter, tmo))
         break;
@@ -640,13 +768,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       RingPos bp;
       uint32_t issued = 0;  // stages whose b_full phase this thread started
       bool ok = true;
-      for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
-        const ItemDesc d = decode_item<kRaster>(args, it, num_blocks, bpe);
+      for (int it = unit0; it < items && ok; it += units) {
+        const ItemDesc d = decode_item<kRaster, kPair>(args, it, num_blocks, bpe, rank);
         if (d.e < 0) continue;
-        const int box_row = (args.family == kMasked) ? d.e * args.m + (d.blk - d.e * bpe) * bm
-                                                     : d.blk * bm;
+        // a pair's CTA loads its half of the block's rows
+        const int box_row = ((args.family == kMasked) ? d.e * args.m + (d.blk - d.e * bpe) * bm
+                                                      : d.blk * bm) +
+                            static_cast<int>(rank) * bm_local;
         for (int st = 0; st < n_stp; ++st, bp.next(BS)) {
-          if (!wait_phase(B.be(bp.slot), bp.phase ^ 1, abort_flag, status, kWhereGatherB, tmo)) {
+          if (!wait_phase<kPair>(B.be(bp.slot), bp.phase ^ 1, abort_flag, status, kWhereGatherB,
+                                 tmo)) {
             ok = false;
             break;
           }
@@ -687,14 +818,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t a_phase = 0;  // uses of A slot wg so far, mod 2
     int u = 0;             // global stage index of this CTA
     bool ok = true;
-    for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
-      const ItemDesc d = decode_item<kRaster>(args, it, num_blocks, bpe);
+    W4A16_PROF_DECL
+    for (int it = unit0; it < items && ok; it += units) {
+      const ItemDesc d = decode_item<kRaster, kPair>(args, it, num_blocks, bpe, rank);
       if (d.e < 0) continue;
       // item-local stages of this warpgroup: st = wg - u (mod 4), step 4
       for (int st = (wg - u) & 3; st < n_stp; st += 4) {
+        W4A16_PROF_MARK(4);
         ok = warp_wait_phase_backoff(B.wf(wp.slot), wp.phase, abort_flag, status, kWhereDequantW,
                                      tmo);
         if (!ok) break;
+        W4A16_PROF_MARK(0);
         const int nks = min(2, max(0, args.k_steps - 2 * st));
         const uint8_t* stp = sm.w_ring + static_cast<size_t>(wp.slot) * kWStageBytes;
         uint4 qv[2][2];
@@ -713,9 +847,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(B.we(wp.slot));
         wp.advance(4, WS);
         // the MMAs of this slot's previous use must be done before overwriting
-        ok = warp_wait_phase_backoff(B.ae(wg), a_phase ^ 1, abort_flag, status, kWhereDequantA,
-                                     tmo);
+        W4A16_PROF_MARK(1);
+        ok = warp_wait_phase_backoff<kPair>(B.ae(wg), a_phase ^ 1, abort_flag, status,
+                                            kWhereDequantA, tmo);
         if (!ok) break;
+        W4A16_PROF_MARK(2);
         tc_fence_after();
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
@@ -731,11 +867,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(B.af(wg));
+        W4A16_PROF_MARK(3);
+        if (lane == 0) {
+          // the pair's leader issues the MMAs: the peer's warps arrive there
+          if (kPair && !leader) {
+            mbar_arrive_remote_relaxed(map_to_cta(B.af(wg), 0));
+          } else {
+            mbar_arrive(B.af(wg));
+          }
+        }
         a_phase ^= 1u;
+        W4A16_PROF_MARK(5);
       }
       u += n_stp;
     }
+    W4A16_PROF_MARK(4);
+    W4A16_PROF_STORE();
   } else if (warp >= kWarpEpilogue0 && warp < kWarpEpilogue0 + 4) {
     // ======================= epilogue =======================================
     // Warp q reads TMEM lanes 32q..32q+31 (weight rows of the tile = output
@@ -753,14 +900,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int c4 = lane & 7;                            // 4-column group of this lane
     const int jr0 = lane >> 3;                          // first token row of this lane
     const bool vec4 = (args.n & 3) == 0;
+    // the accumulator slot is freed on the barrier of the CTA that issues the
+    // MMAs (the pair's leader)
+    auto release_acc = [&](uint32_t bar) {
+      if (kPair && !leader) {
+        mbar_arrive_remote_relaxed(map_to_cta(bar, 0));
+      } else {
+        mbar_arrive(bar);
+      }
+    };
     grid_dependency_wait();  // the previous grid may zero the output this one adds into
     RingPos ip, dp;
-    for (int it = blockIdx.x; it < items; it += gridDim.x) {
-      const ItemDesc d = decode_item<kRaster>(args, it, num_blocks, bpe);
+    for (int it = unit0; it < items; it += units) {
+      const ItemDesc d = decode_item<kRaster, kPair>(args, it, num_blocks, bpe, rank);
       if (d.e < 0) continue;
       const int islot = ip.slot;
       const int dslot = dp.slot;
-      if (!warp_wait_phase(B.accf(dslot), dp.phase, abort_flag, status, kWhereEpiAcc, tmo) ||
+      if (!warp_wait_phase<kPair>(B.accf(dslot), dp.phase, abort_flag, status, kWhereEpiAcc,
+                                  tmo) ||
           !warp_wait_phase(B.itf(islot), ip.phase, abort_flag, status, kWhereEpiItem, tmo))
         break;
       tc_fence_after();
@@ -830,7 +987,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (early) {
             tc_fence_before();
-            if (lane == 0) mbar_arrive(B.acce(dslot));
+            if (lane == 0) release_acc(B.acce(dslot));
           }
           for (int j0 = p0; j0 < p1; j0 += 16) {
             const float* slab = tile + (j0 - p0) * 32;
@@ -908,7 +1065,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!early) tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          if (!early) mbar_arrive(B.acce(dslot));
+          if (!early) release_acc(B.acce(dslot));
           mbar_arrive(B.ite(islot));
         }
       } else {
@@ -1049,7 +1206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(B.acce(dslot));
+          release_acc(B.acce(dslot));
           mbar_arrive(B.ite(islot));
         }
       }
@@ -1062,15 +1219,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncwarp();
   tc_fence_before();
   __syncthreads();
+  // a pair's leader may still read the peer's TMEM and shared memory until
+  // its issuers have drained: both CTAs leave together
+  if constexpr (kPair) cluster_sync_all();
   if (warp == kWarpMma0) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    if constexpr (kPair) {
+      tmem_dealloc_pair(tmem, kTmemCols);
+    } else {
+      tmem_dealloc(tmem, kTmemCols);
+    }
   }
 }
 
-size_t gemm_smem_bytes(int block_m, int w_stages, int b_stages) {
+size_t gemm_smem_bytes(int block_m, int w_stages, int b_stages, bool pair) {
   size_t off = 1024;  // alignment slack
-  off += static_cast<size_t>(b_stages) * 2 * block_m * 128;
+  // a CTA of a pair holds half of the block's token rows
+  off += static_cast<size_t>(b_stages) * 2 * (pair ? block_m / 2 : block_m) * 128;
   off += static_cast<size_t>(w_stages) * kWStageBytes;
   off += static_cast<size_t>(kItemSlots) * block_m * (4 + 4) + 2 * kItemSlots * 4;
   off = (off + 15) / 16 * 16 + epi_tile_bytes(block_m);
@@ -1160,24 +1325,67 @@ int device_sm_count(int device) {
   return cache[device];
 }
 
-cudaError_t launch_moe_gemm(const GemmArgs& args, int grid, bool dependent, cudaStream_t stream) {
-  // At least 118 KB so that two CTAs never share an SM: each CTA allocates
-  // all 512 TMEM columns.
-  size_t smem = gemm_smem_bytes(args.block_m, args.w_stages, args.b_stages);
-  if (smem < 118 * 1024) smem = 118 * 1024;
+template <bool kPair>
+void* pick_kernel(const GemmArgs& args) {
   const bool glu = args.out_mode == kOutGluBf16;
   const bool rows = args.out_mode == kOutF32Rows;
   // the whole-block staging tile exists for exactly these block sizes
   const bool early = epi_stage_rows(args.block_m) > 16;
   auto kernel =
-      rows ? (early ? w4a16_moe_gemm_kernel<false, false, true, true>
-                    : w4a16_moe_gemm_kernel<false, false, false, true>)
-      : glu ? (early ? w4a16_moe_gemm_kernel<true, false, true, false>
-                     : w4a16_moe_gemm_kernel<true, false, false, false>)
-      : args.raster_rows ? (early ? w4a16_moe_gemm_kernel<false, true, true, false>
-                                  : w4a16_moe_gemm_kernel<false, true, false, false>)
-                         : (early ? w4a16_moe_gemm_kernel<false, false, true, false>
-                                  : w4a16_moe_gemm_kernel<false, false, false, false>);
+      rows ? (early ? w4a16_moe_gemm_kernel<false, false, true, true, kPair>
+                    : w4a16_moe_gemm_kernel<false, false, false, true, kPair>)
+      : glu ? (early ? w4a16_moe_gemm_kernel<true, false, true, false, kPair>
+                     : w4a16_moe_gemm_kernel<true, false, false, false, kPair>)
+      : args.raster_rows ? (early ? w4a16_moe_gemm_kernel<false, true, true, false, kPair>
+                                  : w4a16_moe_gemm_kernel<false, true, false, false, kPair>)
+                         : (early ? w4a16_moe_gemm_kernel<false, false, true, false, kPair>
+                                  : w4a16_moe_gemm_kernel<false, false, false, false, kPair>);
+  return reinterpret_cast<void*>(kernel);
+}
+
+size_t launch_smem_bytes(const GemmArgs& args) {
+  // At least 118 KB so that two CTAs never share an SM: each CTA allocates
+  // all 512 TMEM columns.
+  size_t smem = gemm_smem_bytes(args.block_m, args.w_stages, args.b_stages, args.pair != 0);
+  return smem < 118 * 1024 ? 118 * 1024 : smem;
+}
+
+int max_pair_clusters(const GemmArgs& args) {
+  // CTA pairs that can be resident at once (a pair needs two SMs of one GPC)
+  static std::mutex mu;
+  static int cache[8][2] = {};
+  const bool early = epi_stage_rows(args.block_m) > 16;
+  const int key = (args.out_mode == kOutGluBf16 ? 4 : 0) + (args.raster_rows ? 2 : 0) + (early ? 1 : 0);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[key][0] != dev + 1) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = launch_smem_bytes(args);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    void* k = pick_kernel<true>(args);
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(cfg.dynamicSmemBytes)) != cudaSuccess ||
+        cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess)
+      return 0;
+    cache[key][0] = dev + 1;
+    cache[key][1] = n;
+  }
+  return cache[key][1];
+}
+
+cudaError_t launch_moe_gemm(const GemmArgs& args, int grid, bool dependent, cudaStream_t stream) {
+  const size_t smem = launch_smem_bytes(args);
+  void* kernel = args.pair ? pick_kernel<true>(args) : pick_kernel<false>(args);
   cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
@@ -1186,12 +1394,21 @@ cudaError_t launch_moe_gemm(const GemmArgs& args, int grid, bool dependent, cuda
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = dependent ? 1 : 0;
+  int nattr = 1;
+  if (args.pair) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    nattr = 2;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, args);
+  cfg.numAttrs = nattr;
+  void* params[] = {const_cast<GemmArgs*>(&args)};
+  return cudaLaunchKernelExC(&cfg, kernel, params);
 }
 
 }  // namespace w4a16

@@ -109,6 +109,63 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// ------------------------------------------------------------ clusters ---
+
+// Rank of this CTA in its cluster.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Shared-window address of the same location in CTA `cta` of the cluster.
+__device__ __forceinline__ uint32_t map_to_cta(uint32_t smem_addr, uint32_t cta) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(cta));
+  return r;
+}
+// Arrive once on an mbarrier of another CTA of the cluster (address from
+// map_to_cta), without release semantics: an arrive with release at cluster
+// scope was measured at about 1400 cycles on GB300, which throttled every
+// cross-CTA hand-off. Callers complete what the other CTA will read before
+// arriving (tcgen05.wait::st / wait::ld and tcgen05.fence::before_thread_sync
+// for TMEM, an observed tensor-copy completion for shared memory).
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+// try_wait that acquires at cluster scope: the phase may have been completed
+// by arrivals from another CTA of the cluster.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity,
+                                                      uint32_t suspend_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(suspend_ns)
+      : "memory");
+  return ok != 0;
+}
+// The same without a suspend hint: returns at once.
+__device__ __forceinline__ bool mbar_try_wait_cluster_now(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Every thread of both CTAs of the cluster (all threads must take part).
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // ------------------------------------------------ dependent launches ---
 
 // Wait until the grids this grid depends on (programmatic launch) have
@@ -138,6 +195,21 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
+// TMEM allocation of a CTA pair (cta_group::2): one warp of each of the two
+// CTAs executes it; both receive the same column address.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
 // D[tmem] (+)= A[tmem] x B[smem]^T, kind::f16 (BF16 inputs, FP32 accumulate),
 // one CTA. `accumulate` = 0 overwrites D.
 __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
@@ -147,6 +219,30 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// The same over a CTA pair (cta_group::2, M = 256): A rows 0..127 from this
+// CTA's TMEM and rows 128..255 from the peer's, at the same column address;
+// B columns 0..N/2-1 from this CTA's shared memory and N/2..N-1 from the
+// peer's, at the same address; D rows split like A. Issued by the pair's
+// even-ranked CTA.
+__device__ __forceinline__ void mma_bf16_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                 uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive once on the mbarrier at shared offset `bar` of each CTA of the pair
+// in `cta_mask` when the pair MMAs this thread issued have completed.
+__device__ __forceinline__ void tc_commit_pair_mc(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+      "[%0], %1;" ::"r"(bar),
+      "h"(cta_mask)
       : "memory");
 }
 
@@ -212,13 +308,14 @@ __device__ __forceinline__ uint64_t smem_desc_sw128_kmajor(uint32_t saddr) {
 }
 
 // Instruction descriptor of kind::f16: D fp32, A and B BF16, both K-major,
-// M = 128, N = n (multiple of 16, 16..256).
-__device__ __forceinline__ uint32_t idesc_bf16_m128(uint32_t n) {
+// M = m (128, or 256 for a CTA pair), N = n (multiple of 16, 16..256).
+__device__ __forceinline__ uint32_t idesc_bf16(uint32_t m, uint32_t n) {
   return (1u << 4)            // D format: F32
          | (1u << 7)          // A format: BF16
          | (1u << 10)         // B format: BF16
          | ((n >> 3) << 17)   // N >> 3
-         | ((128u >> 4) << 24);  // M >> 4
+         | ((m >> 4) << 24);  // M >> 4
 }
+__device__ __forceinline__ uint32_t idesc_bf16_m128(uint32_t n) { return idesc_bf16(128u, n); }
 
 }  // namespace w4a16

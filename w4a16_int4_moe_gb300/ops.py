@@ -52,7 +52,7 @@ class Plan(ctypes.Structure):
     """Mirror of w4a16_plan_t."""
     _fields_ = [(name, ctypes.c_int) for name in (
         "block_m", "bn", "bk", "stages", "b_stages", "split_k", "ctas_per_sm", "swap_ab",
-        "layout", "grid")]
+        "layout", "grid", "cta_pair")]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}
