@@ -350,6 +350,32 @@ def time_indexed_layer(layer, x, tokens, ids, w, out, flush, steps, warmup, laye
     return gu, dn, wall
 
 
+def time_single_launch(gu_glu, dn, p, x, ids, w, out, flush, device, steps, warmup):
+    """µs of the whole layer (gate_up, activation, down) in one GEMM launch
+    (w4a16_moe_layer, with its row permute), L2 flushed before every step."""
+    import torch
+    from w4a16_int4_moe_gb300 import moe as moe_mod
+    from w4a16_int4_moe_gb300 import ops
+    layer = moe_mod.W4A16MoE(gu_glu, dn, p.topk, p.tokens, tok_e_hint=p.tok_e_hint(),
+                             device=device, single_launch=True)
+    stream = torch.cuda.current_stream()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    for i in range(warmup + steps):
+        e = ev[i - warmup] if i >= warmup else None
+        flush.zero_()
+        layer.align(ids)
+        if e is not None:
+            e[0].record(stream)
+        layer.layer_single_launch(x, p.tokens, w, out)
+        if e is not None:
+            e[1].record(stream)
+    torch.cuda.synchronize()
+    st, word = ops.w4a16_read_device_status(layer.layer_workspace)
+    if st != ops.W4A16_OK:
+        raise SystemExit(f"device status {word:#x} in the single-launch layer")
+    return statistics.mean(e[0].elapsed_time(e[1]) * 1e3 for e in ev)
+
+
 def roofline_entry(bound, kernel, achieved, peak, nominal, peak_src, extra=None):
     unit = "GB/s" if bound == "hbm" else "TFLOP/s"
     d = {"bound": bound, "kernel": kernel, "achieved": achieved, "peak": peak, "unit": unit,
@@ -360,7 +386,7 @@ def roofline_entry(bound, kernel, achieved, peak, nominal, peak_src, extra=None)
     return d
 
 
-def indexed_config(name, packed, device, flush, steps, warmup, peaks):
+def indexed_config(name, packed, device, flush, steps, warmup, peaks, glu_packed=None):
     """One indexed configuration (TP8 or EP8 prefill) with the given packed
     weights {(n, k): PackedExperts}: gate_up and down µs, roofline."""
     import torch
@@ -381,6 +407,10 @@ def indexed_config(name, packed, device, flush, steps, warmup, peaks):
     if st != ops.W4A16_OK:
         raise SystemExit(f"device status {word:#x} in configuration {name}")
     g, d_ = statistics.mean(gu_us), statistics.mean(dn_us)
+    single_us = None
+    if glu_packed is not None:
+        single_us = time_single_launch(glu_packed, dn, p, x, ids, w, out, flush,
+                                       device, steps, warmup)
     hbm, tf, src = peaks
     tensor = name == "ep8_prefill"
     layer_us = g + d_
@@ -398,6 +428,7 @@ def indexed_config(name, packed, device, flush, steps, warmup, peaks):
             "steps": steps, "block_m": layer.block_m, "routed_rows": work["rows"],
             "active_experts": work["active_experts"],
             "gate_up_gbs": work["gate_up"]["bytes"] / (g * 1e-6) / 1e9,
+            "single_launch_layer_us": single_us,
             "tflops": total_f / (layer_us * 1e-6) / 1e12, "roofline": roof}
 
 
@@ -496,6 +527,7 @@ def run_configs(args, packed_ep8, device, flush, peaks):
     """The `configs` block: every other configuration, measured in this run."""
     import torch
     from w4a16_int4_moe_gb300 import moe as moe_mod
+    from w4a16_int4_moe_gb300 import ops
     steps = max(3, min(args.steps, 20))
     warmup = max(3, min(args.warmup, 5))
     res = {}
@@ -507,12 +539,15 @@ def run_configs(args, packed_ep8, device, flush, peaks):
             if tp8_packed is None:
                 q, s = device_weights(384, 512, 7168, 11, device)
                 gu = moe_mod.PackedExperts.from_checkpoint(q, s)
+                tp8_glu = moe_mod.PackedExperts.from_checkpoint(
+                    q, s, layout=ops.W4A16_LAYOUT_KTILE64_GLU16)
                 del q, s
                 q, s = device_weights(384, 7168, 256, 12, device)
                 dn = moe_mod.PackedExperts.from_checkpoint(q, s)
                 del q, s
                 tp8_packed = {(512, 7168): gu, (7168, 256): dn}
-            r = indexed_config(name, tp8_packed, device, flush, steps, warmup, peaks)
+            r = indexed_config(name, tp8_packed, device, flush, steps, warmup, peaks,
+                               glu_packed=tp8_glu)
         elif name == "ep8_prefill":
             r = indexed_config(name, packed, device, flush, steps, warmup, peaks)
         else:
@@ -606,12 +641,15 @@ def run_ours(args):
         st, word = ops.w4a16_read_device_status(layer_f.workspace)
         if st != ops.W4A16_OK:
             raise SystemExit(f"device status {word:#x} in the fused-activation layer")
+        single_us = time_single_launch(gu_glu, dn, p, x, ids, w, out, flush, device, nf,
+                                       args.warmup)
         fused = {
             "gate_up_silu_us": statistics.mean(e[0].elapsed_time(e[1]) * 1e3 for e in ev_f),
             "down_us": statistics.mean(e[1].elapsed_time(e[2]) * 1e3 for e in ev_f),
             "layer_with_act_us": statistics.mean(e[0].elapsed_time(e[2]) * 1e3 for e in ev_f),
             "unfused_layer_with_act_us": statistics.mean(e[3].elapsed_time(e[4]) * 1e3
                                                          for e in ev_f),
+            "single_launch_layer_us": single_us,
             "steps": nf,
         }
 
@@ -691,8 +729,11 @@ def run_ours(args):
         "gpu_launches": 6 * L * args.steps,
         "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
-                "call": "W4A16MoE.forward (align, gate_up with fused activation, down)"
-                        if layer_f is not None else "W4A16MoE.forward (align, gate_up, act, down)"},
+                "call": ("W4A16MoE.forward (align, then gate_up with the fused activation and "
+                         "down in one launch)" if layer_f is not None and layer_f.single_launch
+                         else "W4A16MoE.forward (align, gate_up with fused activation, down)"
+                         if layer_f is not None
+                         else "W4A16MoE.forward (align, gate_up, act, down)")},
         "clocks": clk,
         "fused_activation": fused,
         "configs": configs,

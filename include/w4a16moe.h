@@ -323,6 +323,53 @@ w4a16_status w4a16_silu_and_mul(const uint16_t* in, int rows, int inter, uint16_
 w4a16_status w4a16_read_device_status(void* workspace, int* detail, void* stream);
 
 /*
+ * Device workspace bytes of w4a16_moe_layer: 256 bytes of status words, the
+ * x rows in routing order (rows x roundup(hidden, 64) BF16), the activation
+ * rows in routing order (rows x inter BF16), one int32 completion counter per
+ * routing block; each part rounded up to 256 bytes. rows = the routing
+ * capacity.
+ */
+size_t w4a16_layer_workspace_size(const w4a16_plan_t* plan, int rows, int hidden, int inter);
+
+/*
+ * The whole expert pair of one MoE layer in a single GEMM launch: gate_up
+ * with the activation fused (W4A16_GATE_UP_SILU), then down with the top-k
+ * weighted scatter-add (W4A16_DOWN), over the same routing blocks ([P-arex]
+ * "调度由每个专家收到的 token 数决定": gate_up then down over sorted_ids /
+ * expert_ids / num_tokens_padded; the activation between them is the glue the
+ * pages leave out of the timed pair).
+ *   packed_gate_up  [num_experts, 2*inter, hidden] packed with
+ *                   W4A16_LAYOUT_KTILE64_GLU16 (plan->layout must say so);
+ *   packed_down     [num_experts, hidden, inter] packed with
+ *                   W4A16_LAYOUT_KTILE64;
+ *   x               BF16 [tokens, hidden]; topk_weights fp32 [tokens, topk];
+ *   out             FP32 [tokens, hidden]: zeroed first unless
+ *                   W4A16_FLAG_ACCUMULATE, then every token's top-k weighted
+ *                   down rows are added (in no fixed order).
+ * One persistent launch runs every gate_up work item, then every down work
+ * item; the down items of a routing block start once all gate_up items of the
+ * block (on any CTA) have written its activation rows to the workspace (a
+ * per-block counter in device memory, polled with a bounded wait). The
+ * result equals w4a16_moe_indexed_gemm(W4A16_GATE_UP_SILU) followed by
+ * w4a16_moe_indexed_gemm(W4A16_DOWN) up to the order of the FP32 additions.
+ * Requirements: inter % 64 == 0, hidden % 32 == 0 and hidden % 4 == 0
+ * (else W4A16_ERR_UNSUPPORTED); plan->cta_pair == 0; flags
+ * VALIDATE_ROUTING and ACCUMULATE only (else W4A16_ERR_INVALID_ARG); ws_bytes
+ * >= w4a16_layer_workspace_size(plan, capacity, hidden, inter) (else
+ * W4A16_ERR_WORKSPACE). Every CTA of the launch must be resident at once (it
+ * uses at most one CTA per SM); if the device is shared so that some cannot
+ * start, the waits run out and w4a16_read_device_status reports
+ * W4A16_ERR_TIMEOUT.
+ */
+w4a16_status w4a16_moe_layer(const void* packed_gate_up, const void* packed_down, int num_experts,
+                             int hidden, int inter, const uint16_t* x, int tokens, int topk,
+                             const int32_t* sorted_ids, const int32_t* expert_ids,
+                             const int32_t* num_tokens_padded, int capacity,
+                             const float* topk_weights, float* out, int flags,
+                             const w4a16_plan_t* plan, void* workspace, size_t ws_bytes,
+                             void* stream);
+
+/*
  * No-allocation variant of w4a16_moe_indexed_gemm. The pages have no
  * counterpart of this call; it exists for callers that cannot allocate
  * device memory when they call the operator: a host whose caching allocator

@@ -127,3 +127,49 @@ def test_gemm_from_pack_quantized_checkpoint(cuda_dev):
     pe = checkpoint.packed_experts_from_pack_quantized(words, scales)
     ref = ops.w4a16_prepack(dev(p.q_gu, cuda_dev), dev(p.s_gu.view(np.int16), cuda_dev))
     assert torch.equal(pe.packed, ref)
+
+
+# --------------------------------------------------- the single-launch layer --
+
+def _layers(p, device, single_bm=None):
+    def t(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+    gu = moe_mod.PackedExperts.from_checkpoint(t(p.q_gu), t(p.s_gu.view(np.int16)),
+                                               layout=ops.W4A16_LAYOUT_KTILE64_GLU16)
+    dn = moe_mod.PackedExperts.from_checkpoint(t(p.q_dn), t(p.s_dn.view(np.int16)))
+    two = moe_mod.W4A16MoE(gu, dn, p.topk, p.tokens, tok_e_hint=p.tok_e_hint(), device=device)
+    one = moe_mod.W4A16MoE(gu, dn, p.topk, p.tokens, tok_e_hint=p.tok_e_hint(), device=device,
+                           single_launch=True)
+    return two, one, t
+
+
+@pytest.mark.parametrize("maker", ["tiny", "ragged", "tp8_like"])
+def test_single_launch_layer_matches_two_launches_and_oracle(cuda_dev, maker):
+    # gate_up (fused activation) and down in one persistent launch: the same
+    # result as the two launches up to the order of the FP32 additions, and
+    # the oracle's layer on the same activation
+    if maker == "tiny":
+        p = wl.tiny(seed=81)
+    elif maker == "ragged":
+        p = wl.uniform_problem(77, 320, 192, 6, 3, seed=82)
+        p.topk_ids[::5, 0] = -1
+    else:
+        p = wl.uniform_problem(16, 1024, 256, 96, 8, seed=83)    # ~1.3 rows per expert
+    two, one, t = _layers(p, cuda_dev)
+    x = bf16_tensor(p.x, cuda_dev)
+    ids, w = t(p.topk_ids), t(p.topk_weights)
+    y2 = two.forward(x, ids, w)
+    y1 = one.forward(x, ids, w)
+    torch.cuda.synchronize()
+    for layer in (two, one):
+        ws = layer.layer_workspace if layer.single_launch else layer.workspace
+        st, word = ops.w4a16_read_device_status(ws)
+        assert st == ops.W4A16_OK, hex(word)
+    assert_close(y1.cpu().numpy(), y2.cpu().numpy(), f"{maker}: one launch vs two",
+                 rel_l2=1e-6, max_abs_frac=1e-5)
+    # the oracle's down pass on the activation both paths computed
+    routed = ((p.topk_ids >= 0) & (p.topk_ids < p.num_experts)).reshape(-1)
+    act_bits = bf16_bits(two.act_buf[: p.numel])
+    a = np.where(routed[:, None], act_bits, 0).astype(np.uint16)
+    y_ref = oracle.indexed_down(a, p.topk_ids, p.topk_weights, p.q_dn, p.s_dn)
+    assert_close(y1.cpu().numpy(), y_ref, f"{maker}: one launch vs oracle down")

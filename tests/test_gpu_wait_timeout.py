@@ -60,3 +60,31 @@ def test_expired_waits_are_reported_and_the_context_recovers(cuda_dev, monkeypat
     ref = oracle.indexed_gate_up(p.x, p.topk_ids, p.q_gu, p.s_gu)
     got = oracle.bf16_bits_to_f64(bf16_bits(out))
     assert_close(got[routed], ref[routed], "gate_up after a timed-out call")
+
+
+def test_single_launch_layer_wait_runs_out_and_recovers(cuda_dev, monkeypatch):
+    # the down items of the single-launch layer wait on a per-block counter
+    # raised by other CTAs: with the bound lowered, that wait (or another)
+    # gives up, the call reports it, and the next call is correct
+    from w4a16_int4_moe_gb300 import moe as moe_mod
+    p = wl.uniform_problem(128, 1024, 256, 8, 2, seed=44)
+
+    def t(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(cuda_dev)
+    gu = moe_mod.PackedExperts.from_checkpoint(t(p.q_gu), t(p.s_gu.view(np.int16)),
+                                               layout=ops.W4A16_LAYOUT_KTILE64_GLU16)
+    dn = moe_mod.PackedExperts.from_checkpoint(t(p.q_dn), t(p.s_dn.view(np.int16)))
+    layer = moe_mod.W4A16MoE(gu, dn, p.topk, p.tokens, device=cuda_dev, single_launch=True)
+    x, ids, w = bf16_tensor(p.x, cuda_dev), t(p.topk_ids), t(p.topk_weights)
+    monkeypatch.setenv("W4A16_WAIT_TIMEOUT_CYCLES", "500")
+    layer.forward(x, ids, w)
+    st, word = ops.w4a16_read_device_status(layer.layer_workspace)
+    assert st == ops.W4A16_ERR_TIMEOUT, (st, hex(word))
+    assert word & 0x1000 and 1 <= (word & 0xFF) <= 15, hex(word)
+    monkeypatch.delenv("W4A16_WAIT_TIMEOUT_CYCLES")
+    y = layer.forward(x, ids, w)
+    st, word = ops.w4a16_read_device_status(layer.layer_workspace)
+    assert st == ops.W4A16_OK, hex(word)
+    ref = moe_mod.W4A16MoE(gu, dn, p.topk, p.tokens, device=cuda_dev).forward(x, ids, w)
+    assert_close(y.cpu().numpy(), ref.cpu().numpy(), "layer after a timed-out call",
+                 rel_l2=1e-6, max_abs_frac=1e-5)

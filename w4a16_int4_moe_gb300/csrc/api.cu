@@ -90,6 +90,33 @@ void set_ring_depths(w4a16_plan_t* p) {
   }
 }
 
+// Trusted-routing validation off keeps a call capturable; on, the routing is
+// copied back (after a stream synchronisation) and checked here.
+w4a16_status validate_routing(const int32_t* sorted_ids, const int32_t* expert_ids,
+                              const int32_t* num_tokens_padded, int capacity, int bm,
+                              long long numel, int num_experts, cudaStream_t s) {
+  if (cudaStreamSynchronize(s) != cudaSuccess) return W4A16_ERR_CUDA;
+  int ntp = 0;
+  if (cudaMemcpy(&ntp, num_tokens_padded, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return W4A16_ERR_CUDA;
+  if (ntp < 0 || ntp > capacity || ntp % bm != 0) return W4A16_ERR_ROUTING;
+  std::vector<int32_t> eid(ntp / bm), sid(ntp);
+  if (ntp > 0) {
+    if (cudaMemcpy(eid.data(), expert_ids, eid.size() * 4, cudaMemcpyDeviceToHost) !=
+            cudaSuccess ||
+        cudaMemcpy(sid.data(), sorted_ids, sid.size() * 4, cudaMemcpyDeviceToHost) != cudaSuccess)
+      return W4A16_ERR_CUDA;
+  }
+  for (size_t b = 0; b < eid.size(); ++b) {
+    if (eid[b] < -1 || eid[b] >= num_experts) return W4A16_ERR_ROUTING;
+    for (int j = 0; j < bm; ++j) {
+      const int id = sid[b * bm + j];
+      if (id < 0 || id > numel) return W4A16_ERR_ROUTING;
+    }
+  }
+  return W4A16_OK;
+}
+
 int current_sm_count() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -288,28 +315,9 @@ w4a16_status indexed_gemm(int mode, const void* packed, int num_experts, int n, 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   if (flags & W4A16_FLAG_VALIDATE_ROUTING) {
-    // Trusted-routing validation off keeps the call capturable; on, the
-    // routing is copied back and checked here.
-    if (cudaStreamSynchronize(s) != cudaSuccess) return W4A16_ERR_CUDA;
-    int ntp = 0;
-    if (cudaMemcpy(&ntp, num_tokens_padded, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
-      return W4A16_ERR_CUDA;
-    if (ntp < 0 || ntp > capacity || ntp % bm != 0) return W4A16_ERR_ROUTING;
-    std::vector<int32_t> eid(ntp / bm), sid(ntp);
-    if (ntp > 0) {
-      if (cudaMemcpy(eid.data(), expert_ids, eid.size() * 4, cudaMemcpyDeviceToHost) !=
-              cudaSuccess ||
-          cudaMemcpy(sid.data(), sorted_ids, sid.size() * 4, cudaMemcpyDeviceToHost) !=
-              cudaSuccess)
-        return W4A16_ERR_CUDA;
-    }
-    for (size_t b = 0; b < eid.size(); ++b) {
-      if (eid[b] < -1 || eid[b] >= num_experts) return W4A16_ERR_ROUTING;
-      for (int j = 0; j < bm; ++j) {
-        const int id = sid[b * bm + j];
-        if (id < 0 || id > numel) return W4A16_ERR_ROUTING;
-      }
-    }
+    const w4a16_status vs = validate_routing(sorted_ids, expert_ids, num_tokens_padded, capacity,
+                                             bm, numel, num_experts, s);
+    if (vs != W4A16_OK) return vs;
   }
   // every check passed: only now may anything be enqueued. The library's
   // own scratch array keeps what the previous call left: its status word is
@@ -540,6 +548,127 @@ w4a16_status w4a16_silu_and_mul(const uint16_t* in, int rows, int inter, uint16_
   if (rows > 0 && (in == nullptr || out == nullptr)) return W4A16_ERR_INVALID_ARG;
   if (rows > 0 && (!aligned16(in) || !aligned16(out))) return W4A16_ERR_INVALID_ARG;
   return cuda_status(launch_silu_and_mul(in, rows, inter, out, static_cast<cudaStream_t>(stream)));
+}
+
+size_t w4a16_layer_workspace_size(const w4a16_plan_t* plan, int rows, int hidden, int inter) {
+  if (plan == nullptr || plan->block_m <= 0 || rows <= 0 || hidden <= 0 || inter <= 0)
+    return kStatusBytes;
+  const size_t flags_bytes = (static_cast<size_t>(rows / plan->block_m + 1) * 4 + 255) / 256 * 256;
+  return kStatusBytes + (permuted_bytes(rows, hidden) + 255) / 256 * 256 +
+         (permuted_bytes(rows, inter) + 255) / 256 * 256 + flags_bytes;
+}
+
+w4a16_status w4a16_moe_layer(const void* packed_gate_up, const void* packed_down, int num_experts,
+                             int hidden, int inter, const uint16_t* x, int tokens, int topk,
+                             const int32_t* sorted_ids, const int32_t* expert_ids,
+                             const int32_t* num_tokens_padded, int capacity,
+                             const float* topk_weights, float* out, int flags,
+                             const w4a16_plan_t* plan, void* workspace, size_t ws_bytes,
+                             void* stream) {
+  if (num_experts <= 0 || hidden <= 0 || inter <= 0 || tokens < 0 || topk <= 0 || capacity < 0)
+    return W4A16_ERR_INVALID_ARG;
+  if (hidden % kGroup != 0 || inter % 64 != 0 || hidden % 4 != 0) return W4A16_ERR_UNSUPPORTED;
+  if (plan == nullptr || packed_gate_up == nullptr || packed_down == nullptr || out == nullptr ||
+      sorted_ids == nullptr || expert_ids == nullptr || num_tokens_padded == nullptr)
+    return W4A16_ERR_INVALID_ARG;
+  if (tokens > 0 && (x == nullptr || topk_weights == nullptr)) return W4A16_ERR_INVALID_ARG;
+  if ((flags & ~(W4A16_FLAG_VALIDATE_ROUTING | W4A16_FLAG_ACCUMULATE)) != 0)
+    return W4A16_ERR_INVALID_ARG;
+  if (!aligned16(packed_gate_up) || !aligned16(packed_down) || !aligned16(out) ||
+      (x != nullptr && !aligned16(x)))
+    return W4A16_ERR_INVALID_ARG;
+  // the gate_up weights carry the interleaved gate/up packing of the fused
+  // activation; the layer runs unpaired
+  if (plan->layout != W4A16_LAYOUT_KTILE64_GLU16 || plan->cta_pair != 0)
+    return W4A16_ERR_INVALID_ARG;
+  Pipeline pl;
+  if (!plan_pipeline(*plan, std::max(hidden, inter), &pl)) return W4A16_ERR_INVALID_ARG;
+  const int bm = plan->block_m;
+  if (capacity % bm != 0) return W4A16_ERR_INVALID_ARG;
+  const long long numel = static_cast<long long>(tokens) * topk;
+  if (numel >= (1LL << 30)) return W4A16_ERR_UNSUPPORTED;
+  if (workspace == nullptr || ws_bytes < w4a16_layer_workspace_size(plan, capacity, hidden, inter))
+    return W4A16_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (flags & W4A16_FLAG_VALIDATE_ROUTING) {
+    const w4a16_status vs = validate_routing(sorted_ids, expert_ids, num_tokens_padded, capacity,
+                                             bm, numel, num_experts, s);
+    if (vs != W4A16_OK) return vs;
+  }
+  const size_t zero_bytes = (flags & W4A16_FLAG_ACCUMULATE)
+                                ? 0
+                                : static_cast<size_t>(tokens) * hidden * sizeof(float);
+  if (numel == 0 || capacity == 0) {
+    if (zero_bytes > 0 && cudaMemsetAsync(out, 0, zero_bytes, s) != cudaSuccess)
+      return W4A16_ERR_CUDA;
+    return W4A16_OK;
+  }
+  const int sms = current_sm_count();
+  if (sms <= 0) return W4A16_ERR_CUDA;
+  // workspace: status words, x rows in routing order, activation rows in
+  // routing order, one completion counter per routing block
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint16_t* x_sorted = reinterpret_cast<uint16_t*>(ws + kStatusBytes);
+  uint16_t* act_sorted = reinterpret_cast<uint16_t*>(
+      ws + kStatusBytes + (permuted_bytes(capacity, hidden) + 255) / 256 * 256);
+  int* block_done = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(act_sorted) +
+                                           (permuted_bytes(capacity, inter) + 255) / 256 * 256);
+  const int blocks = capacity / bm;
+  GemmArgs g;
+  std::memset(&g, 0, sizeof(g));
+  g.wpack = static_cast<const uint8_t*>(packed_gate_up);
+  g.expert_bytes = static_cast<long long>(packed_expert_bytes(2 * inter, hidden));
+  g.num_experts = num_experts;
+  g.n = 2 * inter;
+  g.k = hidden;
+  g.n_tiles = packed_tiles(2 * inter);
+  g.k_steps = packed_ksteps(hidden);
+  g.wpack2 = static_cast<const uint8_t*>(packed_down);
+  g.expert_bytes2 = static_cast<long long>(packed_expert_bytes(hidden, inter));
+  g.n2 = hidden;
+  g.n_tiles2 = packed_tiles(hidden);
+  g.k_steps2 = packed_ksteps(inter);
+  if (!encode_permuted_tmap(&g.tmap, x_sorted, capacity, permuted_row_elems(hidden), bm) ||
+      !encode_permuted_tmap(&g.tmap2, act_sorted, capacity, inter, bm))
+    return W4A16_ERR_CUDA;
+  if (cudaMemsetAsync(block_done, 0, static_cast<size_t>(blocks) * 4, s) != cudaSuccess)
+    return W4A16_ERR_CUDA;
+  const size_t zero_vec_bytes = zero_bytes / 16 * 16;
+  if (zero_bytes != zero_vec_bytes &&
+      cudaMemsetAsync(reinterpret_cast<uint8_t*>(out) + zero_vec_bytes, 0,
+                      zero_bytes - zero_vec_bytes, s) != cudaSuccess)
+    return W4A16_ERR_CUDA;
+  if (launch_permute_rows(x, hidden, topk, static_cast<int>(numel), sorted_ids, num_tokens_padded,
+                          capacity, x_sorted, out, zero_vec_bytes, sms, s) != cudaSuccess)
+    return W4A16_ERR_CUDA;
+  g.act = x_sorted;
+  g.gather_rows = 1;
+  g.act_rows = capacity;
+  g.family = kIndexed;
+  g.out_mode = kOutGluBf16;
+  g.sorted_ids = sorted_ids;
+  g.expert_ids = expert_ids;
+  g.num_tokens_padded = num_tokens_padded;
+  g.capacity = capacity;
+  g.numel = static_cast<int>(numel);
+  g.a_div = topk;
+  g.o_div = topk;
+  g.topk_weights = topk_weights;
+  g.block_m = bm;
+  g.out = act_sorted;
+  g.out2 = out;
+  g.block_done = block_done;
+  g.layer = 1;
+  g.status = static_cast<int*>(workspace);
+  fill_pipeline(pl, &g);
+  g.timeout_cycles = wait_timeout_cycles();
+  long long grid = plan->grid > 0 ? plan->grid : static_cast<long long>(sms) * plan->ctas_per_sm;
+  // every CTA must be resident at once (down items wait on other CTAs'
+  // gate_up items): at most one CTA per SM
+  grid = std::max<long long>(1, std::min<long long>(grid, sms));
+  grid = std::min<long long>(grid, static_cast<long long>(blocks) * (g.n_tiles + g.n_tiles2));
+  if (launch_moe_gemm(g, static_cast<int>(grid), true, s) != cudaSuccess) return W4A16_ERR_CUDA;
+  return W4A16_OK;
 }
 
 w4a16_status w4a16_read_device_status(void* workspace, int* detail, void* stream) {

@@ -98,6 +98,18 @@ struct GemmArgs {
   // 1: CTA pairs (clusters of 2) issue M = 256 MMAs over two weight tiles;
   // needs an even tile count and block_m a multiple of 32; grid even
   int pair;
+  // the single-launch layer (w4a16_moe_layer): after the gate_up items (out =
+  // the activation rows at their routing positions) come the down items of
+  // the same routing blocks, with their own packed weights, reduction length
+  // (k_steps2), width n2, activation map (tmap2) and FP32 output (out2); a
+  // block's down items wait until block_done[block] reaches 4 * n_tiles
+  const uint8_t* wpack2;
+  long long expert_bytes2;
+  int n2, n_tiles2, k_steps2;
+  CUtensorMap tmap2;
+  float* out2;
+  int* block_done;
+  int layer;
   long long timeout_cycles;
 };
 

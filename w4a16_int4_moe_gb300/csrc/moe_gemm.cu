@@ -118,7 +118,8 @@ constexpr int kWarpRouter = 26;     // per-item routing info, items ahead of the
 enum Where {
   kWhereProducer = 1, kWhereDequantW = 2, kWhereDequantA = 3, kWhereGatherItem = 4,
   kWhereGatherB = 5, kWhereMmaItem = 6, kWhereMmaAcc = 7, kWhereMmaA = 8, kWhereMmaB = 9,
-  kWhereEpiAcc = 10, kWhereEpiItem = 11, kWhereDrain = 12, kWhereRouter = 13, kWhereRelay = 14
+  kWhereEpiAcc = 10, kWhereEpiItem = 11, kWhereDrain = 12, kWhereRouter = 13, kWhereRelay = 14,
+  kWhereBlockDone = 15
 };
 
 struct Smem {
@@ -177,6 +178,26 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
       if (status != nullptr) atomicCAS(status, 0, 0x1000 | where);
       return false;
     }
+  }
+}
+
+// Bounded wait until the counter at `flag` (global memory, raised by other
+// CTAs) reaches `target`; acquires at GPU scope. False when the CTA is
+// aborting or the wait ran out (then it starts the abort).
+__device__ __forceinline__ bool wait_count(const int* flag, int target, volatile int* abort_flag,
+                                           int* status, int where, long long timeout) {
+  const long long t0 = clock64();
+  while (true) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    if (v >= target) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > timeout) {
+      *abort_flag = 1;
+      if (status != nullptr) atomicCAS(status, 0, 0x1000 | where);
+      return false;
+    }
+    __nanosleep(256);
   }
 }
 
@@ -286,6 +307,7 @@ __device__ __forceinline__ IssuerPlan issuer_plan(int q, int parts) {
 
 struct ItemDesc {
   int blk, tile, e;
+  int phase;  // the single-launch layer: 0 gate_up, 1 down (else 0)
 };
 
 // Which routing block and weight tile item `it` is, and its expert (-1: skip).
@@ -299,11 +321,26 @@ struct ItemDesc {
 // kernel measurable time on short items (instruction footprint).
 constexpr int kRasterBlocks = 8;
 
-template <bool kRaster, bool kPair>
+template <bool kRaster, bool kPair, bool kLayer>
 __device__ __forceinline__ ItemDesc decode_item(const GemmArgs& a, int it, int num_blocks,
                                                 int blocks_per_expert, uint32_t rank) {
   ItemDesc d;
-  if constexpr (kRaster) {
+  d.phase = 0;
+  if constexpr (kLayer) {
+    // the single-launch layer: every gate_up item, then every down item, each
+    // list block-major, so that a block's activation rows are complete early
+    // and the down items of early blocks can fill the gate_up tail
+    const int items_gu = num_blocks * a.n_tiles;
+    if (it < items_gu) {
+      d.blk = it / a.n_tiles;
+      d.tile = it - d.blk * a.n_tiles;
+    } else {
+      const int j = it - items_gu;
+      d.phase = 1;
+      d.blk = j / a.n_tiles2;
+      d.tile = j - d.blk * a.n_tiles2;
+    }
+  } else if constexpr (kRaster) {
     const int per_group = kRasterBlocks * (kPair ? a.n_tiles >> 1 : a.n_tiles);
     const int group = it / per_group;
     const int rem = it - group * per_group;
@@ -336,7 +373,7 @@ __device__ __forceinline__ ItemDesc decode_item(const GemmArgs& a, int it, int n
 // weight of the down pass.
 // kRows (the deterministic down pass): the output row is the routing
 // position itself.
-template <bool kRows>
+template <bool kRows, bool kLayer>
 __device__ __forceinline__ void row_info(const GemmArgs& a, const ItemDesc& d, int j, int& dst,
                                          float& wt) {
   dst = -1;
@@ -345,7 +382,17 @@ __device__ __forceinline__ void row_info(const GemmArgs& a, const ItemDesc& d, i
     const long long pos = static_cast<long long>(d.blk) * a.block_m + j;
     const int id = __ldg(a.sorted_ids + pos);
     if (id >= 0 && id < a.numel) {
-      if constexpr (kRows) {
+      if constexpr (kLayer) {
+        // gate_up: activation rows at their routing positions; down: the
+        // top-k weighted add into the token's row
+        if (d.phase == 0) {
+          dst = static_cast<int>(pos);
+          wt = 1.f;
+        } else {
+          dst = id / a.o_div;
+          wt = __ldg(a.topk_weights + id);
+        }
+      } else if constexpr (kRows) {
         dst = static_cast<int>(pos);
         wt = __ldg(a.topk_weights + id);
       } else {
@@ -412,10 +459,11 @@ __device__ __forceinline__ void dequant_group(const uint4 q, uint32_t scale_bits
 // grouped item order, and kEarly: the epilogue that frees the accumulator
 // slot before its stores (blocks of 48 or 64 rows, whose accumulators fill
 // TMEM's single slot), and kRows: the deterministic down pass (out_mode
-// kOutF32Rows) are compiled into their own instantiations so that they cannot
-// change the register allocation or the instruction footprint of the plain
-// kernel.
-template <bool kGlu, bool kRaster, bool kEarly, bool kRows, bool kPair>
+// kOutF32Rows), kPair: the CTA-pair kernel, and kLayer: the single-launch
+// layer (gate_up items, then down items) are compiled into their own
+// instantiations so that they cannot change the register allocation or the
+// instruction footprint of the plain kernel.
+template <bool kGlu, bool kRaster, bool kEarly, bool kRows, bool kPair, bool kLayer = false>
 __global__ void __launch_bounds__(kThreads, 1)
     w4a16_moe_gemm_kernel(const __grid_constant__ GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
@@ -552,12 +600,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     bpe = (args.m + bm - 1) / bm;
     num_blocks = args.num_experts * bpe;
   }
-  const int items = num_blocks * (kPair ? args.n_tiles >> 1 : args.n_tiles);
+  const int items = kLayer ? num_blocks * (args.n_tiles + args.n_tiles2)
+                           : num_blocks * (kPair ? args.n_tiles >> 1 : args.n_tiles);
   // TMEM columns: the kASlots A slots (64 columns each), then per accumulator
   // slot the `parts` partial accumulators, d_cols each.
   const int d_col_base = kASlots * kAColsPerSlot;
   const int n_st = (args.k_steps + 1) / 2;  // stages holding data
   const int n_stp = n_st + (n_st & 1);      // stages per item (even)
+  // the single-launch layer's down items: their own reduction length
+  const int n_st2 = kLayer ? (args.k_steps2 + 1) / 2 : n_st;
+  const int n_stp2 = kLayer ? n_st2 + (n_st2 & 1) : n_stp;
+  // reduction steps and stages of an item (the layer's down items differ)
+  auto ksteps_of = [&](const ItemDesc& d) { return (kLayer && d.phase) ? args.k_steps2 : args.k_steps; };
+  auto nstp_of = [&](const ItemDesc& d) { return (kLayer && d.phase) ? n_stp2 : n_stp; };
   const long long tmo = args.timeout_cycles;
   volatile int* abort_flag = sm.abort_flag;
   int* status = args.status;
@@ -571,16 +626,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       RingPos wp;
       bool ok = true;
       for (int it = unit0; it < items && ok; it += units) {
-        const ItemDesc d = decode_item<kRaster, kPair>(args, it, num_blocks, bpe, rank);
+        const ItemDesc d = decode_item<kRaster, kPair, kLayer>(args, it, num_blocks, bpe, rank);
         if (d.e < 0) continue;
-        const uint8_t* src = args.wpack + static_cast<long long>(d.e) * args.expert_bytes +
-                             static_cast<long long>(d.tile) * args.k_steps * kStepBytes;
-        for (int st = 0; st < n_stp; ++st, wp.next(WS)) {
+        const int ks = ksteps_of(d);
+        const uint8_t* wbase = (kLayer && d.phase) ? args.wpack2 : args.wpack;
+        const long long ebytes = (kLayer && d.phase) ? args.expert_bytes2 : args.expert_bytes;
+        const uint8_t* src = wbase + static_cast<long long>(d.e) * ebytes +
+                             static_cast<long long>(d.tile) * ks * kStepBytes;
+        const int nst_i = nstp_of(d);
+        for (int st = 0; st < nst_i; ++st, wp.next(WS)) {
           if (!wait_phase(B.we(wp.slot), wp.phase ^ 1, abort_flag, status, kWhereProducer, tmo)) {
             ok = false;
             break;
           }
-          const int nks = min(2, max(0, args.k_steps - 2 * st));
+          const int nks = min(2, max(0, ks - 2 * st));
           if (nks > 0) {
             const uint32_t bytes = static_cast<uint32_t>(nks * kStepBytes);
             mbar_arrive_expect_tx(B.wf(wp.slot), bytes);
@@ -614,9 +673,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t leader_bf = map_to_cta(B.b_full, 0);
       bool ok = true;
       for (int it = unit0; it < items && ok; it += units) {
-        const ItemDesc d = decode_item<kRaster, kPair>(args, it, num_blocks, bpe, rank);
+        const ItemDesc d = decode_item<kRaster, kPair, kLayer>(args, it, num_blocks, bpe, rank);
         if (d.e < 0) continue;
-        for (int st = 0; st < n_stp; ++st, bp.next(BS)) {
+        const int nst_i = nstp_of(d);
+        for (int st = 0; st < nst_i; ++st, bp.next(BS)) {
           W4A16_PROF_MARK(2);
           if (!wait_phase(B.bf(bp.slot), bp.phase, abort_flag, status, kWhereRelay, tmo)) {
             ok = false;
@@ -639,7 +699,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       const uint64_t b_desc0 = smem_desc_sw128_kmajor(smem_u32(sm.b_ring));
       for (int it = unit0; it < items && ok; it += units) {
-        const ItemDesc d = decode_item<kRaster, kPair>(args, it, num_blocks, bpe, rank);
+        const ItemDesc d = decode_item<kRaster, kPair, kLayer>(args, it, num_blocks, bpe, rank);
         if (d.e < 0) continue;
         if (!wait_phase(B.itf(ip.slot), ip.phase, abort_flag, status, kWhereMmaItem, tmo)) {
           ok = false;
@@ -657,7 +717,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      : idesc_bf16_m128(static_cast<uint32_t>(n16));
         const uint32_t d_tmem = tmem + d_col_base + (dp.slot * parts + q) * args.d_cols;
         uint32_t acc = 0;
-        for (int st = pl.first; st < n_stp; st += pl.stride) {
+        const int ks = ksteps_of(d);
+        const int nst_i = nstp_of(d);
+        for (int st = pl.first; st < nst_i; st += pl.stride) {
           W4A16_PROF_MARK(5);
           if (!wait_phase<kPair>(B.af(ap.slot), ap.phase, abort_flag, status, kWhereMmaA, tmo)) {
             ok = false;
@@ -671,7 +733,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           W4A16_PROF_MARK(3);
           tc_fence_after();
           for (int j = pl.j0; j <= pl.j1; ++j) {
-            if (2 * st + j >= args.k_steps) break;
+            if (2 * st + j >= ks) break;
             // slot and k-step offsets are multiples of 1024 bytes
             const uint64_t b_desc =
                 b_desc0 + ((static_cast<uint32_t>(bp.slot) * b_stage_bytes + j * b_step_bytes) >> 4);
@@ -726,7 +788,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // loads of the routing tensors stay off the copy and MMA critical path.
     RingPos ip;
     for (int it = unit0; it < items; it += units) {
-      const ItemDesc d = decode_item<kRaster, kPair>(args, it, num_blocks, bpe, rank);
+      const ItemDesc d = decode_item<kRaster, kPair, kLayer>(args, it, num_blocks, bpe, rank);
       if (d.e < 0) continue;
       if (!warp_wait_phase(B.ite(ip.slot), ip.phase ^ 1, abort_flag, status, kWhereRouter, tmo))
         break;
@@ -736,7 +798,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = lane; j < bm; j += 32) {
         int dd;
         float w;
-        row_info<kRows>(args, d, j, dd, w);
+        row_info<kRows, kLayer>(args, d, j, dd, w);
         idst[j] = dd;
         iwt[j] = w;
         if (dd >= 0) maxj = j;
@@ -769,25 +831,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t issued = 0;  // stages whose b_full phase this thread started
       bool ok = true;
       for (int it = unit0; it < items && ok; it += units) {
-        const ItemDesc d = decode_item<kRaster, kPair>(args, it, num_blocks, bpe, rank);
+        const ItemDesc d = decode_item<kRaster, kPair, kLayer>(args, it, num_blocks, bpe, rank);
         if (d.e < 0) continue;
         // a pair's CTA loads its half of the block's rows
         const int box_row = ((args.family == kMasked) ? d.e * args.m + (d.blk - d.e * bpe) * bm
                                                       : d.blk * bm) +
                             static_cast<int>(rank) * bm_local;
-        for (int st = 0; st < n_stp; ++st, bp.next(BS)) {
+        const CUtensorMap* tmap = &args.tmap;
+        if (kLayer && d.phase) {
+          // the layer's down item reads the block's activation rows, written
+          // by the gate_up items of this launch (any CTA): wait until all of
+          // them are out (4 epilogue warps per gate_up tile), then order the
+          // tensor copies after what the wait observed
+          if (!wait_count(args.block_done + d.blk, 4 * args.n_tiles, abort_flag, status,
+                          kWhereBlockDone, tmo)) {
+            ok = false;
+            break;
+          }
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+          tmap = &args.tmap2;
+        }
+        const int ks = ksteps_of(d);
+        const int nst_i = nstp_of(d);
+        for (int st = 0; st < nst_i; ++st, bp.next(BS)) {
           if (!wait_phase<kPair>(B.be(bp.slot), bp.phase ^ 1, abort_flag, status, kWhereGatherB,
                                  tmo)) {
             ok = false;
             break;
           }
-          const int nks = min(2, max(0, args.k_steps - 2 * st));
+          const int nks = min(2, max(0, ks - 2 * st));
           const uint32_t dst = smem_u32(sm.b_ring + static_cast<size_t>(bp.slot) * b_stage_bytes);
           if (nks == 0) {
             mbar_arrive(B.bf(bp.slot));  // pad stage: no data
           } else if (gather) {
             mbar_arrive_expect_tx(B.bf(bp.slot), b_stage_bytes);
-            tma_load_3d(dst, &args.tmap, 0, box_row, 2 * st, B.bf(bp.slot));
+            tma_load_3d(dst, tmap, 0, box_row, 2 * st, B.bf(bp.slot));
           } else {
             mbar_arrive_expect_tx(B.bf(bp.slot), nks * b_step_bytes);
             for (int j = 0; j < nks; ++j)
@@ -820,16 +898,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     W4A16_PROF_DECL
     for (int it = unit0; it < items && ok; it += units) {
-      const ItemDesc d = decode_item<kRaster, kPair>(args, it, num_blocks, bpe, rank);
+      const ItemDesc d = decode_item<kRaster, kPair, kLayer>(args, it, num_blocks, bpe, rank);
       if (d.e < 0) continue;
+      const int ks = ksteps_of(d);
+      const int nst_i = nstp_of(d);
       // item-local stages of this warpgroup: st = wg - u (mod 4), step 4
-      for (int st = (wg - u) & 3; st < n_stp; st += 4) {
+      for (int st = (wg - u) & 3; st < nst_i; st += 4) {
         W4A16_PROF_MARK(4);
         ok = warp_wait_phase_backoff(B.wf(wp.slot), wp.phase, abort_flag, status, kWhereDequantW,
                                      tmo);
         if (!ok) break;
         W4A16_PROF_MARK(0);
-        const int nks = min(2, max(0, args.k_steps - 2 * st));
+        const int nks = min(2, max(0, ks - 2 * st));
         const uint8_t* stp = sm.w_ring + static_cast<size_t>(wp.slot) * kWStageBytes;
         uint4 qv[2][2];
         uint32_t sc[2][2];
@@ -879,7 +959,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         a_phase ^= 1u;
         W4A16_PROF_MARK(5);
       }
-      u += n_stp;
+      u += nst_i;
     }
     W4A16_PROF_MARK(4);
     W4A16_PROF_STORE();
@@ -912,7 +992,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     grid_dependency_wait();  // the previous grid may zero the output this one adds into
     RingPos ip, dp;
     for (int it = unit0; it < items; it += units) {
-      const ItemDesc d = decode_item<kRaster, kPair>(args, it, num_blocks, bpe, rank);
+      const ItemDesc d = decode_item<kRaster, kPair, kLayer>(args, it, num_blocks, bpe, rank);
       if (d.e < 0) continue;
       const int islot = ip.slot;
       const int dslot = dp.slot;
@@ -1069,12 +1149,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(B.ite(islot));
         }
       } else {
+        const int live = kLayer ? min(parts, ksteps_of(d)) : live_parts;
         for (int j0 = 0; j0 < rows; j0 += 16) {
           // the first two partial accumulators with one TMEM round trip, any
           // further ones one by one; summed in the fixed order
           // ((p0 + p1) + p2) + p3
           uint32_t v[16], w[16];
-          if (live_parts == 4 && rows - j0 <= 8) {
+          if (live == 4 && rows - j0 <= 8) {
             // at most 8 token columns left (TP8 blocks): all four partials in
             // one TMEM round trip, added in the same fixed order (measured
             // 9-13% faster on TP8 down than three round trips)
@@ -1093,14 +1174,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int jj = 8; jj < 16; ++jj) v[jj] = 0u;
           } else {
             tmem_ld_32x32b_x16(dcol0 + j0, v);
-            if (live_parts > 1) tmem_ld_32x32b_x16(dcol0 + args.d_cols + j0, w);
+            if (live > 1) tmem_ld_32x32b_x16(dcol0 + args.d_cols + j0, w);
             tmem_ld_wait();
-            if (live_parts > 1) {
+            if (live > 1) {
 #pragma unroll
               for (int jj = 0; jj < 16; ++jj)
                 v[jj] = __float_as_uint(__uint_as_float(v[jj]) + __uint_as_float(w[jj]));
             }
-            for (int p = 2; p < live_parts; ++p) {
+            for (int p = 2; p < live; ++p) {
               tmem_ld_32x32b_x16(dcol0 + p * args.d_cols + j0, w);
               tmem_ld_wait();
 #pragma unroll
@@ -1108,7 +1189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 v[jj] = __float_as_uint(__uint_as_float(v[jj]) + __uint_as_float(w[jj]));
             }
           }
-          if constexpr (kGlu) {
+          if (kGlu || (kLayer && d.phase == 0)) {
             // Fused activation: lanes 0..15 hold gate columns, lanes 16..31 the
             // matching up columns (W4A16_LAYOUT_KTILE64_GLU16). Per pair of
             // token columns, lane l < 16 computes column 2m and lane l + 16
@@ -1145,6 +1226,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();  // the tile is rewritten by the next 16 token columns
           } else {
+            // the layer's down items add into the layer output (width n2)
+            const int nn = kLayer ? args.n2 : args.n;
+            void* out_ptr = kLayer ? args.out2 : args.out;
+            const bool wadd = kLayer || args.out_mode == kOutF32WeightedAdd;
             // transpose through shared memory: tile[jj][lane] = value of token
             // column j0 + jj for weight row lane
 #pragma unroll
@@ -1154,37 +1239,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int jr = jr0; jr < 16 && j0 + jr < rows; jr += 4) {
               const int j = j0 + jr;
               const int dr = idst[j];
-              if (dr < 0 || ng >= args.n) continue;
+              if (dr < 0 || ng >= nn) continue;
               const float4 x = *reinterpret_cast<const float4*>(tile + jr * 32 + 4 * c4);
               if constexpr (kRows) {
                 // deterministic down pass: the weighted row at its routing position
                 float* o =
-                    static_cast<float*>(args.out) + static_cast<long long>(dr) * args.n + ng;
+                    static_cast<float*>(out_ptr) + static_cast<long long>(dr) * nn + ng;
                 const float wt = iwt[j];
                 if (vec4) {
                   *reinterpret_cast<float4*>(o) =
                       make_float4(wt * x.x, wt * x.y, wt * x.z, wt * x.w);
                 } else {
                   o[0] = wt * x.x;
-                  if (ng + 1 < args.n) o[1] = wt * x.y;
-                  if (ng + 2 < args.n) o[2] = wt * x.z;
-                  if (ng + 3 < args.n) o[3] = wt * x.w;
+                  if (ng + 1 < nn) o[1] = wt * x.y;
+                  if (ng + 2 < nn) o[2] = wt * x.z;
+                  if (ng + 3 < nn) o[3] = wt * x.w;
                 }
-              } else if (args.out_mode == kOutF32WeightedAdd) {
-                float* o = static_cast<float*>(args.out) + static_cast<long long>(dr) * args.n + ng;
+              } else if (wadd) {
+                float* o = static_cast<float*>(out_ptr) + static_cast<long long>(dr) * nn + ng;
                 const float wt = iwt[j];
                 if (vec4) {
                   atomicAdd(reinterpret_cast<float4*>(o),
                             make_float4(wt * x.x, wt * x.y, wt * x.z, wt * x.w));
                 } else {
                   atomicAdd(o, wt * x.x);
-                  if (ng + 1 < args.n) atomicAdd(o + 1, wt * x.y);
-                  if (ng + 2 < args.n) atomicAdd(o + 2, wt * x.z);
-                  if (ng + 3 < args.n) atomicAdd(o + 3, wt * x.w);
+                  if (ng + 1 < nn) atomicAdd(o + 1, wt * x.y);
+                  if (ng + 2 < nn) atomicAdd(o + 2, wt * x.z);
+                  if (ng + 3 < nn) atomicAdd(o + 3, wt * x.w);
                 }
               } else {
-                __nv_bfloat16* o = static_cast<__nv_bfloat16*>(args.out) +
-                                   static_cast<long long>(dr) * args.n + ng;
+                __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out_ptr) +
+                                   static_cast<long long>(dr) * nn + ng;
                 const __nv_bfloat162 lo = __floats2bfloat162_rn(x.x, x.y);
                 const __nv_bfloat162 hi = __floats2bfloat162_rn(x.z, x.w);
                 if (vec4) {
@@ -1194,14 +1279,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                   *reinterpret_cast<uint2*>(o) = pk;
                 } else {
                   o[0] = lo.x;
-                  if (ng + 1 < args.n) o[1] = lo.y;
-                  if (ng + 2 < args.n) o[2] = hi.x;
-                  if (ng + 3 < args.n) o[3] = hi.y;
+                  if (ng + 1 < nn) o[1] = lo.y;
+                  if (ng + 2 < nn) o[2] = hi.x;
+                  if (ng + 3 < nn) o[3] = hi.y;
                 }
               }
             }
             __syncwarp();  // the tile is rewritten by the next 16 token columns
           }
+        }
+        if (kLayer && d.phase == 0) {
+          // this warp's activation rows of the block are out: count them for
+          // the down items that wait on the block (any CTA)
+          __threadfence();
+          __syncwarp();
+          if (lane == 0) atomicAdd(args.block_done + d.blk, 1);
         }
         tc_fence_before();
         __syncwarp();
@@ -1385,7 +1477,12 @@ int max_pair_clusters(const GemmArgs& args) {
 
 cudaError_t launch_moe_gemm(const GemmArgs& args, int grid, bool dependent, cudaStream_t stream) {
   const size_t smem = launch_smem_bytes(args);
-  void* kernel = args.pair ? pick_kernel<true>(args) : pick_kernel<false>(args);
+  // the single-launch layer: the fused activation for its gate_up items and
+  // the weighted add for its down items, chosen per item
+  void* kernel = args.layer ? reinterpret_cast<void*>(
+                                  w4a16_moe_gemm_kernel<false, false, false, false, false, true>)
+                 : args.pair ? pick_kernel<true>(args)
+                             : pick_kernel<false>(args);
   cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;

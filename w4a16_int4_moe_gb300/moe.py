@@ -40,12 +40,17 @@ class W4A16MoE:
 
     def __init__(self, gate_up: PackedExperts, down: PackedExperts, topk: int,
                  max_tokens: int, tok_e_hint: float = 0.0, device=None,
-                 deterministic: bool = False):
+                 deterministic: bool = False, single_launch: Optional[bool] = None):
         """With gate_up packed as W4A16_LAYOUT_KTILE64_GLU16 the activation is
         fused into the gate_up call (forward skips the separate pass). With
         deterministic=True the down pass adds each token's top-k rows in a
         fixed order (W4A16_FLAG_DETERMINISTIC): the output bits do not depend
-        on the schedule."""
+        on the schedule. single_launch=True (GLU16 gate_up weights) runs
+        gate_up, the activation and down in one launch (w4a16_moe_layer);
+        None chooses it when the gate_up weights are GLU16, the pass is not
+        deterministic and the down reduction is long (inter >= 1024: measured
+        4% faster at the EP8 decode shard, I = 2048; slower at the TP8 shard,
+        I = 256, whose down items are two pipeline stages long)."""
         assert gate_up.num_experts == down.num_experts
         assert gate_up.n == 2 * down.k and gate_up.k == down.n
         self.gate_up, self.down = gate_up, down
@@ -56,6 +61,12 @@ class W4A16MoE:
         self.max_tokens = max_tokens
         self.tok_e_hint = tok_e_hint
         self.deterministic = deterministic
+        glu = gate_up.layout == ops.W4A16_LAYOUT_KTILE64_GLU16
+        if single_launch is None:
+            single_launch = glu and not deterministic and down.k >= 1024
+        self.single_launch = single_launch
+        if single_launch and (not glu or deterministic):
+            raise ValueError("single_launch needs GLU16 gate_up weights and no deterministic pass")
         self._plan_for(max_tokens)
 
     def _plan_for(self, tokens: int):
@@ -82,6 +93,10 @@ class W4A16MoE:
         self.workspace = ops.new_workspace(
             self.plan_gu, dev, self.capacity, max(self.hidden, self.inter),
             det_n=self.hidden if self.deterministic else 0, det_numel=numel)
+        if self.single_launch:
+            self.layer_workspace = torch.zeros(
+                ops.w4a16_layer_workspace_size(self.plan_gu, self.capacity, self.hidden,
+                                               self.inter), dtype=torch.uint8, device=dev)
 
     def align(self, topk_ids: torch.Tensor, stream=None):
         return ops.w4a16_moe_align_block_size(
@@ -102,6 +117,14 @@ class W4A16MoE:
             ops.W4A16_GATE_UP_SILU, self.gate_up.packed, self.num_experts, self.gate_up.n,
             self.gate_up.k, x, tokens, self.topk, self.sorted_ids, self.expert_ids, self.ntp,
             self.plan_gu, self.workspace, out=self.act_buf[:numel], stream=stream)
+
+    def layer_single_launch(self, x: torch.Tensor, tokens: int, topk_weights: torch.Tensor,
+                            out: torch.Tensor, stream=None):
+        """gate_up, activation and down in one launch (w4a16_moe_layer)."""
+        return ops.w4a16_moe_layer(
+            self.gate_up.packed, self.down.packed, self.num_experts, self.hidden, self.inter, x,
+            tokens, self.topk, self.sorted_ids, self.expert_ids, self.ntp, self.plan_gu,
+            self.layer_workspace, topk_weights, out=out, stream=stream)
 
     def activation(self, tokens: int, stream=None):
         numel = tokens * self.topk
@@ -148,6 +171,8 @@ class W4A16MoE:
         if out is None:
             out = torch.empty((tokens, self.hidden), dtype=torch.float32, device=x.device)
         self.align(topk_ids, stream)
+        if self.single_launch:
+            return self.layer_single_launch(x, tokens, topk_weights, out, stream)
         if self.fused_act:
             self.gate_up_act(x, tokens, stream)
         else:

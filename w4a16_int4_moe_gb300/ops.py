@@ -44,7 +44,8 @@ EXPORTED = (
     "w4a16_moe_align_block_size", "w4a16_prepack_size", "w4a16_prepack", "w4a16_unpack",
     "w4a16_workspace_size", "w4a16_moe_indexed_gemm", "w4a16_moe_grouped_gemm",
     "w4a16_silu_and_mul", "w4a16_read_device_status", "w4a16_moe_indexed_gemm_noalloc",
-    "w4a16_topk_softmax", "w4a16_deterministic_bytes",
+    "w4a16_topk_softmax", "w4a16_deterministic_bytes", "w4a16_layer_workspace_size",
+    "w4a16_moe_layer",
 )
 
 
@@ -101,6 +102,9 @@ def load_library(path: Optional[str] = None):
         "w4a16_silu_and_mul": (_I, [_P, _I, _I, _P, _P]),
         "w4a16_topk_softmax": (_I, [_P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
         "w4a16_read_device_status": (_I, [_P, ctypes.POINTER(_I), _P]),
+        "w4a16_layer_workspace_size": (_Z, [ctypes.POINTER(Plan), _I, _I, _I]),
+        "w4a16_moe_layer": (_I, [_P, _P, _I, _I, _I, _P, _I, _I, _P, _P, _P, _I, _P, _P, _I,
+                                 ctypes.POINTER(Plan), _P, _Z, _P]),
         "w4a16_moe_indexed_gemm_noalloc": (_I, [_I, _P, _I, _I, _I, _P, _I, _I, _P, _P, _P, _I,
                                                 _P, _P, _I, ctypes.POINTER(Plan), _P]),
     }
@@ -257,6 +261,28 @@ def w4a16_moe_grouped_gemm(kind: int, packed: torch.Tensor, num_experts: int, n:
         kind, _ptr(packed), num_experts, n, k, _ptr(a), m, _ptr(layout), expected_m, _ptr(out),
         flags, None if plan is None else ctypes.byref(plan), _ptr(workspace), workspace.numel(),
         _stream(stream)))
+    return out
+
+
+def w4a16_layer_workspace_size(plan: Plan, rows: int, hidden: int, inter: int) -> int:
+    return int(load_library().w4a16_layer_workspace_size(ctypes.byref(plan), rows, hidden, inter))
+
+
+def w4a16_moe_layer(packed_gate_up: torch.Tensor, packed_down: torch.Tensor, num_experts: int,
+                    hidden: int, inter: int, x: torch.Tensor, tokens: int, topk: int,
+                    sorted_ids: torch.Tensor, expert_ids: torch.Tensor,
+                    num_tokens_padded: torch.Tensor, plan: Plan, workspace: torch.Tensor,
+                    topk_weights: torch.Tensor, out: Optional[torch.Tensor] = None,
+                    flags: int = 0, stream=None):
+    """The layer's gate_up (fused activation) and down in one launch:
+    out FP32 [tokens, hidden]."""
+    if out is None:
+        out = torch.empty((tokens, hidden), dtype=torch.float32, device=x.device)
+    _check("w4a16_moe_layer", load_library().w4a16_moe_layer(
+        _ptr(packed_gate_up), _ptr(packed_down), num_experts, hidden, inter, _ptr(x), tokens,
+        topk, _ptr(sorted_ids), _ptr(expert_ids), _ptr(num_tokens_padded), sorted_ids.numel(),
+        _ptr(topk_weights), _ptr(out), flags, ctypes.byref(plan), _ptr(workspace),
+        workspace.numel(), _stream(stream)))
     return out
 
 
