@@ -300,6 +300,28 @@ w4a16_status w4a16_topk_softmax(const void* logits, int logits_dtype, int tokens
                                 void* stream);
 
 /*
+ * The routing front end in ONE launch: w4a16_topk_softmax followed by
+ * w4a16_moe_align_block_size over its topk_ids (num_experts of the align =
+ * num_local_experts). Every CTA routes a share of the tokens; the CTA that
+ * finishes last (it counts arrivals in `arrivals`; no CTA waits on another)
+ * then runs the alignment. Outputs are bit-identical to the two calls.
+ *   arrivals  uint32 [1] device: zero before the first call (e.g. cudaMemset
+ *             once at allocation); each call leaves it zero. Calls that may
+ *             run at the same time need separate counters.
+ * Other arguments as w4a16_topk_softmax and w4a16_moe_align_block_size
+ * (sentinel tokens*topk; capacity a multiple of block_m and at least
+ * w4a16_align_capacity(tokens*topk, num_local_experts, block_m)).
+ * num_local_experts in [1, 1024], block_m in [1, 1024]. No host
+ * synchronisation: graph-capturable.
+ */
+w4a16_status w4a16_moe_route_align(const void* logits, int logits_dtype, int tokens,
+                                   int num_experts, int topk, int renormalize, int expert_offset,
+                                   int num_local_experts, int block_m, int capacity,
+                                   int32_t* topk_ids, float* topk_weights, int32_t* sorted_ids,
+                                   int32_t* expert_ids, int32_t* num_tokens_padded,
+                                   uint32_t* arrivals, void* stream);
+
+/*
  * Activation between gate_up and down (the pages leave it out of the timed
  * pair, [P-arex] "六个场景的逐层测量与限定条件"; its form is this library's
  * reading): in BF16 [rows, 2*inter] = [gate | up]; out BF16 [rows, inter]

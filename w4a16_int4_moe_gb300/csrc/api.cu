@@ -140,7 +140,7 @@ const char* w4a16_status_string(int status) {
   }
 }
 
-int w4a16_version(void) { return 120; }
+int w4a16_version(void) { return 121; }
 
 w4a16_status w4a16_plan(int tokens, int topk, int num_experts, int n, int k, float tok_e_hint,
                         w4a16_plan_t* out) {
@@ -540,6 +540,38 @@ w4a16_status w4a16_topk_softmax(const void* logits, int logits_dtype, int tokens
                                          num_experts, topk, renormalize != 0, expert_offset,
                                          num_local_experts, topk_ids, topk_weights, sms,
                                          static_cast<cudaStream_t>(stream)));
+}
+
+w4a16_status w4a16_moe_route_align(const void* logits, int logits_dtype, int tokens,
+                                   int num_experts, int topk, int renormalize, int expert_offset,
+                                   int num_local_experts, int block_m, int capacity,
+                                   int32_t* topk_ids, float* topk_weights, int32_t* sorted_ids,
+                                   int32_t* expert_ids, int32_t* num_tokens_padded,
+                                   uint32_t* arrivals, void* stream) {
+  if (tokens < 0 || num_experts <= 0 || topk <= 0 || num_local_experts <= 0 || block_m <= 0 ||
+      capacity < 0)
+    return W4A16_ERR_INVALID_ARG;
+  if (logits_dtype != W4A16_DTYPE_F32 && logits_dtype != W4A16_DTYPE_BF16)
+    return W4A16_ERR_INVALID_ARG;
+  if (num_experts > 1024 || topk > 32 || topk > num_experts) return W4A16_ERR_UNSUPPORTED;
+  if (num_local_experts > 1024 || block_m > 1024) return W4A16_ERR_UNSUPPORTED;
+  const long long numel = static_cast<long long>(tokens) * topk;
+  if (numel >= (1LL << 30)) return W4A16_ERR_UNSUPPORTED;
+  if (sorted_ids == nullptr || expert_ids == nullptr || num_tokens_padded == nullptr ||
+      arrivals == nullptr)
+    return W4A16_ERR_INVALID_ARG;
+  if (tokens > 0 && (logits == nullptr || topk_ids == nullptr || topk_weights == nullptr))
+    return W4A16_ERR_INVALID_ARG;
+  if (capacity % block_m != 0) return W4A16_ERR_INVALID_ARG;
+  if (static_cast<size_t>(capacity) <
+      w4a16_align_capacity(static_cast<int>(numel), num_local_experts, block_m))
+    return W4A16_ERR_INVALID_ARG;
+  const int sms = current_sm_count();
+  if (sms <= 0) return W4A16_ERR_CUDA;
+  return cuda_status(launch_route_align(
+      logits, logits_dtype == W4A16_DTYPE_BF16, tokens, num_experts, topk, renormalize != 0,
+      expert_offset, num_local_experts, block_m, capacity, topk_ids, topk_weights, sorted_ids,
+      expert_ids, num_tokens_padded, arrivals, sms, static_cast<cudaStream_t>(stream)));
 }
 
 w4a16_status w4a16_silu_and_mul(const uint16_t* in, int rows, int inter, uint16_t* out,

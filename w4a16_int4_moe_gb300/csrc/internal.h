@@ -147,6 +147,14 @@ bool encode_permuted_tmap(CUtensorMap* map, const void* act, long long rows, int
 // kernel on `stream` (the row permute), see w4a16_permute_rows_kernel.
 cudaError_t launch_moe_gemm(const GemmArgs& args, int grid, bool dependent, cudaStream_t stream);
 
+// Top-k routing and moe_align_block_size in one launch (topk.cu).
+cudaError_t launch_route_align(const void* logits, int bf16_logits, int tokens, int num_experts,
+                               int topk, int renormalize, int expert_offset, int num_local,
+                               int block_m, int capacity, int32_t* topk_ids, float* topk_weights,
+                               int32_t* sorted_ids, int32_t* expert_ids,
+                               int32_t* num_tokens_padded, unsigned int* arrivals, int sms,
+                               cudaStream_t stream);
+
 cudaError_t launch_align(const int32_t* topk_ids, int numel, int num_experts, int block_m,
                          int capacity, int32_t* sorted_ids, int32_t* expert_ids,
                          int32_t* num_tokens_padded, cudaStream_t stream);

@@ -701,16 +701,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int it = unit0; it < items && ok; it += units) {
         const ItemDesc d = decode_item<kRaster, kPair, kLayer>(args, it, num_blocks, bpe, rank);
         if (d.e < 0) continue;
+        W4A16_PROF_MARK(5);
         if (!wait_phase(B.itf(ip.slot), ip.phase, abort_flag, status, kWhereMmaItem, tmo)) {
           ok = false;
           break;
         }
+        W4A16_PROF_MARK(0);
         const int n16 = sm.info_n16[ip.slot];
         if (!wait_phase<kPair>(B.acce(dp.slot), dp.phase ^ 1, abort_flag, status, kWhereMmaAcc,
                                tmo)) {
           ok = false;
           break;
         }
+        W4A16_PROF_MARK(1);
         tc_fence_after();
         // a pair's MMA takes N/2 token rows from each CTA: N is the whole block
         const uint32_t idesc = kPair ? idesc_bf16(256u, static_cast<uint32_t>(bm))
@@ -990,16 +993,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
     grid_dependency_wait();  // the previous grid may zero the output this one adds into
+    W4A16_PROF_DECL
     RingPos ip, dp;
     for (int it = unit0; it < items; it += units) {
       const ItemDesc d = decode_item<kRaster, kPair, kLayer>(args, it, num_blocks, bpe, rank);
       if (d.e < 0) continue;
       const int islot = ip.slot;
       const int dslot = dp.slot;
+      W4A16_PROF_MARK(3);
       if (!warp_wait_phase<kPair>(B.accf(dslot), dp.phase, abort_flag, status, kWhereEpiAcc,
                                   tmo) ||
           !warp_wait_phase(B.itf(islot), ip.phase, abort_flag, status, kWhereEpiItem, tmo))
         break;
+      W4A16_PROF_MARK(0);
       tc_fence_after();
       const int rows = sm.info_rows[islot];
       const int* idst = sm.info_dst + islot * bm;
@@ -1069,6 +1075,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             if (lane == 0) release_acc(B.acce(dslot));
           }
+          W4A16_PROF_MARK(1);
           for (int j0 = p0; j0 < p1; j0 += 16) {
             const float* slab = tile + (j0 - p0) * 32;
             if constexpr (kGlu) {
@@ -1148,6 +1155,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!early) release_acc(B.acce(dslot));
           mbar_arrive(B.ite(islot));
         }
+        W4A16_PROF_MARK(2);
       } else {
         const int live = kLayer ? min(parts, ksteps_of(d)) : live_parts;
         for (int j0 = 0; j0 < rows; j0 += 16) {
@@ -1305,6 +1313,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ip.next(kItemSlots);
       dp.next(args.d_slots);
     }
+    W4A16_PROF_MARK(3);
+    W4A16_PROF_STORE();
   }
 
   // ---- teardown ----

@@ -154,12 +154,34 @@ class W4A16MoE:
         return ops.w4a16_topk_softmax(router_logits, self.topk, renormalize, expert_offset,
                                       self.num_experts, out=out, stream=stream)
 
+    def route_align(self, router_logits: torch.Tensor, expert_offset: int = 0,
+                    renormalize: bool = True, stream=None):
+        """route() and align() in one launch (w4a16_moe_route_align): returns
+        (topk_ids, topk_weights) and fills the layer's routing tensors."""
+        tokens = router_logits.shape[0]
+        if tokens > self.max_tokens:
+            raise ValueError("more tokens than the layer was planned for")
+        if not hasattr(self, "_route_ids"):
+            self._route_ids = torch.empty((self.max_tokens, self.topk), dtype=torch.int32,
+                                          device=self.device)
+            self._route_w = torch.empty((self.max_tokens, self.topk), dtype=torch.float32,
+                                        device=self.device)
+        if not hasattr(self, "_arrivals"):
+            self._arrivals = torch.zeros(1, dtype=torch.int32, device=self.device)
+        ids, w = self._route_ids[:tokens], self._route_w[:tokens]
+        ops.w4a16_moe_route_align(
+            router_logits, self.topk, self.block_m, self._arrivals, renormalize, expert_offset,
+            self.num_experts, self.capacity,
+            out=(ids, w, self.sorted_ids, self.expert_ids, self.ntp), stream=stream)
+        return ids, w
+
     def forward_from_logits(self, x: torch.Tensor, router_logits: torch.Tensor,
                             expert_offset: int = 0, renormalize: bool = True,
                             out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-        """The whole layer from router logits: route, align, gate_up(+act), down."""
-        ids, w = self.route(router_logits, expert_offset, renormalize, stream)
-        return self.forward(x, ids, w, out=out, stream=stream)
+        """The whole layer from router logits: route + align (one launch),
+        gate_up(+act), down."""
+        _, w = self.route_align(router_logits, expert_offset, renormalize, stream)
+        return self.experts(x, w, out=out, stream=stream)
 
     def forward(self, x: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor,
                 out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
@@ -171,6 +193,14 @@ class W4A16MoE:
         if out is None:
             out = torch.empty((tokens, self.hidden), dtype=torch.float32, device=x.device)
         self.align(topk_ids, stream)
+        return self.experts(x, topk_weights, out=out, stream=stream)
+
+    def experts(self, x: torch.Tensor, topk_weights: torch.Tensor,
+                out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+        """gate_up(+act) and down over the routing tensors already aligned."""
+        tokens = x.shape[0]
+        if out is None:
+            out = torch.empty((tokens, self.hidden), dtype=torch.float32, device=x.device)
         if self.single_launch:
             return self.layer_single_launch(x, tokens, topk_weights, out, stream)
         if self.fused_act:

@@ -45,7 +45,7 @@ EXPORTED = (
     "w4a16_workspace_size", "w4a16_moe_indexed_gemm", "w4a16_moe_grouped_gemm",
     "w4a16_silu_and_mul", "w4a16_read_device_status", "w4a16_moe_indexed_gemm_noalloc",
     "w4a16_topk_softmax", "w4a16_deterministic_bytes", "w4a16_layer_workspace_size",
-    "w4a16_moe_layer",
+    "w4a16_moe_layer", "w4a16_moe_route_align",
 )
 
 
@@ -101,6 +101,8 @@ def load_library(path: Optional[str] = None):
                                         ctypes.POINTER(Plan), _P, _Z, _P]),
         "w4a16_silu_and_mul": (_I, [_P, _I, _I, _P, _P]),
         "w4a16_topk_softmax": (_I, [_P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
+        "w4a16_moe_route_align": (_I, [_P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P,
+                                       _P, _P, _P]),
         "w4a16_read_device_status": (_I, [_P, ctypes.POINTER(_I), _P]),
         "w4a16_layer_workspace_size": (_Z, [ctypes.POINTER(Plan), _I, _I, _I]),
         "w4a16_moe_layer": (_I, [_P, _P, _I, _I, _I, _P, _I, _I, _P, _P, _P, _I, _P, _P, _I,
@@ -306,6 +308,38 @@ def w4a16_topk_softmax(logits: torch.Tensor, topk: int, renormalize: bool = True
         _ptr(logits.contiguous()), dtype, tokens, e, topk, int(bool(renormalize)), expert_offset,
         num_local_experts, _ptr(ids), _ptr(w), _stream(stream)))
     return ids, w
+
+
+def w4a16_moe_route_align(logits: torch.Tensor, topk: int, block_m: int,
+                          arrivals: torch.Tensor, renormalize: bool = True,
+                          expert_offset: int = 0, num_local_experts: Optional[int] = None,
+                          capacity: Optional[int] = None, out=None, stream=None):
+    """Top-k routing and moe_align_block_size in one launch. arrivals: int32
+    [1] device, zero before the first call (each call leaves it zero).
+    Returns (topk_ids, topk_weights, sorted_ids, expert_ids, num_tokens_padded)."""
+    tokens, e = logits.shape
+    if num_local_experts is None:
+        num_local_experts = e
+    dtype = {torch.float32: W4A16_DTYPE_F32, torch.bfloat16: W4A16_DTYPE_BF16}.get(logits.dtype)
+    if dtype is None:
+        raise W4A16Error("w4a16_moe_route_align", W4A16_ERR_INVALID_ARG,
+                         f"logits of dtype {logits.dtype}")
+    if capacity is None:
+        capacity = w4a16_align_capacity(tokens * topk, num_local_experts, block_m)
+    dev = logits.device
+    if out is None:
+        out = (torch.empty((tokens, topk), dtype=torch.int32, device=dev),
+               torch.empty((tokens, topk), dtype=torch.float32, device=dev),
+               torch.empty(capacity, dtype=torch.int32, device=dev),
+               torch.empty(capacity // block_m, dtype=torch.int32, device=dev),
+               torch.empty(1, dtype=torch.int32, device=dev))
+    ids, w, sorted_ids, expert_ids, ntp = out
+    logits = logits.contiguous()
+    _check("w4a16_moe_route_align", load_library().w4a16_moe_route_align(
+        _ptr(logits), dtype, tokens, e, topk, int(bool(renormalize)), expert_offset,
+        num_local_experts, block_m, sorted_ids.numel(), _ptr(ids), _ptr(w), _ptr(sorted_ids),
+        _ptr(expert_ids), _ptr(ntp), _ptr(arrivals), _stream(stream)))
+    return ids, w, sorted_ids, expert_ids, ntp
 
 
 def w4a16_silu_and_mul(x: torch.Tensor, out: Optional[torch.Tensor] = None, stream=None):
