@@ -129,6 +129,35 @@ w4a16_status w4a16_plan(int tokens, int topk, int num_experts, int n, int k,
                         float tok_e_hint, w4a16_plan_t* out);
 
 /*
+ * The plan a grouped call (w4a16_moe_grouped_gemm with plan NULL) uses:
+ * w4a16_plan with tok_e = expected_m (the masked layout's row budget), else
+ * m, and block_m 128 when that tok_e exceeds 80 rows. Host only. Errors:
+ * INVALID_ARG on a bad kind, negative m or non-positive n, k.
+ */
+w4a16_status w4a16_grouped_plan(int kind, int m, int expected_m, int n, int k,
+                                w4a16_plan_t* out);
+
+/* What a plan becomes on the device. */
+typedef struct {
+  int mma_issuers;    /* threads issuing tcgen05.mma, each into its own
+                         partial FP32 accumulator (1, 2 or 4)             */
+  int acc_slots;      /* work items whose accumulators TMEM holds at once */
+  int acc_cols;       /* TMEM columns of one partial accumulator          */
+  int early_epilogue; /* 1: the accumulator slot is freed before the
+                         epilogue's global stores                         */
+  int w_stages;       /* weight ring, stages of 2 K steps                 */
+  int b_stages;       /* activation ring, stages of 2 K steps             */
+  size_t smem_bytes;  /* dynamic shared memory of one CTA                 */
+} w4a16_plan_info_t;
+
+/*
+ * Describe a plan for a GEMM of reduction length k (host only). Errors:
+ * INVALID_ARG for a NULL pointer, k <= 0, or a plan the GEMM entry points
+ * would refuse.
+ */
+w4a16_status w4a16_plan_info(const w4a16_plan_t* plan, int k, w4a16_plan_info_t* out);
+
+/*
  * Rows to allocate for sorted_ids so that any routing of `numel` rows over
  * `num_experts` experts fits after padding every expert to block_m:
  * roundup(numel + min(num_experts, numel) * (block_m - 1), block_m).

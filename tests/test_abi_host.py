@@ -33,7 +33,7 @@ def test_status_strings(lib):
     for st in range(7):
         assert ops.status_string(st)
     assert ops.status_string(99) == "unknown status"
-    assert ops.w4a16_version() == 121
+    assert ops.w4a16_version() == 122
 
 
 def test_align_capacity_closed_form(lib):

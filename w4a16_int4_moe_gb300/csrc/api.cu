@@ -140,7 +140,7 @@ const char* w4a16_status_string(int status) {
   }
 }
 
-int w4a16_version(void) { return 121; }
+int w4a16_version(void) { return 122; }
 
 w4a16_status w4a16_plan(int tokens, int topk, int num_experts, int n, int k, float tok_e_hint,
                         w4a16_plan_t* out) {
@@ -248,6 +248,39 @@ w4a16_status w4a16_unpack(const void* packed, int num_experts, int n, int k, int
 size_t w4a16_deterministic_bytes(int capacity, int n, int numel) {
   if (capacity < 0 || n <= 0 || numel < 0) return 0;
   return det_rows_bytes(capacity, n) + (static_cast<size_t>(numel) * 4 + 255) / 256 * 256;
+}
+
+w4a16_status w4a16_grouped_plan(int kind, int m, int expected_m, int n, int k,
+                                w4a16_plan_t* out) {
+  if (out == nullptr || m < 0 || n <= 0 || k <= 0) return W4A16_ERR_INVALID_ARG;
+  if (kind != W4A16_GROUPED_CONTIGUOUS && kind != W4A16_GROUPED_MASKED)
+    return W4A16_ERR_INVALID_ARG;
+  // every expert's rows form whole blocks: tok_e is the expected rows of one
+  // expert (its row budget), else all rows
+  const int rows = expected_m > 0 ? expected_m : std::max(1, m);
+  const w4a16_status st = w4a16_plan(rows, 1, 1, n, k, static_cast<float>(rows), out);
+  if (st != W4A16_OK) return st;
+  if (rows > 80) {
+    // long experts: the widest block (MMA N 128), measured faster than 64 on
+    // the contiguous layouts whose experts hold 128..1024 rows
+    out->block_m = 128;
+    set_ring_depths(out);
+  }
+  return W4A16_OK;
+}
+
+w4a16_status w4a16_plan_info(const w4a16_plan_t* plan, int k, w4a16_plan_info_t* out) {
+  if (plan == nullptr || out == nullptr || k <= 0) return W4A16_ERR_INVALID_ARG;
+  Pipeline pl;
+  if (!plan_pipeline(*plan, k, &pl)) return W4A16_ERR_INVALID_ARG;
+  out->mma_issuers = pl.parts;
+  out->acc_slots = pl.d_slots;
+  out->acc_cols = pl.d_cols;
+  out->early_epilogue = early_epilogue(plan->block_m) ? 1 : 0;
+  out->w_stages = pl.w_stages;
+  out->b_stages = pl.b_stages;
+  out->smem_bytes = pl.smem;
+  return W4A16_OK;
 }
 
 size_t w4a16_workspace_size(const w4a16_plan_t* plan, int rows, int k) {
@@ -440,12 +473,8 @@ w4a16_status w4a16_moe_grouped_gemm(int kind, const void* packed, int num_expert
     return W4A16_ERR_INVALID_ARG;
   w4a16_plan_t local;
   if (plan == nullptr) {
-    const int rows = expected_m > 0 ? expected_m : std::max(1, m);
-    w4a16_plan(rows, 1, 1, n, k, static_cast<float>(rows), &local);
-    if (rows > 80) {
-      local.block_m = 128;
-      set_ring_depths(&local);
-    }
+    const w4a16_status ps = w4a16_grouped_plan(kind, m, expected_m, n, k, &local);
+    if (ps != W4A16_OK) return ps;
     plan = &local;
   }
   if (workspace == nullptr || ws_bytes < kStatusBytes) return W4A16_ERR_WORKSPACE;

@@ -1347,6 +1347,10 @@ size_t gemm_smem_bytes(int block_m, int w_stages, int b_stages, bool pair) {
   return off;
 }
 
+// The epilogue that frees the accumulator slot before its stores: exactly
+// the block sizes whose staging tile holds a whole block.
+bool early_epilogue(int block_m) { return epi_stage_rows(block_m) > 16; }
+
 bool tmem_accumulators(int block_m, int k_steps, int* d_cols, int* parts, int* d_slots) {
   const int dcols = (block_m + 31) / 32 * 32;
   const int free_cols = kTmemCols - kASlots * kAColsPerSlot;
@@ -1431,8 +1435,7 @@ template <bool kPair>
 void* pick_kernel(const GemmArgs& args) {
   const bool glu = args.out_mode == kOutGluBf16;
   const bool rows = args.out_mode == kOutF32Rows;
-  // the whole-block staging tile exists for exactly these block sizes
-  const bool early = epi_stage_rows(args.block_m) > 16;
+  const bool early = early_epilogue(args.block_m);
   auto kernel =
       rows ? (early ? w4a16_moe_gemm_kernel<false, false, true, true, kPair>
                     : w4a16_moe_gemm_kernel<false, false, false, true, kPair>)
@@ -1456,7 +1459,7 @@ int max_pair_clusters(const GemmArgs& args) {
   // CTA pairs that can be resident at once (a pair needs two SMs of one GPC)
   static std::mutex mu;
   static int cache[8][2] = {};
-  const bool early = epi_stage_rows(args.block_m) > 16;
+  const bool early = early_epilogue(args.block_m);
   const int key = (args.out_mode == kOutGluBf16 ? 4 : 0) + (args.raster_rows ? 2 : 0) + (early ? 1 : 0);
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;

@@ -35,6 +35,16 @@ class PackedExperts:
         return cls(ops.w4a16_prepack(q, scales, group, layout), e, n, kh * 2, layout)
 
 
+def single_launch_default(gate_up_layout: int, deterministic: bool, inter: int) -> bool:
+    """Whether a layer runs gate_up, the activation and down as one launch
+    (w4a16_moe_layer) by default: GLU16 gate_up weights, no deterministic
+    pass, and a long down reduction (inter >= 1024: measured 4% faster at the
+    EP8 decode shard, I = 2048; slower at the TP8 shard, I = 256, whose down
+    items are two pipeline stages long)."""
+    return (gate_up_layout == ops.W4A16_LAYOUT_KTILE64_GLU16 and not deterministic
+            and inter >= 1024)
+
+
 class W4A16MoE:
     """One MoE layer's expert pair on one GPU (gate_up [E, 2I, H], down [E, H, I])."""
 
@@ -47,10 +57,7 @@ class W4A16MoE:
         fixed order (W4A16_FLAG_DETERMINISTIC): the output bits do not depend
         on the schedule. single_launch=True (GLU16 gate_up weights) runs
         gate_up, the activation and down in one launch (w4a16_moe_layer);
-        None chooses it when the gate_up weights are GLU16, the pass is not
-        deterministic and the down reduction is long (inter >= 1024: measured
-        4% faster at the EP8 decode shard, I = 2048; slower at the TP8 shard,
-        I = 256, whose down items are two pipeline stages long)."""
+        None applies single_launch_default."""
         assert gate_up.num_experts == down.num_experts
         assert gate_up.n == 2 * down.k and gate_up.k == down.n
         self.gate_up, self.down = gate_up, down
@@ -63,7 +70,7 @@ class W4A16MoE:
         self.deterministic = deterministic
         glu = gate_up.layout == ops.W4A16_LAYOUT_KTILE64_GLU16
         if single_launch is None:
-            single_launch = glu and not deterministic and down.k >= 1024
+            single_launch = single_launch_default(gate_up.layout, deterministic, down.k)
         self.single_launch = single_launch
         if single_launch and (not glu or deterministic):
             raise ValueError("single_launch needs GLU16 gate_up weights and no deterministic pass")

@@ -45,7 +45,7 @@ EXPORTED = (
     "w4a16_workspace_size", "w4a16_moe_indexed_gemm", "w4a16_moe_grouped_gemm",
     "w4a16_silu_and_mul", "w4a16_read_device_status", "w4a16_moe_indexed_gemm_noalloc",
     "w4a16_topk_softmax", "w4a16_deterministic_bytes", "w4a16_layer_workspace_size",
-    "w4a16_moe_layer", "w4a16_moe_route_align",
+    "w4a16_moe_layer", "w4a16_moe_route_align", "w4a16_grouped_plan", "w4a16_plan_info",
 )
 
 
@@ -54,6 +54,16 @@ class Plan(ctypes.Structure):
     _fields_ = [(name, ctypes.c_int) for name in (
         "block_m", "bn", "bk", "stages", "b_stages", "split_k", "ctas_per_sm", "swap_ab",
         "layout", "grid", "cta_pair")]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+class PlanInfo(ctypes.Structure):
+    """Mirror of w4a16_plan_info_t."""
+    _fields_ = [(name, ctypes.c_int) for name in (
+        "mma_issuers", "acc_slots", "acc_cols", "early_epilogue", "w_stages", "b_stages")] + [
+        ("smem_bytes", ctypes.c_size_t)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -89,6 +99,8 @@ def load_library(path: Optional[str] = None):
         "w4a16_version": (_I, []),
         "w4a16_plan": (_I, [_I, _I, _I, _I, _I, ctypes.c_float, ctypes.POINTER(Plan)]),
         "w4a16_align_capacity": (_Z, [_I, _I, _I]),
+        "w4a16_grouped_plan": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(Plan)]),
+        "w4a16_plan_info": (_I, [ctypes.POINTER(Plan), _I, ctypes.POINTER(PlanInfo)]),
         "w4a16_moe_align_block_size": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
         "w4a16_prepack_size": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(_Z)]),
         "w4a16_prepack": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _Z, _P]),
@@ -161,6 +173,22 @@ def w4a16_prepack_size(num_experts: int, n: int, k: int, group: int = 32,
     _check("w4a16_prepack_size", load_library().w4a16_prepack_size(
         num_experts, n, k, group, layout, ctypes.byref(out)))
     return int(out.value)
+
+
+def w4a16_grouped_plan(kind: int, m: int, n: int, k: int, expected_m: int = 0) -> Plan:
+    """The plan w4a16_moe_grouped_gemm uses when given none."""
+    p = Plan()
+    _check("w4a16_grouped_plan", load_library().w4a16_grouped_plan(
+        kind, m, expected_m, n, k, ctypes.byref(p)))
+    return p
+
+
+def w4a16_plan_info(plan: Plan, k: int) -> PlanInfo:
+    """What a plan becomes on the device for reduction length k."""
+    info = PlanInfo()
+    _check("w4a16_plan_info", load_library().w4a16_plan_info(ctypes.byref(plan), k,
+                                                             ctypes.byref(info)))
+    return info
 
 
 def w4a16_workspace_size(plan: Plan, rows: int = 0, k: int = 0) -> int:

@@ -139,7 +139,8 @@ def tiny(seed=0):
     return uniform_problem(64, 512, 512, 8, 2, seed, name="tiny_T64_H512_I512_E8_top2")
 
 
-def ep8_decode(seed=0, tokens=576, hidden=7168, inter=2048, local_experts=48, topk=8):
+def ep8_decode(seed=0, tokens=576, hidden=7168, inter=2048, local_experts=48, topk=8,
+               weights=True):
     """EP8 decode shard: 48 local experts of 384, 576 routed local rows with
     tokens-per-expert U{9..15} (corrected to sum to 576)."""
     rng = np.random.default_rng(seed)
@@ -155,7 +156,7 @@ def ep8_decode(seed=0, tokens=576, hidden=7168, inter=2048, local_experts=48, to
     ids = _place_local_picks(rng, tokens, topk, lists)
     return make_problem(f"ep8_decode_T{tokens}_H{hidden}_I{inter}_E{local_experts}_top{topk}",
                         rng, tokens, hidden, inter, local_experts, topk, ids,
-                        {"tok_e": counts.tolist()})
+                        {"tok_e": counts.tolist()}, weights=weights)
 
 
 def tp8(tokens, seed=0, hidden=7168, inter_shard=256, experts=384, topk=8, weights=True):
