@@ -414,6 +414,34 @@ def test_grouped_contiguous_full_size_ragged(cuda_dev):
     assert_close(got[rows][:, cols][valid], ref[valid], "contiguous full size")
 
 
+@pytest.mark.slow
+def test_grouped_masked_full_size_down_shape(cuda_dev):
+    # the down projection's shape (n = hidden 7168, k = inter 2048), the
+    # default plan the grouped call picks itself
+    gp = wl.grouped_masked_problem(n=7168, k=2048, seed=13)
+    got = _grouped(gp, cuda_dev)
+    cols = _sample_cols(gp.n, 256, 14)
+    ref = oracle.grouped_masked(gp.a, gp.layout, gp.q, gp.s, cols=cols)
+    valid = ~np.isnan(ref[..., 0])
+    assert_close(got[..., cols][valid], ref[valid], "masked full size, down shape")
+
+
+@pytest.mark.slow
+def test_grouped_contiguous_full_size_down_shape(cuda_dev):
+    rng = np.random.default_rng(15)
+    gp = wl.grouped_contiguous_problem(rng.integers(128, 1025, size=48), n=7168, k=2048,
+                                       seed=15)
+    plan = ops.w4a16_grouped_plan(ops.W4A16_GROUPED_CONTIGUOUS, gp.a.shape[0], gp.n, gp.k,
+                                  expected_m=gp.expected_m)
+    assert plan.block_m == 128
+    got = _grouped(gp, cuda_dev, plan)
+    rows = np.sort(rng.choice(gp.a.shape[0], size=384, replace=False))
+    cols = _sample_cols(gp.n, 128, 16)
+    ref = oracle.grouped_contiguous(gp.a[rows], gp.layout[rows], gp.q, gp.s, cols=cols)
+    valid = gp.layout[rows] >= 0
+    assert_close(got[rows][:, cols][valid], ref[valid], "contiguous full size, down shape")
+
+
 # ------------------------------------------------------------- CTA pairs --
 # Pairs of CTAs (2-CTA clusters) issue M = 256 MMAs over two weight tiles, each
 # CTA holding one tile's dequantised rows and half of the block's token rows.
