@@ -186,6 +186,56 @@ def test_grouped_and_align_argument_checks(lib):
     assert lib.w4a16_silu_and_mul(fake, 4, 12, fake, None) == ops.W4A16_ERR_INVALID_ARG
 
 
+def test_route_align_and_layer_argument_checks(lib):
+    fake = ctypes.c_void_p(1 << 20)   # never dereferenced: checks fail first
+
+    def route(**kw):
+        a = dict(logits=fake, dtype=ops.W4A16_DTYPE_F32, tokens=64, experts=384, topk=8,
+                 renorm=1, offset=0, local=48, bm=16, cap=16 * 100, arrivals=fake)
+        a.update(kw)
+        return lib.w4a16_moe_route_align(a["logits"], a["dtype"], a["tokens"], a["experts"],
+                                         a["topk"], a["renorm"], a["offset"], a["local"], a["bm"],
+                                         a["cap"], fake, fake, fake, fake, fake, a["arrivals"],
+                                         None)
+    assert route(dtype=5) == ops.W4A16_ERR_INVALID_ARG
+    assert route(arrivals=None) == ops.W4A16_ERR_INVALID_ARG      # the counter is required
+    assert route(cap=16 * 100 + 8) == ops.W4A16_ERR_INVALID_ARG   # not whole blocks
+    assert route(cap=16) == ops.W4A16_ERR_INVALID_ARG             # below the bound
+    assert route(local=0) == ops.W4A16_ERR_INVALID_ARG
+    assert route(experts=1025) == ops.W4A16_ERR_UNSUPPORTED
+    assert route(topk=33) == ops.W4A16_ERR_UNSUPPORTED
+    assert route(local=1025, cap=1 << 20) == ops.W4A16_ERR_UNSUPPORTED
+    assert route(tokens=64, logits=None) == ops.W4A16_ERR_INVALID_ARG
+
+    plan = ops.w4a16_plan(576, 8, 48, 4096, 7168, 12.0)
+    glu = ops.Plan.from_buffer_copy(plan)
+    glu.layout = ops.W4A16_LAYOUT_KTILE64_GLU16
+    cap = ops.w4a16_align_capacity(576 * 8, 48, glu.block_m)
+    need = ops.w4a16_layer_workspace_size(glu, cap, 7168, 2048)
+
+    def layer(p=glu, **kw):
+        a = dict(hidden=7168, inter=2048, x=fake, cap=cap, w=fake, out=fake, flags=0,
+                 ws=fake, wsb=need)
+        a.update(kw)
+        return lib.w4a16_moe_layer(fake, fake, 48, a["hidden"], a["inter"], a["x"], 576, 8,
+                                   fake, fake, fake, a["cap"], a["w"], a["out"], a["flags"],
+                                   ctypes.byref(p), a["ws"], a["wsb"], None)
+    assert layer(p=plan) == ops.W4A16_ERR_INVALID_ARG            # gate_up not GLU16-packed
+    pair = ops.Plan.from_buffer_copy(glu)
+    pair.cta_pair = 1
+    assert layer(p=pair) == ops.W4A16_ERR_INVALID_ARG            # the layer runs unpaired
+    assert layer(inter=2000) == ops.W4A16_ERR_UNSUPPORTED        # inter % 64
+    assert layer(hidden=7100) == ops.W4A16_ERR_UNSUPPORTED       # hidden % 32
+    assert layer(w=None) == ops.W4A16_ERR_INVALID_ARG            # top-k weights required
+    assert layer(flags=ops.W4A16_FLAG_DETERMINISTIC) == ops.W4A16_ERR_INVALID_ARG
+    assert layer(cap=cap + 8) == ops.W4A16_ERR_INVALID_ARG       # not whole blocks
+    assert layer(out=ctypes.c_void_p((1 << 20) + 4)) == ops.W4A16_ERR_INVALID_ARG
+    assert layer(wsb=need - 1) == ops.W4A16_ERR_WORKSPACE
+    assert layer(ws=None) == ops.W4A16_ERR_WORKSPACE
+    # status words, both routed-row buffers, one counter per routing block
+    assert need >= 256 + cap * 7168 * 2 + cap * 2048 * 2 + (cap // glu.block_m) * 4
+
+
 def test_product_path_has_no_cpu_fallback():
     # The package never imports the oracle; a missing library is an error.
     import w4a16_int4_moe_gb300 as pkg
