@@ -51,9 +51,14 @@ CASES = {
     "grouped contiguous 128": (
         lambda: ops.w4a16_grouped_plan(ops.W4A16_GROUPED_CONTIGUOUS, 48 * 128, 2 * I, H, 128),
         H, 128, 2, 1, 0),
-    "grouped contiguous 1024": (
+    # 128-row blocks: two issuers over k = 7168, one issuer and two slots over
+    # the down projection's k = 2048 (the epilogue overlaps the next item)
+    "grouped contiguous 1024 gate_up": (
+        lambda: ops.w4a16_grouped_plan(ops.W4A16_GROUPED_CONTIGUOUS, 48 * 1024, 2 * I, H, 1024),
+        H, 128, 2, 1, 0),
+    "grouped contiguous 1024 down": (
         lambda: ops.w4a16_grouped_plan(ops.W4A16_GROUPED_CONTIGUOUS, 48 * 1024, H, I, 1024),
-        I, 128, 2, 1, 0),
+        I, 128, 1, 2, 0),
     "grouped masked 32": (
         lambda: ops.w4a16_grouped_plan(ops.W4A16_GROUPED_MASKED, 32, 2 * I, H, 16),
         H, 32, 4, 2, 0),

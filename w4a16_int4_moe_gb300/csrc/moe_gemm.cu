@@ -1358,10 +1358,14 @@ bool tmem_accumulators(int block_m, int k_steps, int* d_cols, int* parts, int* d
   // tcgen05.mma only every hundred-odd cycles, so even short reductions
   // (TP8 down, k = 256) gain more from four parallel MMA chains (measured 3-7%)
   // than from holding more items in TMEM at once with two.
-  (void)k_steps;
   int p = kMaxIssuers;
   while (p > 1 && p * dcols > free_cols) p >>= 1;
   if (p * dcols > free_cols) return false;
+  // 128-row blocks over a short reduction (k <= 2048): one issuer and two
+  // accumulator slots, so that an item's epilogue overlaps the next item's
+  // MMAs (grouped contiguous down, k = 2048: 271 -> 220 us at 128 rows per
+  // expert); over k = 7168 two issuers and one slot stay faster (377 vs 416).
+  if (dcols == 128 && k_steps <= 32) p = 1;
   *d_cols = dcols;
   *parts = p;
   const int slots = free_cols / (p * dcols);
