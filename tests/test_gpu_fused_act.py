@@ -173,3 +173,54 @@ def test_single_launch_layer_matches_two_launches_and_oracle(cuda_dev, maker):
     a = np.where(routed[:, None], act_bits, 0).astype(np.uint16)
     y_ref = oracle.indexed_down(a, p.topk_ids, p.topk_weights, p.q_dn, p.s_dn)
     assert_close(y1.cpu().numpy(), y_ref, f"{maker}: one launch vs oracle down")
+
+
+def _layer_call(one, x, p, t, out, flags=0):
+    return ops.w4a16_moe_layer(
+        one.gate_up.packed, one.down.packed, one.num_experts, one.hidden, one.inter, x,
+        p.tokens, p.topk, one.sorted_ids, one.expert_ids, one.ntp, one.plan_gu,
+        one.layer_workspace, t(p.topk_weights), out=out, flags=flags)
+
+
+def test_single_launch_layer_flags_and_empty_routing(cuda_dev):
+    # ACCUMULATE adds into the output; VALIDATE_ROUTING checks the routing on
+    # the host first; a routing with no local rows launches no work item and
+    # leaves a zeroed output (or the prior one, with ACCUMULATE)
+    p = wl.tiny(seed=85)
+    two, one, t = _layers(p, cuda_dev)
+    x = bf16_tensor(p.x, cuda_dev)
+    ids, w = t(p.topk_ids), t(p.topk_weights)
+    y = one.forward(x, ids, w)
+    torch.cuda.synchronize()
+    prior = torch.full_like(y, 0.25)
+    out = prior.clone()
+    _layer_call(one, x, p, t, out, flags=ops.W4A16_FLAG_ACCUMULATE | ops.W4A16_FLAG_VALIDATE_ROUTING)
+    torch.cuda.synchronize()
+    assert_close(out.cpu().numpy(), (y + prior).cpu().numpy(), "layer ACCUMULATE",
+                 rel_l2=1e-6, max_abs_frac=1e-5)
+    # no local rows: every id belongs to another GPU
+    none = np.full_like(p.topk_ids, -1)
+    one.align(t(none))
+    out = torch.full_like(y, float("nan"))
+    _layer_call(one, x, p, t, out)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(out).item() == 0
+    out = prior.clone()
+    _layer_call(one, x, p, t, out, flags=ops.W4A16_FLAG_ACCUMULATE)
+    torch.cuda.synchronize()
+    assert torch.equal(out, prior)
+    st, word = ops.w4a16_read_device_status(one.layer_workspace)
+    assert st == ops.W4A16_OK, hex(word)
+
+
+def test_single_launch_layer_refuses_corrupt_routing(cuda_dev):
+    # with VALIDATE_ROUTING an expert id out of range is refused before launch
+    p = wl.tiny(seed=86)
+    two, one, t = _layers(p, cuda_dev)
+    x = bf16_tensor(p.x, cuda_dev)
+    one.align(t(p.topk_ids))
+    one.expert_ids[0] = p.num_experts + 3
+    out = torch.zeros((p.tokens, p.hidden), dtype=torch.float32, device=cuda_dev)
+    with pytest.raises(ops.W4A16Error) as ei:
+        _layer_call(one, x, p, t, out, flags=ops.W4A16_FLAG_VALIDATE_ROUTING)
+    assert ei.value.status == ops.W4A16_ERR_ROUTING
