@@ -326,8 +326,11 @@ def _grouped(gp, device, plan=None):
     lay = dev(gp.layout, device)
     kind = ops.W4A16_GROUPED_CONTIGUOUS if gp.kind == "contiguous" else ops.W4A16_GROUPED_MASKED
     m = gp.a.shape[0] if gp.kind == "contiguous" else gp.a.shape[1]
-    out = ops.w4a16_moe_grouped_gemm(kind, pk, gp.num_experts, gp.n, gp.k, a, m, lay, ws,
-                                     plan=plan, expected_m=gp.expected_m)
+    # rows the call leaves untouched (padding, past a masked count) read as zeros
+    shape = (m, gp.n) if gp.kind == "contiguous" else (gp.num_experts, m, gp.n)
+    out = torch.zeros(shape, dtype=torch.bfloat16, device=device)
+    ops.w4a16_moe_grouped_gemm(kind, pk, gp.num_experts, gp.n, gp.k, a, m, lay, ws, plan=plan,
+                               expected_m=gp.expected_m, out=out)
     st, word = ops.w4a16_read_device_status(ws)
     assert st == ops.W4A16_OK, hex(word)
     return oracle.bf16_bits_to_f64(bf16_bits(out))
