@@ -119,13 +119,17 @@ def test_plan_info_refuses_what_the_gemm_refuses():
 def test_single_launch_layer_rule():
     # the layer runs gate_up + activation + down as one launch when the
     # gate_up weights carry the interleaved gate/up layout, the pass is not
-    # deterministic, and the down reduction is long (inter >= 1024)
+    # deterministic, the down reduction is long (inter >= 1024) and the
+    # routing blocks hold at most 32 rows
     from w4a16_int4_moe_gb300.moe import single_launch_default
     glu, plain = ops.W4A16_LAYOUT_KTILE64_GLU16, ops.W4A16_LAYOUT_KTILE64
-    assert single_launch_default(glu, False, I)            # EP8 decode / prefill shard
-    assert not single_launch_default(glu, False, 256)      # TP8 shard
-    assert not single_launch_default(plain, False, I)
-    assert not single_launch_default(glu, True, I)
+    decode_bm = _plan(576, 8, 48, 2 * I, H, 12.0).block_m
+    prefill_bm = _plan(8192, 8, 48, 2 * I, H, 81.33).block_m
+    assert single_launch_default(glu, False, I, decode_bm)        # EP8 decode shard
+    assert not single_launch_default(glu, False, I, prefill_bm)   # EP8 prefill shard
+    assert not single_launch_default(glu, False, 256, 16)         # TP8 shard
+    assert not single_launch_default(plain, False, I, decode_bm)
+    assert not single_launch_default(glu, True, I, decode_bm)
 
 
 def test_bench_workloads_hit_the_intended_branches():

@@ -35,14 +35,18 @@ class PackedExperts:
         return cls(ops.w4a16_prepack(q, scales, group, layout), e, n, kh * 2, layout)
 
 
-def single_launch_default(gate_up_layout: int, deterministic: bool, inter: int) -> bool:
+def single_launch_default(gate_up_layout: int, deterministic: bool, inter: int,
+                          block_m: int = 32) -> bool:
     """Whether a layer runs gate_up, the activation and down as one launch
     (w4a16_moe_layer) by default: GLU16 gate_up weights, no deterministic
-    pass, and a long down reduction (inter >= 1024: measured 4% faster at the
-    EP8 decode shard, I = 2048; slower at the TP8 shard, I = 256, whose down
-    items are two pipeline stages long)."""
+    pass, a long down reduction (inter >= 1024) and routing blocks of at most
+    32 rows. Measured: 303.8 vs 314.6 us at the EP8 decode shard (I = 2048,
+    block_m 32); slower at the TP8 shard, I = 256, whose down items are two
+    pipeline stages long (516.4 vs 418.5 us at T = 256), and at the EP8
+    prefill shard, whose 64-row blocks need the early-release epilogue the
+    single launch does not have (703.8 vs 634.3 us)."""
     return (gate_up_layout == ops.W4A16_LAYOUT_KTILE64_GLU16 and not deterministic
-            and inter >= 1024)
+            and inter >= 1024 and block_m <= 32)
 
 
 class W4A16MoE:
@@ -70,7 +74,9 @@ class W4A16MoE:
         self.deterministic = deterministic
         glu = gate_up.layout == ops.W4A16_LAYOUT_KTILE64_GLU16
         if single_launch is None:
-            single_launch = single_launch_default(gate_up.layout, deterministic, down.k)
+            block_m = ops.w4a16_plan(max_tokens, topk, gate_up.num_experts, gate_up.n, gate_up.k,
+                                     tok_e_hint).block_m
+            single_launch = single_launch_default(gate_up.layout, deterministic, down.k, block_m)
         self.single_launch = single_launch
         if single_launch and (not glu or deterministic):
             raise ValueError("single_launch needs GLU16 gate_up weights and no deterministic pass")
