@@ -224,3 +224,29 @@ def test_single_launch_layer_refuses_corrupt_routing(cuda_dev):
     with pytest.raises(ops.W4A16Error) as ei:
         _layer_call(one, x, p, t, out, flags=ops.W4A16_FLAG_VALIDATE_ROUTING)
     assert ei.value.status == ops.W4A16_ERR_ROUTING
+
+
+@pytest.mark.slow
+def test_single_launch_layer_ep8_decode_full_size(cuda_dev):
+    # the layer's default at the EP8 decode shard: the single launch equals the
+    # two launches (same activation bits, FP32 adds in another order) and the
+    # oracle's down pass on sampled output columns
+    p = wl.ep8_decode()
+    two, one, t = _layers(p, cuda_dev)
+    assert moe_mod.W4A16MoE(one.gate_up, one.down, p.topk, p.tokens,
+                            tok_e_hint=p.tok_e_hint(), device=cuda_dev).single_launch
+    x = bf16_tensor(p.x, cuda_dev)
+    ids, w = t(p.topk_ids), t(p.topk_weights)
+    y2 = two.forward(x, ids, w)
+    y1 = one.forward(x, ids, w)
+    torch.cuda.synchronize()
+    st, word = ops.w4a16_read_device_status(one.layer_workspace)
+    assert st == ops.W4A16_OK, hex(word)
+    assert_close(y1.cpu().numpy(), y2.cpu().numpy(), "EP8 decode: one launch vs two",
+                 rel_l2=1e-6, max_abs_frac=1e-5)
+    routed = ((p.topk_ids >= 0) & (p.topk_ids < p.num_experts)).reshape(-1)
+    act_bits = bf16_bits(two.act_buf[: p.numel])
+    a = np.where(routed[:, None], act_bits, 0).astype(np.uint16)
+    cols = np.array([0, 5, 127, 128, 2048, 4095, 5000, 7167])
+    y_ref = oracle.indexed_down(a, p.topk_ids, p.topk_weights, p.q_dn, p.s_dn, cols=cols)
+    assert_close(y1.cpu().numpy()[:, cols], y_ref, "EP8 decode: one launch vs oracle down")
