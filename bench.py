@@ -784,6 +784,14 @@ def run_ours(args):
         "layer_roofline": roofline_entry(
             "hbm", "w4a16_moe_gemm_kernel (gate_up + down)", layer_gbs, hbm, NOMINAL_HBM_GBS,
             f"{peak_src} hbm_gbs", {"algorithmic_bytes": total_bytes}),
+        # the same bytes over the single-launch layer (gate_up with the fused
+        # activation, then down, one launch), when measured
+        "single_launch_roofline": (roofline_entry(
+            "hbm", "w4a16_moe_gemm_kernel (single-launch layer)",
+            total_bytes / (fused["single_launch_layer_us"] * 1e-6) / 1e9, hbm, NOMINAL_HBM_GBS,
+            f"{peak_src} hbm_gbs", {"layer_us": fused["single_launch_layer_us"],
+                                    "algorithmic_bytes": total_bytes})
+            if fused and fused.get("single_launch_layer_us") else None),
         # per layer: align, permute + gate_up, silu, permute + down
         "gpu_launches": 6 * L * args.steps,
         "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d,
