@@ -27,7 +27,7 @@ routed rows).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                        [--layers L] [--no-configs]
-                       [--workload ep8_decode|ep8_decode_e12|tp8_16|tp8_64|tp8_256|ep8_prefill|tiny
+                       [--workload ep8_decode|ep8_decode_e12|tp8_16|tp8_64|tp8_256|ep8_prefill|ep8_prefill_x4|tiny
                                    |grouped_contig_{128,256,512,1024}|grouped_masked_32]
 """
 
@@ -56,8 +56,8 @@ PROFILES = os.path.join(ROOT, "profiles")
 NOMINAL_HBM_GBS = 8000.0
 NOMINAL_BF16_TFLOPS = 2250.0
 WEIGHT_BYTES = 0.5 + 2.0 / 32  # uint4 code + BF16 scale per 32 elements
-CONFIG_SET = ("tp8_16", "tp8_64", "tp8_256", "ep8_prefill", "grouped_contig_128",
-              "grouped_contig_1024", "grouped_masked_32")
+CONFIG_SET = ("tp8_16", "tp8_64", "tp8_256", "ep8_prefill", "ep8_prefill_x4",
+              "grouped_contig_128", "grouped_contig_1024", "grouped_masked_32")
 
 
 def make_workload(name, weights=True):
@@ -72,6 +72,9 @@ def make_workload(name, weights=True):
         return wl.tp8(int(name.split("_")[1]), weights=weights)
     if name == "ep8_prefill":
         return wl.ep8_prefill(weights=weights)
+    if name == "ep8_prefill_x4":
+        # four times the tokens and every expert's rows (tok_e 80 .. 2400)
+        return wl.ep8_prefill(weights=weights, scale=4)
     if name == "tiny":
         return wl.tiny()
     raise SystemExit(f"unknown workload {name}")
@@ -468,7 +471,7 @@ def indexed_config(name, packed, device, flush, steps, warmup, peaks, glu_packed
         single_us = time_single_launch(glu_packed, dn, p, x, ids, w, out, flush,
                                        device, steps, warmup)
     hbm, tf, src = peaks
-    tensor = name == "ep8_prefill"
+    tensor = name.startswith("ep8_prefill")
     layer_us = g + d_
     total_b = work["gate_up"]["bytes"] + work["down"]["bytes"]
     total_f = work["gate_up"]["flops"] + work["down"]["flops"]
@@ -481,7 +484,8 @@ def indexed_config(name, packed, device, flush, steps, warmup, peaks, glu_packed
                               total_b / (layer_us * 1e-6) / 1e9, hbm, NOMINAL_HBM_GBS,
                               f"{src} hbm_gbs", {"algorithmic_bytes": total_b})
     return {"workload": p.name, "layer_us": layer_us, "gate_up_us": g, "down_us": d_,
-            "steps": steps, "block_m": layer.block_m, "routed_rows": work["rows"],
+            "steps": steps, "block_m": layer.block_m, "block_m_down": layer.block_m_dn,
+            "routed_rows": work["rows"],
             "active_experts": work["active_experts"],
             "gate_up_gbs": work["gate_up"]["bytes"] / (g * 1e-6) / 1e9,
             "single_launch_layer_us": single_us,
@@ -604,7 +608,7 @@ def run_configs(args, packed_ep8, device, flush, peaks):
                 tp8_packed = {(512, 7168): gu, (7168, 256): dn}
             r = indexed_config(name, tp8_packed, device, flush, steps, warmup, peaks,
                                glu_packed=tp8_glu)
-        elif name == "ep8_prefill":
+        elif name.startswith("ep8_prefill"):
             r = indexed_config(name, packed, device, flush, steps, warmup, peaks)
         else:
             r = grouped_config(name, packed, device, flush, steps, warmup, peaks)

@@ -98,13 +98,14 @@ int w4a16_version(void);
  */
 typedef struct {
   int block_m;     /* routing block rows: the align block size and the
-                      largest MMA N of one work item (16..128, step 16)   */
+                      largest MMA N of one work item (16..256, step 16)   */
   int bn;          /* weight rows per tile (MMA M) = 128                  */
   int bk;          /* K elements per pipeline step = 64                   */
   int stages;      /* weight ring depth, in stages of 2 K steps (4..16;
                       rounded down to a multiple of 4)                    */
-  int b_stages;    /* activation ring depth in K steps (8..32, a multiple
-                      of 4)                                               */
+  int b_stages;    /* activation ring depth in K steps, a multiple of 4:
+                      8..32 for block_m <= 128 (slots of 2 K steps), 4..32
+                      above (slots of 1 K step)                           */
   int split_k;     /* 1 (no split of K)                                   */
   int ctas_per_sm; /* 1 (persistent, one CTA per SM)                      */
   int swap_ab;     /* 1: weights are the MMA M operand, tokens the N one  */
@@ -113,7 +114,8 @@ typedef struct {
   int cta_pair;    /* 1: pairs of CTAs (2-CTA clusters) each work on 256
                       weight rows, the pair's even CTA issuing M = 256
                       tensor-core MMAs over both CTAs' operands; needs
-                      block_m % 32 == 0 (else the plan is refused); used
+                      block_m % 32 == 0 and block_m <= 128 (else the plan
+                      is refused); used
                       when the weight tile count (n / 128, rounded up) is
                       even, else the call runs unpaired. 0: unpaired      */
 } w4a16_plan_t;
@@ -123,7 +125,11 @@ typedef struct {
  * `tokens` tokens routed top-`topk` to `num_experts` local experts.
  * tok_e_hint > 0 overrides the expected rows per expert (default
  * tokens * topk / num_experts); it is known on the host without a sync.
- * Host only. Errors: INVALID_ARG on non-positive sizes or a NULL out.
+ * block_m from tok_e: up to 80, roundup16(1.5 tok_e) within 16..64; then 64
+ * below 120, 128, and 256 from 200 when k > 2048. The two GEMMs of a layer
+ * may so get different block sizes (each call takes routing aligned to its
+ * own plan's block_m). Host only. Errors: INVALID_ARG on non-positive sizes
+ * or a NULL out.
  */
 w4a16_status w4a16_plan(int tokens, int topk, int num_experts, int n, int k,
                         float tok_e_hint, w4a16_plan_t* out);
@@ -140,13 +146,16 @@ w4a16_status w4a16_grouped_plan(int kind, int m, int expected_m, int n, int k,
 /* What a plan becomes on the device. */
 typedef struct {
   int mma_issuers;    /* threads issuing tcgen05.mma, each into its own
-                         partial FP32 accumulator (1, 2 or 4)             */
+                         partial FP32 accumulator (1, 2 or 4; block_m
+                         above 128: 4, of which a work item uses 1, 2 or 4
+                         by its MMA N, 256 / that many columns each)      */
   int acc_slots;      /* work items whose accumulators TMEM holds at once */
   int acc_cols;       /* TMEM columns of one partial accumulator          */
   int early_epilogue; /* 1: the accumulator slot is freed before the
                          epilogue's global stores                         */
   int w_stages;       /* weight ring, stages of 2 K steps                 */
-  int b_stages;       /* activation ring, stages of 2 K steps             */
+  int b_stages;       /* activation ring slots: 2 K steps each, 1 K step
+                         for block_m above 128                            */
   size_t smem_bytes;  /* dynamic shared memory of one CTA                 */
 } w4a16_plan_info_t;
 
@@ -271,7 +280,7 @@ size_t w4a16_deterministic_bytes(int capacity, int n, int numel);
  * not depend on their contents. Blocks with expert -1 and sentinel rows are
  * skipped; ids out of range are ignored, never dereferenced.
  * Requires: k % 32 == 0, n >= 1, plan from w4a16_plan (block_m equal to the
- * align block size, 16..128 step 16), ws_bytes >=
+ * align block size, 16..256 step 16), ws_bytes >=
  * w4a16_workspace_size(plan, capacity, k), a, out 16-byte aligned.
  * The call first copies the routed rows of `a` into routing order in the
  * workspace (one extra kernel on `stream`), then runs the GEMM on them.
@@ -404,7 +413,8 @@ size_t w4a16_layer_workspace_size(const w4a16_plan_t* plan, int rows, int hidden
  * result equals w4a16_moe_indexed_gemm(W4A16_GATE_UP_SILU) followed by
  * w4a16_moe_indexed_gemm(W4A16_DOWN) up to the order of the FP32 additions.
  * Requirements: inter % 64 == 0, hidden % 32 == 0 and hidden % 4 == 0
- * (else W4A16_ERR_UNSUPPORTED); plan->cta_pair == 0; flags
+ * (else W4A16_ERR_UNSUPPORTED); plan->cta_pair == 0 and plan->block_m <= 128
+ * (else W4A16_ERR_INVALID_ARG); flags
  * VALIDATE_ROUTING and ACCUMULATE only (else W4A16_ERR_INVALID_ARG); ws_bytes
  * >= w4a16_layer_workspace_size(plan, capacity, hidden, inter) (else
  * W4A16_ERR_WORKSPACE). Every CTA of the launch must be resident at once (it

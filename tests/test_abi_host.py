@@ -53,12 +53,15 @@ def test_plan_follows_tok_e(lib):
     assert ops.w4a16_plan(16, 8, 384, 512, 7168).block_m == 16
     # prefill above the ~80 rows/expert switch
     assert ops.w4a16_plan(8192, 8, 384, 4096, 7168, 81.3).block_m == 64
-    assert ops.w4a16_plan(8192, 8, 48, 4096, 7168, 600.0).block_m == 64
+    # heavy prefill: 256-row blocks for the long gate_up reduction, 128 for down
+    assert ops.w4a16_plan(8192, 8, 48, 4096, 7168, 600.0).block_m == 256
+    assert ops.w4a16_plan(8192, 8, 48, 7168, 2048, 600.0).block_m == 128
     for tok_e in (0.3, 5, 12, 40, 80, 81, 150, 400):
         p = ops.w4a16_plan(1024, 8, 48, 4096, 7168, float(tok_e))
-        assert 16 <= p.block_m <= 64 and p.block_m % 16 == 0
+        assert 16 <= p.block_m <= 256 and p.block_m % 16 == 0
         assert 4 <= p.stages <= 16 and p.stages % 4 == 0 and p.split_k == 1
-        assert 8 <= p.b_stages <= 32 and p.b_stages % 4 == 0
+        assert 4 <= p.b_stages <= 32 and p.b_stages % 4 == 0
+        ops.w4a16_plan_info(p, 7168)  # a plan the GEMM accepts
 
 
 def test_plan_ring_depths():
@@ -72,6 +75,12 @@ def test_plan_ring_depths():
     assert (tp8.block_m, tp8.b_stages, tp8.stages) == (16, 16, 16)
     prefill = ops.w4a16_plan(8192, 8, 48, 4096, 7168, 81.3)
     assert (prefill.block_m, prefill.b_stages, prefill.stages) == (64, 12, 8)
+    # 128-row blocks: 4 two-step activation slots (32 KB each), 8 weight
+    # stages; 256-row blocks: 4 single-step slots (32 KB each), 8 weight stages
+    heavy_dn = ops.w4a16_plan(8192, 8, 48, 7168, 2048, 300.0)
+    assert (heavy_dn.block_m, heavy_dn.b_stages, heavy_dn.stages) == (128, 8, 8)
+    heavy_gu = ops.w4a16_plan(8192, 8, 48, 4096, 7168, 300.0)
+    assert (heavy_gu.block_m, heavy_gu.b_stages, heavy_gu.stages) == (256, 4, 8)
 
 
 def test_plan_rejects_bad_sizes(lib):

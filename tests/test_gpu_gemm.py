@@ -36,8 +36,13 @@ def _routing(ids, experts, bm, device):
 def _plan(bm, n, k, stages=None, b_stages=None, grid=0, pair=False):
     p = ops.w4a16_plan(64, 1, 1, n, k, float(bm))
     p.block_m = bm
-    p.b_stages = b_stages or 8
-    p.stages = stages or min(p.stages, 8)
+    if bm > 128:
+        # four activation slots of one k step (32 KB at 256 rows), eight weight stages
+        p.b_stages = b_stages or 4
+        p.stages = stages or 8
+    else:
+        p.b_stages = b_stages or 8
+        p.stages = stages or min(p.stages, 8)
     p.grid = grid
     p.cta_pair = int(pair)
     return p
@@ -73,8 +78,9 @@ def _routed(p):
     return (flat >= 0) & (flat < p.num_experts)
 
 
-def _check_pair(p, device, bm, cols_gu=None, cols_dn=None, what="", cta_pair=False):
-    """gate_up vs oracle, then down (on the GPU's activation) vs oracle."""
+def _check_pair(p, device, bm, cols_gu=None, cols_dn=None, what="", cta_pair=False, bm_dn=None):
+    """gate_up vs oracle, then down (on the GPU's activation) vs oracle; the
+    down GEMM on its own routing blocks of bm_dn rows when given."""
     pk_gu = _pack(p.q_gu, p.s_gu, device)
     pk_dn = _pack(p.q_dn, p.s_dn, device)
     routing = _routing(p.topk_ids, p.num_experts, bm, device)
@@ -94,7 +100,9 @@ def _check_pair(p, device, bm, cols_gu=None, cols_dn=None, what="", cta_pair=Fal
                  rel_l2=4e-3, max_abs_frac=1e-2)
     a_bits_clean = a_bits.copy()
     a_bits_clean[~routed] = 0
-    y = _down(p, pk_dn, routing, _plan(bm, p.hidden, p.inter, pair=cta_pair), a_bits_clean,
+    bm_dn = bm_dn or bm
+    routing_dn = routing if bm_dn == bm else _routing(p.topk_ids, p.num_experts, bm_dn, device)
+    y = _down(p, pk_dn, routing_dn, _plan(bm_dn, p.hidden, p.inter, pair=cta_pair), a_bits_clean,
               device)
     y_ref = oracle.indexed_down(a_bits_clean, p.topk_ids, p.topk_weights, p.q_dn, p.s_dn,
                                 cols=cols_dn)
@@ -109,15 +117,16 @@ def _check_pair(p, device, bm, cols_gu=None, cols_dn=None, what="", cta_pair=Fal
 
 # ------------------------------------------------------------ small shapes --
 
-@pytest.mark.parametrize("bm", [16, 32, 48, 64, 128])
+@pytest.mark.parametrize("bm", [16, 32, 48, 64, 128, 256])
 def test_tiny_all_block_sizes(cuda_dev, bm):
     _check_pair(wl.tiny(), cuda_dev, bm, what=f"tiny bm={bm}")
 
 
-@pytest.mark.parametrize("bm", [64, 128])
+@pytest.mark.parametrize("bm", [64, 128, 256])
 def test_blocks_of_mixed_fill(cuda_dev, bm):
     # 50..73 rows per expert: at block_m 64 an expert fills one block and
-    # part of a second, at block_m 128 a block is between 39% and 57% full
+    # part of a second, at block_m 128 a block is between 39% and 57% full,
+    # at 256 between 20% and 29%
     p = wl.uniform_problem(256, 1024, 512, 16, 4, seed=61)
     _check_pair(p, cuda_dev, bm, what=f"mixed fill bm={bm}")
 
@@ -127,6 +136,8 @@ def test_blocks_of_mixed_fill(cuda_dev, bm):
     (200, 320, 224, 6, 2, 64),   # ragged n tiles (448 / 320 rows), k = 32 mod 64 on down
     (5, 64, 32, 40, 4, 16),      # far more experts than rows: many empty experts
     (130, 256, 160, 3, 1, 64),   # top-1, several blocks per expert
+    (37, 96, 96, 5, 3, 256),     # 256-row blocks: k = 32 mod 64, so pad k steps on both GEMMs
+    (700, 320, 192, 2, 1, 256),  # 256-row blocks, two or more per expert, ragged last block
 ])
 def test_ragged_shapes(cuda_dev, tokens, hidden, inter, experts, topk, bm):
     p = wl.uniform_problem(tokens, hidden, inter, experts, topk, seed=tokens)
@@ -317,6 +328,35 @@ def test_layer_forward_and_graph_capture(cuda_dev):
     assert_close(out.cpu().numpy(), y_ref, "graph replay")
 
 
+@pytest.mark.parametrize("from_logits", [False, True])
+def test_layer_with_different_blocks_per_gemm(cuda_dev, from_logits):
+    # tok_e 256 over a long gate_up reduction (k = 4096) and a short down one
+    # (k = 256): gate_up takes 256-row blocks, down 128, each on its own
+    # routing; experts of a little under or over 256 rows give items of 1
+    # issuer and of 4 (a short second block); the result is the oracle layer's
+    rng = np.random.default_rng(23)
+    tokens, hidden, inter, experts, topk = 512, 4096, 256, 8, 4
+    logits = rng.standard_normal((tokens, experts)).astype(np.float32)
+    ids, wts = oracle.topk_softmax(logits, topk, renormalize=True)
+    ids = ids.astype(np.int32)
+    wts = wts.astype(np.float32)
+    p = wl.make_problem("blocks_per_gemm", rng, tokens, hidden, inter, experts, topk, ids)
+    gu = moe_mod.PackedExperts.from_checkpoint(dev(p.q_gu, cuda_dev),
+                                               dev(p.s_gu.view(np.int16), cuda_dev))
+    dn = moe_mod.PackedExperts.from_checkpoint(dev(p.q_dn, cuda_dev),
+                                               dev(p.s_dn.view(np.int16), cuda_dev))
+    layer = moe_mod.W4A16MoE(gu, dn, topk, tokens, tok_e_hint=256.0)
+    assert (layer.block_m, layer.block_m_dn) == (256, 128)
+    x = bf16_tensor(p.x, cuda_dev)
+    if from_logits:
+        y = layer.forward_from_logits(x, dev(logits, cuda_dev))
+    else:
+        y = layer.forward(x, dev(ids, cuda_dev), dev(wts, cuda_dev))
+    torch.cuda.synchronize()
+    _, _, _, y_ref = oracle.moe_layer(p.x, ids, wts, p.q_gu, p.s_gu, p.q_dn, p.s_dn)
+    assert_close(y.cpu().numpy(), y_ref, f"layer, blocks 256 / 128, from_logits={from_logits}")
+
+
 # ---------------------------------------------------------- grouped GEMMs --
 
 def _grouped(gp, device, plan=None):
@@ -393,6 +433,19 @@ def test_ep8_prefill_full_size(cuda_dev):
                         p.tok_e_hint()).block_m
     _check_pair(p, cuda_dev, bm, cols_gu=_sample_cols(4096, 128, 5),
                 cols_dn=_sample_cols(7168, 128, 6), what="EP8 prefill")
+
+
+@pytest.mark.slow
+def test_ep8_prefill_heavy_full_size(cuda_dev):
+    # four times the prefill rows (tok_e 80 .. 2400): gate_up on 256-row
+    # blocks (items of 1, 2 or 4 issuers by their rows), down on 128
+    p = wl.ep8_prefill(scale=4)
+    hint = p.tok_e_hint()
+    bm = ops.w4a16_plan(p.tokens, p.topk, p.num_experts, 2 * p.inter, p.hidden, hint).block_m
+    bm_dn = ops.w4a16_plan(p.tokens, p.topk, p.num_experts, p.hidden, p.inter, hint).block_m
+    assert (bm, bm_dn) == (256, 128)
+    _check_pair(p, cuda_dev, bm, cols_gu=_sample_cols(4096, 96, 7),
+                cols_dn=_sample_cols(7168, 96, 8), what="EP8 prefill x4", bm_dn=bm_dn)
 
 
 @pytest.mark.slow

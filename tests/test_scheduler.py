@@ -24,10 +24,19 @@ def _plan(tokens, topk, experts, n, k, hint=0.0):
     (11.0, 32), (12.0, 32), (21.0, 32),             # the EP8 decode shard: 12
     (22.0, 48), (32.0, 48),
     (33.0, 64), (80.0, 64),                         # capped at 64
-    (80.1, 64), (600.0, 64),                        # above the switch
+    (80.1, 64), (119.0, 64),                        # above the switch (EP8 prefill: 81)
+    (120.0, 128), (199.0, 128),
+    (200.0, 256), (600.0, 256),                     # long reduction (k = 7168)
 ])
 def test_block_m_follows_tok_e(tok_e, block_m):
     assert _plan(1, 1, 1, 4096, H, tok_e).block_m == block_m
+
+
+@pytest.mark.parametrize("tok_e,block_m", [(100.0, 64), (150.0, 128), (200.0, 128),
+                                           (600.0, 128)])
+def test_short_reductions_stop_at_128(tok_e, block_m):
+    # the down projection (k = 2048) keeps 128-row blocks at any tok_e
+    assert _plan(1, 1, 1, H, I, tok_e).block_m == block_m
 
 
 def test_plan_ignores_total_tokens_given_tok_e():
@@ -48,6 +57,10 @@ CASES = {
     "tp8 T=256 gate_up": (lambda: _plan(256, 8, 384, 512, H), H, 16, 4, 2, 0),
     "ep8_prefill gate_up": (lambda: _plan(8192, 8, 48, 2 * I, H, 81.33), H, 64, 4, 1, 1),
     "ep8_prefill down": (lambda: _plan(8192, 8, 48, H, I, 81.33), I, 64, 4, 1, 1),
+    # four times the EP8 prefill rows (tok_e 325): gate_up 256-row blocks,
+    # four issuer threads of which an item uses 1, 2 or 4; down 128 rows
+    "heavy prefill gate_up": (lambda: _plan(32768, 8, 48, 2 * I, H, 325.3), H, 256, 4, 1, 0),
+    "heavy prefill down": (lambda: _plan(32768, 8, 48, H, I, 325.3), I, 128, 1, 2, 0),
     "grouped contiguous 128": (
         lambda: ops.w4a16_grouped_plan(ops.W4A16_GROUPED_CONTIGUOUS, 48 * 128, 2 * I, H, 128),
         H, 128, 2, 1, 0),
@@ -75,12 +88,19 @@ def test_choices_at_each_workload(name):
     # fixed by design: 128 weight rows per tile, whole K per item, one
     # persistent CTA per SM, no CTA pairs (measured no faster)
     assert (plan.bn, plan.split_k, plan.ctas_per_sm, plan.grid, plan.cta_pair) == (128, 1, 1, 0, 0)
-    # the TMEM split: A slots (256 columns) + issuers x slots x block columns
-    assert 256 + info.mma_issuers * info.acc_slots * info.acc_cols <= 512
-    assert info.acc_cols == (block_m + 31) // 32 * 32
+    # the TMEM split: A slots (256 columns) + issuers x slots x block columns;
+    # above 128 rows one slot of 256 columns that an item splits among the
+    # issuers it uses
+    if block_m > 128:
+        assert info.acc_cols == 256 and info.acc_slots == 1
+    else:
+        assert 256 + info.mma_issuers * info.acc_slots * info.acc_cols <= 512
+        assert info.acc_cols == (block_m + 31) // 32 * 32
     # the rings fill the shared memory a CTA may take, activation ring first
     assert info.smem_bytes <= 227 * 1024
     assert info.b_stages >= 4 and info.w_stages >= 4 and info.w_stages % 4 == 0
+    if block_m > 128:
+        assert info.b_stages % 4 == 0   # single-step slots: one reader per slot
 
 
 # (activation stages, weight stages) in order of preference: an activation
@@ -105,7 +125,7 @@ def test_rings_are_the_first_preference_that_fits(tok_e):
 
 def test_plan_info_refuses_what_the_gemm_refuses():
     plan = _plan(576, 8, 48, 2 * I, H, 12.0)
-    for field, bad in (("block_m", 24), ("block_m", 256), ("split_k", 2), ("bn", 64),
+    for field, bad in (("block_m", 24), ("block_m", 272), ("split_k", 2), ("bn", 64),
                        ("stages", 2), ("b_stages", 6)):
         p = ops.Plan(**{f: getattr(plan, f) for f, _ in ops.Plan._fields_})
         setattr(p, field, bad)

@@ -43,21 +43,25 @@ struct Pipeline {
 // accumulators of one or two items. plan.stages is the weight ring depth in
 // stages of two k steps (rounded down to a multiple of 4: each of the four
 // dequant warpgroups owns every fourth stage); plan.b_stages is the
-// activation ring depth in k steps (a multiple of 4: an even number of
-// stages).
+// activation ring depth in k steps: a multiple of 4 (an even number of
+// two-step slots up to 128 rows; above, single-step slots, a multiple of 4 so
+// that each slot has one MMA issuer within an item).
 bool plan_pipeline(const w4a16_plan_t& p, int k, Pipeline* out) {
-  if (p.block_m < 16 || p.block_m > 128 || p.block_m % 16 != 0) return false;
+  if (p.block_m < 16 || p.block_m > 256 || p.block_m % 16 != 0) return false;
   if (p.bn != kTileRows || p.bk != kKStep || p.split_k != 1) return false;
   if (p.layout != W4A16_LAYOUT_KTILE64 && p.layout != W4A16_LAYOUT_KTILE64_GLU16) return false;
-  if (p.stages < 4 || p.stages > 16 || p.b_stages < 8 || p.b_stages > 32 || p.b_stages % 4 != 0)
-    return false;
+  const bool step_slots = activation_slot_is_step(p.block_m);
+  if (p.stages < 4 || p.stages > 16 || p.b_stages > 32) return false;
+  if (p.b_stages < (step_slots ? 4 : 8) || p.b_stages % 4 != 0) return false;
   Pipeline pl;
   if (!tmem_accumulators(p.block_m, packed_ksteps(k), &pl.d_cols, &pl.parts, &pl.d_slots))
     return false;
+  // single-step activation slots are read by one MMA issuer
+  if (step_slots && pl.parts != 1) return false;
   pl.w_stages = p.stages / 4 * 4;
-  pl.b_stages = p.b_stages / 2;
+  pl.b_stages = step_slots ? p.b_stages : p.b_stages / 2;
   if (p.cta_pair != 0 && p.cta_pair != 1) return false;
-  if (p.cta_pair && p.block_m % 32 != 0) return false;
+  if (p.cta_pair && (p.block_m % 32 != 0 || step_slots)) return false;
   pl.smem = gemm_smem_bytes(p.block_m, pl.w_stages, pl.b_stages, p.cta_pair != 0);
   if (pl.smem > static_cast<size_t>(kMaxDynSmem)) return false;
   *out = pl;
@@ -81,6 +85,20 @@ void set_ring_depths(w4a16_plan_t* p) {
                                    {6, 8},  {4, 16}, {4, 12}, {4, 8},  {4, 4}};
   p->b_stages = 8;
   p->stages = 4;
+  if (activation_slot_is_step(p->block_m)) {
+    // single-step activation slots (a 256-row k step is 32 KB), a multiple
+    // of 4, then the deepest weight ring beside them
+    static const int kStepDepths[][2] = {{8, 8}, {8, 4}, {4, 8}, {4, 4}};
+    for (const auto& dw : kStepDepths) {
+      if (gemm_smem_bytes(p->block_m, dw[1], dw[0]) <= static_cast<size_t>(kMaxDynSmem)) {
+        p->b_stages = dw[0];
+        p->stages = dw[1];
+        return;
+      }
+    }
+    p->b_stages = 4;
+    return;
+  }
   for (const auto& dw : kDepths) {
     if (gemm_smem_bytes(p->block_m, dw[1], dw[0]) <= static_cast<size_t>(kMaxDynSmem)) {
       p->b_stages = 2 * dw[0];
@@ -154,12 +172,25 @@ w4a16_status w4a16_plan(int tokens, int topk, int num_experts, int n, int k, flo
   // headroom for the spread, so each weight tile streams once per expert;
   // above it the block is sized by padded expert rows. The MMA N of a block
   // is its real row count rounded to 16, so padding costs no tensor time.
+  // Above the switch (GB300 measurements, 48 local experts): 64-row blocks
+  // up to tok_e 120 (the skewed EP8 prefill shard, tok_e 81: 64 -> 634 us per
+  // layer, 128 -> 776, 256 -> 1037); 128-row blocks from 120 (uniform tok_e
+  // 128: gate_up 410 vs 461 us at 64); from 200, for long reductions (k >
+  // 2048), 256-row blocks, whose items of more than 128 rows issue M = 128,
+  // N up to 256 MMAs from one thread (uniform tok_e 256: gate_up 742 vs 859
+  // us at 128; tok_e 512: 1601 vs 2064). Short reductions keep 128: their
+  // items are too short to hide the epilogue behind a single 256-column
+  // accumulator (down at tok_e 512: 1099 us at 256, 875 at 128).
   int block_m;
   if (tok_e <= 80.0) {
     block_m = round_up(std::max(16, static_cast<int>(std::ceil(1.5 * tok_e))), 16);
     block_m = std::min(block_m, 64);
-  } else {
+  } else if (tok_e < 120.0) {
     block_m = 64;
+  } else if (tok_e >= 200.0 && k > 2048) {
+    block_m = 256;
+  } else {
+    block_m = 128;
   }
   w4a16_plan_t p;
   std::memset(&p, 0, sizeof(p));
@@ -273,7 +304,9 @@ w4a16_status w4a16_plan_info(const w4a16_plan_t* plan, int k, w4a16_plan_info_t*
   if (plan == nullptr || out == nullptr || k <= 0) return W4A16_ERR_INVALID_ARG;
   Pipeline pl;
   if (!plan_pipeline(*plan, k, &pl)) return W4A16_ERR_INVALID_ARG;
-  out->mma_issuers = pl.parts;
+  // blocks above 128 rows: four issuer threads, of which an item uses 1, 2
+  // or 4 by its MMA N
+  out->mma_issuers = activation_slot_is_step(plan->block_m) ? 4 : pl.parts;
   out->acc_slots = pl.d_slots;
   out->acc_cols = pl.d_cols;
   out->early_epilogue = early_epilogue(plan->block_m) ? 1 : 0;
@@ -400,7 +433,11 @@ w4a16_status indexed_gemm(int mode, const void* packed, int num_experts, int n, 
   const int a_div = mode == W4A16_DOWN ? 1 : topk;
   // CTA pairs: each CTA of a pair loads half of a block's rows
   const bool pair = plan->cta_pair != 0 && packed_tiles(n) % 2 == 0;
-  if (!encode_permuted_tmap(&g.tmap, permuted, capacity, permuted_row_elems(k), pair ? bm / 2 : bm))
+  const bool step_slots = !pair && activation_slot_is_step(bm);
+  if (!encode_permuted_tmap(&g.tmap, permuted, capacity, permuted_row_elems(k),
+                            activation_box_rows(bm, pair), step_slots ? 1 : 2) ||
+      (step_slots && !encode_permuted_tmap(&g.tmap2, permuted, capacity, permuted_row_elems(k),
+                                           kActivationBoxRowsSmall, 1)))
     return W4A16_ERR_CUDA;
   // (n * 4 bytes per row is a multiple of 16 when n % 4 == 0; otherwise the
   // tail is cleared separately)
@@ -524,7 +561,10 @@ w4a16_status w4a16_moe_grouped_gemm(int kind, const void* packed, int num_expert
   g.gather_rows = 0;
   g.act_rows = static_cast<int>(rows_total);
   const bool pair = plan->cta_pair != 0 && g.n_tiles % 2 == 0;
-  if (!encode_act_tmap(&g.tmap, a, rows_total, k, pair ? bm / 2 : bm)) return W4A16_ERR_CUDA;
+  if (!encode_act_tmap(&g.tmap, a, rows_total, k, activation_box_rows(bm, pair)) ||
+      (!pair && activation_slot_is_step(bm) &&
+       !encode_act_tmap(&g.tmap2, a, rows_total, k, kActivationBoxRowsSmall)))
+    return W4A16_ERR_CUDA;
   g.family = kind == W4A16_GROUPED_CONTIGUOUS ? kContiguous : kMasked;
   g.out_mode = kOutBf16;
   g.layout = layout;
@@ -639,8 +679,9 @@ w4a16_status w4a16_moe_layer(const void* packed_gate_up, const void* packed_down
       (x != nullptr && !aligned16(x)))
     return W4A16_ERR_INVALID_ARG;
   // the gate_up weights carry the interleaved gate/up packing of the fused
-  // activation; the layer runs unpaired
-  if (plan->layout != W4A16_LAYOUT_KTILE64_GLU16 || plan->cta_pair != 0)
+  // activation; the layer runs unpaired, on blocks of at most 128 rows
+  if (plan->layout != W4A16_LAYOUT_KTILE64_GLU16 || plan->cta_pair != 0 ||
+      activation_slot_is_step(plan->block_m))
     return W4A16_ERR_INVALID_ARG;
   Pipeline pl;
   if (!plan_pipeline(*plan, std::max(hidden, inter), &pl)) return W4A16_ERR_INVALID_ARG;
@@ -689,8 +730,8 @@ w4a16_status w4a16_moe_layer(const void* packed_gate_up, const void* packed_down
   g.n2 = hidden;
   g.n_tiles2 = packed_tiles(hidden);
   g.k_steps2 = packed_ksteps(inter);
-  if (!encode_permuted_tmap(&g.tmap, x_sorted, capacity, permuted_row_elems(hidden), bm) ||
-      !encode_permuted_tmap(&g.tmap2, act_sorted, capacity, inter, bm))
+  if (!encode_permuted_tmap(&g.tmap, x_sorted, capacity, permuted_row_elems(hidden), bm, 2) ||
+      !encode_permuted_tmap(&g.tmap2, act_sorted, capacity, inter, bm, 2))
     return W4A16_ERR_CUDA;
   if (cudaMemsetAsync(block_done, 0, static_cast<size_t>(blocks) * 4, s) != cudaSuccess)
     return W4A16_ERR_CUDA;

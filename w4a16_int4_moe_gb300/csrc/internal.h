@@ -128,7 +128,19 @@ w4a16_status indexed_gemm(int mode, const void* packed, int num_experts, int n, 
 // Device address of the no-allocation scratch array on the current device
 // (nullptr on a CUDA error).
 void* noalloc_scratch_address();
+// Shared memory of a launch: b_stages activation slots (two k steps each, or
+// one for blocks above 128 rows) and w_stages weight stages.
 size_t gemm_smem_bytes(int block_m, int w_stages, int b_stages, bool pair = false);
+// Blocks above 128 rows: the activation ring holds single k steps. An item
+// whose MMA N exceeds 128 is filled by one copy of the whole block (map tmap);
+// a smaller one by copies of kActivationBoxRowsSmall rows up to its N (map
+// tmap2), so that a mostly empty block does not read the rows it lacks.
+constexpr bool activation_slot_is_step(int block_m) { return block_m > 128; }
+constexpr int kActivationBoxRowsSmall = 64;
+// Token rows of one activation tensor copy of the main map (tmap).
+constexpr int activation_box_rows(int block_m, bool pair) {
+  return pair ? block_m / 2 : block_m;
+}
 // CTA pairs of the GEMM kernel for `args` that can be resident at once (0 on
 // error).
 int max_pair_clusters(const GemmArgs& args);
@@ -141,9 +153,9 @@ bool early_epilogue(int block_m);
 // 2-D map of BF16 [rows, k] (box 64 x box_rows, 128-byte swizzle).
 bool encode_act_tmap(CUtensorMap* map, const void* act, long long rows, int k, int box_rows);
 // 3-D map of the permuted rows [rows, k_pad]: dims (64 columns, rows, k_pad /
-// 64 chunks), box 64 x box_rows x 2 (two k steps), 128-byte swizzle.
+// 64 chunks), box 64 x box_rows x box_steps (1 or 2 k steps), 128-byte swizzle.
 bool encode_permuted_tmap(CUtensorMap* map, const void* act, long long rows, int k_pad,
-                          int box_rows);
+                          int box_rows, int box_steps);
 // dependent = true: launched as a programmatic dependent of the previous
 // kernel on `stream` (the row permute), see w4a16_permute_rows_kernel.
 cudaError_t launch_moe_gemm(const GemmArgs& args, int grid, bool dependent, cudaStream_t stream);

@@ -103,6 +103,21 @@ __host__ __device__ constexpr int epi_stage_rows(int block_m) {
 __host__ __device__ constexpr int epi_tile_bytes(int block_m) {
   return 4 * epi_stage_rows(block_m) * 32 * 4;  // 4 epilogue warps x rows x 32 FP32
 }
+// Blocks above 128 rows: one 64-k step of token rows is up to 32 KB, so the
+// activation ring holds single k steps (two stage-sized slots would leave
+// room for too few in flight), and the one MMA issuer waits on each k step.
+__host__ __device__ constexpr bool b_per_step(int block_m) {
+  return activation_slot_is_step(block_m);
+}
+// Blocks above 128 rows: the 256 accumulator columns hold P partial
+// accumulators of 256 / P columns, P chosen per item from its MMA N: four
+// issuers up to 64 token rows, two up to 128, one above (one thread issues a
+// tcgen05.mma only every hundred-odd cycles, so small N needs several).
+constexpr int kBigAccCols = 256;
+constexpr int kSmallBoxRows = kActivationBoxRowsSmall;  // token rows per copy of tmap2
+__device__ __forceinline__ int big_block_parts(int n16) {
+  return n16 <= 64 ? 4 : (n16 <= 128 ? 2 : 1);
+}
 
 // Warp roles. The dequant and epilogue warpgroups start at multiples of 4
 // warps, so that warp % 4 selects the TMEM lane quarter each warp may access.
@@ -123,7 +138,7 @@ enum Where {
 };
 
 struct Smem {
-  uint8_t* b_ring;      // [BS stages][2 k steps][block_m rows][128 B], 128-byte swizzle
+  uint8_t* b_ring;      // [BS slots][2 k steps, or 1 (b_per_step)][block_m rows][128 B], 128-byte swizzle
   uint8_t* w_ring;      // [WS stages][2 k steps][kStepBytes]
   int* info_dst;        // [kItemSlots][block_m]: output row, -1 = not a real row
   float* info_wt;       // [kItemSlots][block_m]: top-k weight (down pass)
@@ -276,6 +291,13 @@ struct RingPos {
       slot -= n;
       phase ^= 1u;
     }
+  }
+  // advance by any number of slots
+  __device__ __forceinline__ void skip(int step, int n) {
+    const int t = slot + step;
+    const int wraps = t / n;
+    slot = t - wraps * n;
+    phase ^= static_cast<uint32_t>(wraps & 1);
   }
 };
 
@@ -459,11 +481,13 @@ __device__ __forceinline__ void dequant_group(const uint4 q, uint32_t scale_bits
 // grouped item order, and kEarly: the epilogue that frees the accumulator
 // slot before its stores (blocks of 48 or 64 rows, whose accumulators fill
 // TMEM's single slot), and kRows: the deterministic down pass (out_mode
-// kOutF32Rows), kPair: the CTA-pair kernel, and kLayer: the single-launch
-// layer (gate_up items, then down items) are compiled into their own
-// instantiations so that they cannot change the register allocation or the
-// instruction footprint of the plain kernel.
-template <bool kGlu, bool kRaster, bool kEarly, bool kRows, bool kPair, bool kLayer = false>
+// kOutF32Rows), kPair: the CTA-pair kernel, kLayer: the single-launch
+// layer (gate_up items, then down items), and kBig: blocks above 128 rows
+// are compiled into their own instantiations so that they cannot change the
+// register allocation or the instruction footprint of the plain kernel
+// (compiled into it, the 256-row code made the TP8 down pass 18% slower).
+template <bool kGlu, bool kRaster, bool kEarly, bool kRows, bool kPair, bool kLayer = false,
+          bool kBig = false>
 __global__ void __launch_bounds__(kThreads, 1)
     w4a16_moe_gemm_kernel(const __grid_constant__ GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
@@ -490,10 +514,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int bm_local = kPair ? bm >> 1 : bm;
   const uint32_t b_step_bytes = static_cast<uint32_t>(bm_local) * 128u;
   const uint32_t b_stage_bytes = 2u * b_step_bytes;
+  // kBig (blocks above 128 rows; never a pair or the single-launch layer,
+  // which refuse such blocks): activation ring of single k steps, issuers
+  // chosen per item
+  constexpr bool b_steps = kBig && !kPair && !kLayer;
+  const uint32_t b_slot_bytes = b_steps ? b_step_bytes : b_stage_bytes;
   Smem sm;
   size_t off = 0;
   sm.b_ring = base;
-  off += static_cast<size_t>(BS) * b_stage_bytes;
+  off += static_cast<size_t>(BS) * b_slot_bytes;
   sm.w_ring = base + off;
   off += static_cast<size_t>(WS) * kWStageBytes;
   sm.info_dst = reinterpret_cast<int*>(base + off);
@@ -539,7 +568,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     b0 += 8 * kMaxDSlots;
     B.final_bar = b0;
   }
-  // issuers that read each stage (each commits once per stage)
+  // issuers that read each stage (each commits once per stage); blocks above
+  // 128 rows: one reader per activation slot, two commits per A slot
   const int readers = parts < 2 ? parts : 2;
 
   if (threadIdx.x == 0) {
@@ -551,19 +581,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the gather warp's arrival (+ tensor-copy bytes); the pair leader's
       // also counts the peer's relayed arrival for its half of the rows
       mbar_init(B.bf(i), (kPair && leader) ? 2 : 1);
-      mbar_init(B.be(i), readers);  // tcgen05.commit of the stage's issuers
+      mbar_init(B.be(i), b_steps ? 1 : readers);  // tcgen05.commit of the slot's issuers
     }
     for (int i = 0; i < kASlots; ++i) {
       // the 4 warps of the slot's dequant warpgroup (of both CTAs of a pair)
       mbar_init(B.af(i), kPair ? 8 : 4);
-      mbar_init(B.ae(i), readers);
+      mbar_init(B.ae(i), b_steps ? 2 : readers);
     }
     for (int i = 0; i < kItemSlots; ++i) {
       mbar_init(B.itf(i), 1);  // the router warp
       mbar_init(B.ite(i), 4);  // the 4 epilogue warps
     }
     for (int i = 0; i < kMaxDSlots; ++i) {
-      mbar_init(B.accf(i), parts);  // one tcgen05.commit per MMA issuer
+      // one tcgen05.commit per MMA issuer (blocks above 128 rows: all four,
+      // the issuers without MMAs in the item by a plain arrive)
+      mbar_init(B.accf(i), b_steps ? kMaxIssuers : parts);
       mbar_init(B.acce(i), kPair ? 8 : 4);  // the epilogue warps (of both CTAs of a pair)
     }
     for (int i = 0; i < kMaxIssuers; ++i) mbar_init(B.fin(i), 1);
@@ -691,7 +723,91 @@ __global__ void __launch_bounds__(kThreads, 1)
       W4A16_PROF_STORE();
     }
     W4A16_PROF_DECL
-    if ((!kPair || leader) && lane == 0 && q < parts) {
+    if (b_steps) {
+      // Blocks above 128 rows: per item, P = big_block_parts(N) issuers take
+      // part and issuer q takes the k steps ks % P == q into its own partial.
+      // Every issuer walks every item: it reads the item's N, waits until the
+      // previous item's accumulator is released and adds one arrival to the
+      // item's accumulator barrier (the readers by tcgen05.commit). Within an
+      // item each activation slot (BS % 4 == 0) and each A slot has fixed
+      // readers, which alone free it: an activation slot by one commit, an A
+      // slot by two arrivals (a lone issuer adds a plain one to its commit).
+      // The release wait at every item start keeps an issuer that skipped
+      // slots from waiting on a phase two behind or ahead of the barrier.
+      if (lane == 0) {
+        RingPos ip, ap, bp;
+        uint32_t acc_phase = 0;  // one accumulator slot
+        bool ok = true;
+        const uint64_t b_desc0 = smem_desc_sw128_kmajor(smem_u32(sm.b_ring));
+        for (int it = unit0; it < items && ok; it += units) {
+          const ItemDesc d = decode_item<kRaster, kPair, kLayer>(args, it, num_blocks, bpe, rank);
+          if (d.e < 0) continue;
+          if (!wait_phase(B.itf(ip.slot), ip.phase, abort_flag, status, kWhereMmaItem, tmo) ||
+              !wait_phase(B.acce(0), acc_phase ^ 1, abort_flag, status, kWhereMmaAcc, tmo)) {
+            ok = false;
+            break;
+          }
+          const int n16 = sm.info_n16[ip.slot];
+          const int P = big_block_parts(n16);
+          const int nst_i = nstp_of(d);
+          if (q >= P) {
+            // no MMAs in this item: pass its slots
+            mbar_arrive(B.accf(0));
+            ap.skip(nst_i, kASlots);
+            bp.skip(2 * nst_i, BS);
+          } else {
+            tc_fence_after();
+            const uint32_t idesc = idesc_bf16_m128(static_cast<uint32_t>(n16));
+            const uint32_t d_tmem = tmem + d_col_base + q * (kBigAccCols / P);
+            const int ks = ksteps_of(d);
+            uint32_t acc = 0;
+            for (int st = 0; st < nst_i && ok; ++st) {
+              const int r0 = (2 * st) & (P - 1), r1 = (2 * st + 1) & (P - 1);
+              if (r0 != q && r1 != q) {
+                ap.next(kASlots);
+                bp.skip(2, BS);
+                continue;
+              }
+              if (!wait_phase(B.af(ap.slot), ap.phase, abort_flag, status, kWhereMmaA, tmo)) {
+                ok = false;
+                break;
+              }
+              for (int j = 0; j < 2; ++j, bp.next(BS)) {
+                if ((j ? r1 : r0) != q) continue;
+                if (!wait_phase(B.bf(bp.slot), bp.phase, abort_flag, status, kWhereMmaB, tmo)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+                if (2 * st + j < ks) {
+                  // slot offsets are multiples of 1024 bytes
+                  const uint64_t b_desc =
+                      b_desc0 + ((static_cast<uint32_t>(bp.slot) * b_step_bytes) >> 4);
+                  const uint32_t a_tmem = tmem + ap.slot * kAColsPerSlot + j * kAColsPerStep;
+#pragma unroll
+                  for (int kk = 0; kk < 4; ++kk) {
+                    mma_bf16_ts(d_tmem, a_tmem + kk * 8, b_desc + 2 * kk, idesc, acc);
+                    acc = 1;
+                  }
+                }
+                tc_commit(B.be(bp.slot));
+              }
+              if (!ok) break;
+              // the slot expects two arrivals: a lone issuer adds a plain one
+              if (P == 1) mbar_arrive(B.ae(ap.slot));
+              tc_commit(B.ae(ap.slot));
+              ap.next(kASlots);
+            }
+            if (!ok) break;
+            tc_commit(B.accf(0));
+          }
+          acc_phase ^= 1u;
+          ip.next(kItemSlots);
+        }
+        tc_commit(B.fin(q));
+        drain_phase(B.fin(q), 0, kDrainCycles);
+      }
+    } else if ((!kPair || leader) && lane == 0 && q < parts) {
       const IssuerPlan pl = issuer_plan(q, parts);
       RingPos ip, dp, ap, bp;
       ap.slot = pl.first;
@@ -830,7 +946,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the token rows may come from the previous grid (the row permute)
     grid_dependency_wait();
     if (lane == 0) {
-      RingPos bp;
+      RingPos bp, gip;
       uint32_t issued = 0;  // stages whose b_full phase this thread started
       bool ok = true;
       for (int it = unit0; it < items && ok; it += units) {
@@ -856,6 +972,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int ks = ksteps_of(d);
         const int nst_i = nstp_of(d);
+        // blocks above 128 rows: an item with N > 128 takes the whole block in
+        // one copy, a smaller one its rows up to N in copies of kSmallBoxRows
+        // (N from the item ring)
+        int chunks = 1;
+        bool whole = true;
+        if (b_steps) {
+          if (!wait_phase(B.itf(gip.slot), gip.phase, abort_flag, status, kWhereGatherItem, tmo)) {
+            ok = false;
+            break;
+          }
+          const int n16 = sm.info_n16[gip.slot];
+          whole = n16 > 128;
+          chunks = whole ? 1 : (n16 + kSmallBoxRows - 1) / kSmallBoxRows;
+          gip.next(kItemSlots);
+        }
         for (int st = 0; st < nst_i; ++st, bp.next(BS)) {
           if (!wait_phase<kPair>(B.be(bp.slot), bp.phase ^ 1, abort_flag, status, kWhereGatherB,
                                  tmo)) {
@@ -863,8 +994,40 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           const int nks = min(2, max(0, ks - 2 * st));
-          const uint32_t dst = smem_u32(sm.b_ring + static_cast<size_t>(bp.slot) * b_stage_bytes);
-          if (nks == 0) {
+          const uint32_t dst = smem_u32(sm.b_ring + static_cast<size_t>(bp.slot) * b_slot_bytes);
+          if (b_steps) {
+            // one k step per slot: this stage's second k step has the next slot
+            for (int j = 0; j < 2 && ok; ++j) {
+              if (j == 1) {
+                ++issued;
+                bp.next(BS);
+                if (!wait_phase(B.be(bp.slot), bp.phase ^ 1, abort_flag, status, kWhereGatherB,
+                                tmo)) {
+                  ok = false;
+                  break;
+                }
+              }
+              const uint32_t dj = smem_u32(sm.b_ring + static_cast<size_t>(bp.slot) * b_step_bytes);
+              if (j >= nks) {
+                mbar_arrive(B.bf(bp.slot));  // pad k step: no data
+              } else {
+                const CUtensorMap* map = whole ? &args.tmap : &args.tmap2;
+                mbar_arrive_expect_tx(B.bf(bp.slot),
+                                      whole ? b_step_bytes
+                                            : static_cast<uint32_t>(chunks * kSmallBoxRows * 128));
+                for (int c = 0; c < chunks; ++c) {
+                  const uint32_t dc = dj + static_cast<uint32_t>(c * kSmallBoxRows * 128);
+                  const int row = box_row + c * kSmallBoxRows;
+                  if (gather) {
+                    tma_load_3d(dc, map, 0, row, 2 * st + j, B.bf(bp.slot));
+                  } else {
+                    tma_load_2d(dc, map, (2 * st + j) * kKStep, row, B.bf(bp.slot));
+                  }
+                }
+              }
+            }
+            if (!ok) break;
+          } else if (nks == 0) {
             mbar_arrive(B.bf(bp.slot));  // pad stage: no data
           } else if (gather) {
             mbar_arrive_expect_tx(B.bf(bp.slot), b_stage_bytes);
@@ -1157,7 +1320,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         W4A16_PROF_MARK(2);
       } else {
-        const int live = kLayer ? min(parts, ksteps_of(d)) : live_parts;
+        // the item's partial accumulators and their column stride (blocks
+        // above 128 rows choose them per item; the others read the launch's)
+        int big_parts = 1;
+        if constexpr (b_steps) big_parts = big_block_parts(sm.info_n16[islot]);
+        auto pstride = [&]() -> int {
+          if constexpr (b_steps) {
+            return kBigAccCols / big_parts;
+          } else {
+            return args.d_cols;
+          }
+        };
+        const int live = kLayer    ? min(parts, ksteps_of(d))
+                         : b_steps ? min(big_parts, ksteps_of(d))
+                                   : live_parts;
         for (int j0 = 0; j0 < rows; j0 += 16) {
           // the first two partial accumulators with one TMEM round trip, any
           // further ones one by one; summed in the fixed order
@@ -1169,9 +1345,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // 9-13% faster on TP8 down than three round trips)
             uint32_t a8[8], b8[8], c8[8], d8[8];
             tmem_ld_32x32b_x8(dcol0 + j0, a8);
-            tmem_ld_32x32b_x8(dcol0 + args.d_cols + j0, b8);
-            tmem_ld_32x32b_x8(dcol0 + 2 * args.d_cols + j0, c8);
-            tmem_ld_32x32b_x8(dcol0 + 3 * args.d_cols + j0, d8);
+            tmem_ld_32x32b_x8(dcol0 + pstride() + j0, b8);
+            tmem_ld_32x32b_x8(dcol0 + 2 * pstride() + j0, c8);
+            tmem_ld_32x32b_x8(dcol0 + 3 * pstride() + j0, d8);
             tmem_ld_wait();
 #pragma unroll
             for (int jj = 0; jj < 8; ++jj)
@@ -1182,7 +1358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int jj = 8; jj < 16; ++jj) v[jj] = 0u;
           } else {
             tmem_ld_32x32b_x16(dcol0 + j0, v);
-            if (live > 1) tmem_ld_32x32b_x16(dcol0 + args.d_cols + j0, w);
+            if (live > 1) tmem_ld_32x32b_x16(dcol0 + pstride() + j0, w);
             tmem_ld_wait();
             if (live > 1) {
 #pragma unroll
@@ -1190,7 +1366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 v[jj] = __float_as_uint(__uint_as_float(v[jj]) + __uint_as_float(w[jj]));
             }
             for (int p = 2; p < live; ++p) {
-              tmem_ld_32x32b_x16(dcol0 + p * args.d_cols + j0, w);
+              tmem_ld_32x32b_x16(dcol0 + p * pstride() + j0, w);
               tmem_ld_wait();
 #pragma unroll
               for (int jj = 0; jj < 16; ++jj)
@@ -1336,8 +1512,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 size_t gemm_smem_bytes(int block_m, int w_stages, int b_stages, bool pair) {
   size_t off = 1024;  // alignment slack
-  // a CTA of a pair holds half of the block's token rows
-  off += static_cast<size_t>(b_stages) * 2 * (pair ? block_m / 2 : block_m) * 128;
+  // a CTA of a pair holds half of the block's token rows; a slot holds two
+  // k steps, or one above 128 rows
+  const int steps_per_slot = (!pair && b_per_step(block_m)) ? 1 : 2;
+  off += static_cast<size_t>(b_stages) * steps_per_slot * (pair ? block_m / 2 : block_m) * 128;
   off += static_cast<size_t>(w_stages) * kWStageBytes;
   off += static_cast<size_t>(kItemSlots) * block_m * (4 + 4) + 2 * kItemSlots * 4;
   off = (off + 15) / 16 * 16 + epi_tile_bytes(block_m);
@@ -1397,7 +1575,7 @@ bool encode_act_tmap(CUtensorMap* map, const void* act, long long rows, int k, i
 }
 
 bool encode_permuted_tmap(CUtensorMap* map, const void* act, long long rows, int k_pad,
-                          int box_rows) {
+                          int box_rows, int box_steps) {
   using EncodeFn = PFN_cuTensorMapEncodeTiled_v12000;
   static EncodeFn encode = nullptr;
   static std::once_flag once;
@@ -1409,12 +1587,14 @@ bool encode_permuted_tmap(CUtensorMap* map, const void* act, long long rows, int
         q == cudaDriverEntryPointSuccess)
       encode = reinterpret_cast<EncodeFn>(fn);
   });
-  if (encode == nullptr || rows <= 0 || rows > (1LL << 31) || k_pad <= 0 || k_pad % kKStep != 0)
+  if (encode == nullptr || rows <= 0 || rows > (1LL << 31) || k_pad <= 0 || k_pad % kKStep != 0 ||
+      box_steps < 1 || box_steps > 2)
     return false;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kKStep), static_cast<cuuint64_t>(rows),
                               static_cast<cuuint64_t>(k_pad / kKStep)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(k_pad) * 2, kKStep * 2};
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kKStep), static_cast<cuuint32_t>(box_rows), 2};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kKStep), static_cast<cuuint32_t>(box_rows),
+                            static_cast<cuuint32_t>(box_steps)};
   const cuuint32_t estr[3] = {1, 1, 1};
   return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(act), dims, strides,
                 box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -1440,6 +1620,13 @@ void* pick_kernel(const GemmArgs& args) {
   const bool glu = args.out_mode == kOutGluBf16;
   const bool rows = args.out_mode == kOutF32Rows;
   const bool early = early_epilogue(args.block_m);
+  if (!kPair && b_per_step(args.block_m)) {
+    // blocks above 128 rows: tile-major item order, no early release
+    auto big = rows  ? w4a16_moe_gemm_kernel<false, false, false, true, false, false, true>
+               : glu ? w4a16_moe_gemm_kernel<true, false, false, false, false, false, true>
+                     : w4a16_moe_gemm_kernel<false, false, false, false, false, false, true>;
+    return reinterpret_cast<void*>(big);
+  }
   auto kernel =
       rows ? (early ? w4a16_moe_gemm_kernel<false, false, true, true, kPair>
                     : w4a16_moe_gemm_kernel<false, false, false, true, kPair>)

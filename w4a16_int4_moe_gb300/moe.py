@@ -90,8 +90,11 @@ class W4A16MoE:
                                       self.down.k, hint)
         self.fused_act = self.gate_up.layout == ops.W4A16_LAYOUT_KTILE64_GLU16
         self.plan_gu.layout = self.gate_up.layout
-        # both GEMMs read the same routing blocks
-        self.plan_dn.block_m = self.plan_gu.block_m
+        if self.single_launch:
+            # one launch over one set of routing blocks
+            if self.plan_gu.block_m > 128:
+                raise ValueError("single_launch needs routing blocks of at most 128 rows")
+            self.plan_dn.block_m = self.plan_gu.block_m
         self.block_m = self.plan_gu.block_m
         numel = self.max_tokens * self.topk
         self.capacity = ops.w4a16_align_capacity(numel, self.num_experts, self.block_m)
@@ -99,12 +102,26 @@ class W4A16MoE:
         self.sorted_ids = torch.empty(self.capacity, dtype=torch.int32, device=dev)
         self.expert_ids = torch.empty(self.capacity // self.block_m, dtype=torch.int32, device=dev)
         self.ntp = torch.empty(1, dtype=torch.int32, device=dev)
+        # The down GEMM may take other blocks than gate_up (at large tok_e the
+        # long gate_up reduction takes 256-row blocks, down 128): gate_up
+        # writes its rows in token order, so each GEMM reads its own routing.
+        self.block_m_dn = self.plan_dn.block_m
+        if self.block_m_dn != self.block_m:
+            self.capacity_dn = ops.w4a16_align_capacity(numel, self.num_experts, self.block_m_dn)
+            self.sorted_ids_dn = torch.empty(self.capacity_dn, dtype=torch.int32, device=dev)
+            self.expert_ids_dn = torch.empty(self.capacity_dn // self.block_m_dn,
+                                             dtype=torch.int32, device=dev)
+            self.ntp_dn = torch.empty(1, dtype=torch.int32, device=dev)
+        else:
+            self.capacity_dn = self.capacity
+            self.sorted_ids_dn, self.expert_ids_dn, self.ntp_dn = (
+                self.sorted_ids, self.expert_ids, self.ntp)
         self.inter_buf = torch.empty((numel, 2 * self.inter), dtype=torch.bfloat16, device=dev)
         self.act_buf = torch.empty((numel, self.inter), dtype=torch.bfloat16, device=dev)
         # one workspace for both GEMMs (ordered on one stream): status words
         # and the routed rows of the wider activation (x, k = hidden)
         self.workspace = ops.new_workspace(
-            self.plan_gu, dev, self.capacity, max(self.hidden, self.inter),
+            self.plan_gu, dev, max(self.capacity, self.capacity_dn), max(self.hidden, self.inter),
             det_n=self.hidden if self.deterministic else 0, det_numel=numel)
         if self.single_launch:
             self.layer_workspace = torch.zeros(
@@ -112,9 +129,18 @@ class W4A16MoE:
                                                self.inter), dtype=torch.uint8, device=dev)
 
     def align(self, topk_ids: torch.Tensor, stream=None):
+        """Routing blocks of both GEMMs (one align, two when their block sizes
+        differ)."""
+        self._align_down(topk_ids, stream)
         return ops.w4a16_moe_align_block_size(
             topk_ids, self.num_experts, self.block_m, self.capacity,
             out=(self.sorted_ids, self.expert_ids, self.ntp), stream=stream)
+
+    def _align_down(self, topk_ids: torch.Tensor, stream=None):
+        if self.block_m_dn != self.block_m:
+            ops.w4a16_moe_align_block_size(
+                topk_ids, self.num_experts, self.block_m_dn, self.capacity_dn,
+                out=(self.sorted_ids_dn, self.expert_ids_dn, self.ntp_dn), stream=stream)
 
     def gate_up_gemm(self, x: torch.Tensor, tokens: int, stream=None):
         numel = tokens * self.topk
@@ -148,8 +174,8 @@ class W4A16MoE:
         numel = tokens * self.topk
         return ops.w4a16_moe_indexed_gemm(
             ops.W4A16_DOWN, self.down.packed, self.num_experts, self.down.n, self.down.k,
-            self.act_buf[:numel], tokens, self.topk, self.sorted_ids, self.expert_ids, self.ntp,
-            self.plan_dn, self.workspace, topk_weights=topk_weights, out=out,
+            self.act_buf[:numel], tokens, self.topk, self.sorted_ids_dn, self.expert_ids_dn,
+            self.ntp_dn, self.plan_dn, self.workspace, topk_weights=topk_weights, out=out,
             flags=ops.W4A16_FLAG_DETERMINISTIC if self.deterministic else 0, stream=stream)
 
     def route(self, router_logits: torch.Tensor, expert_offset: int = 0,
@@ -186,6 +212,8 @@ class W4A16MoE:
             router_logits, self.topk, self.block_m, self._arrivals, renormalize, expert_offset,
             self.num_experts, self.capacity,
             out=(ids, w, self.sorted_ids, self.expert_ids, self.ntp), stream=stream)
+        # the down GEMM's own blocks over the same local ids
+        self._align_down(ids, stream)
         return ids, w
 
     def forward_from_logits(self, x: torch.Tensor, router_logits: torch.Tensor,

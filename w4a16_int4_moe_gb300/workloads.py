@@ -167,19 +167,22 @@ def tp8(tokens, seed=0, hidden=7168, inter_shard=256, experts=384, topk=8, weigh
     return p
 
 
-def ep8_prefill_counts(local_experts=48, seed=0):
-    """tok_e for the skewed prefill shard: round(600 * (1 + 0.447 e)^-1.1),
-    randomly permuted (600 .. 20 rows, 3904 in total)."""
+def ep8_prefill_counts(local_experts=48, seed=0, scale=1):
+    """tok_e for the skewed prefill shard: scale * round(600 * (1 + 0.447 e)^-1.1),
+    randomly permuted (600 .. 20 rows, 3904 in total, at scale 1)."""
     rng = np.random.default_rng(seed)
     e = np.arange(local_experts)
-    counts = np.round(600.0 * (1.0 + 0.447 * e) ** -1.1).astype(np.int64)
+    counts = np.round(600.0 * (1.0 + 0.447 * e) ** -1.1).astype(np.int64) * scale
     return counts[rng.permutation(local_experts)]
 
 
 def ep8_prefill(seed=0, tokens=8192, hidden=7168, inter=2048, local_experts=48, topk=8,
-                weights=True):
+                weights=True, scale=1):
+    """The skewed EP8 prefill shard; scale multiplies the tokens and every
+    expert's rows (scale 4: T = 32768, tok_e 80 .. 2400, mean 325)."""
     rng = np.random.default_rng(seed)
-    counts = ep8_prefill_counts(local_experts, seed)
+    tokens = tokens * scale
+    counts = ep8_prefill_counts(local_experts, seed, scale)
     lists = _draw_expert_tokens(rng, tokens, topk, counts)
     ids = _place_local_picks(rng, tokens, topk, lists)
     return make_problem(f"ep8_prefill_T{tokens}_H{hidden}_I{inter}_E{local_experts}_top{topk}",
