@@ -355,10 +355,16 @@ def time_indexed_layer(layer, x, tokens, ids, w, out, flush, steps, warmup, laye
 
 def time_single_launch(gu_glu, dn, p, x, ids, w, out, flush, device, steps, warmup):
     """µs of the whole layer (gate_up, activation, down) in one GEMM launch
-    (w4a16_moe_layer, with its row permute), L2 flushed before every step."""
+    (w4a16_moe_layer, with its row permute), L2 flushed before every step;
+    None where the plan's routing blocks exceed the 128 rows the single
+    launch takes."""
     import torch
     from w4a16_int4_moe_gb300 import moe as moe_mod
     from w4a16_int4_moe_gb300 import ops
+    bm = ops.w4a16_plan(p.tokens, p.topk, p.num_experts, 2 * p.inter, p.hidden,
+                        p.tok_e_hint()).block_m
+    if bm > 128:
+        return None
     layer = moe_mod.W4A16MoE(gu_glu, dn, p.topk, p.tokens, tok_e_hint=p.tok_e_hint(),
                              device=device, single_launch=True)
     stream = torch.cuda.current_stream()

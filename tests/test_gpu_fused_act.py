@@ -137,7 +137,10 @@ def _layers(p, device, single_bm=None):
     gu = moe_mod.PackedExperts.from_checkpoint(t(p.q_gu), t(p.s_gu.view(np.int16)),
                                                layout=ops.W4A16_LAYOUT_KTILE64_GLU16)
     dn = moe_mod.PackedExperts.from_checkpoint(t(p.q_dn), t(p.s_dn.view(np.int16)))
-    two = moe_mod.W4A16MoE(gu, dn, p.topk, p.tokens, tok_e_hint=p.tok_e_hint(), device=device)
+    # two launches asked for explicitly: at the EP8 decode shard the default
+    # is the single launch, which leaves the layer's act_buf unwritten
+    two = moe_mod.W4A16MoE(gu, dn, p.topk, p.tokens, tok_e_hint=p.tok_e_hint(), device=device,
+                           single_launch=False)
     one = moe_mod.W4A16MoE(gu, dn, p.topk, p.tokens, tok_e_hint=p.tok_e_hint(), device=device,
                            single_launch=True)
     return two, one, t

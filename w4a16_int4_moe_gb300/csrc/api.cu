@@ -471,7 +471,12 @@ w4a16_status indexed_gemm(int mode, const void* packed, int num_experts, int n, 
   g.out = det ? static_cast<void*>(det_rows) : out;
   g.status = static_cast<int*>(workspace);
   fill_pipeline(pl, &g);
-  g.raster_rows = 0;
+  // 256-row blocks come with tok_e >= 200 and long reductions: the routed
+  // rows (hundreds of MB) exceed L2, and in tile-major order every weight
+  // tile pass would read them from DRAM again (EP8 prefill at four times the
+  // rows: 5.7 GB of DRAM reads per gate_up launch); grouped in blocks of 8,
+  // a group's rows stay in L2 across its tiles
+  g.raster_rows = step_slots ? 1 : 0;
   g.timeout_cycles = wait_timeout_cycles();
   g.pair = pair ? 1 : 0;
   long long grid = plan->grid > 0 ? plan->grid : static_cast<long long>(sms) * plan->ctas_per_sm;

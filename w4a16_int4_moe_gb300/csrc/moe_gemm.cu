@@ -1621,10 +1621,14 @@ void* pick_kernel(const GemmArgs& args) {
   const bool rows = args.out_mode == kOutF32Rows;
   const bool early = early_epilogue(args.block_m);
   if (!kPair && b_per_step(args.block_m)) {
-    // blocks above 128 rows: tile-major item order, no early release
-    auto big = rows  ? w4a16_moe_gemm_kernel<false, false, false, true, false, false, true>
-               : glu ? w4a16_moe_gemm_kernel<true, false, false, false, false, false, true>
-                     : w4a16_moe_gemm_kernel<false, false, false, false, false, false, true>;
+    // blocks above 128 rows: no early release; the grouped item order when
+    // the call asks for it (the deterministic rows pass keeps tile-major)
+    const bool raster = args.raster_rows != 0;
+    auto big = rows ? w4a16_moe_gemm_kernel<false, false, false, true, false, false, true>
+               : glu ? (raster ? w4a16_moe_gemm_kernel<true, true, false, false, false, false, true>
+                               : w4a16_moe_gemm_kernel<true, false, false, false, false, false, true>)
+               : raster ? w4a16_moe_gemm_kernel<false, true, false, false, false, false, true>
+                        : w4a16_moe_gemm_kernel<false, false, false, false, false, false, true>;
     return reinterpret_cast<void*>(big);
   }
   auto kernel =
