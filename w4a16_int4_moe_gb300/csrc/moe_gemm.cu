@@ -581,7 +581,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the gather warp's arrival (+ tensor-copy bytes); the pair leader's
       // also counts the peer's relayed arrival for its half of the rows
       mbar_init(B.bf(i), (kPair && leader) ? 2 : 1);
-      mbar_init(B.be(i), b_steps ? 1 : readers);  // tcgen05.commit of the slot's issuers
+      mbar_init(B.be(i), b_steps ? 2 : readers);  // tcgen05.commit of the slot's issuers
     }
     for (int i = 0; i < kASlots; ++i) {
       // the 4 warps of the slot's dequant warpgroup (of both CTAs of a pair)
@@ -724,16 +724,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     W4A16_PROF_DECL
     if (b_steps) {
-      // Blocks above 128 rows: per item, P = big_block_parts(N) issuers take
-      // part and issuer q takes the k steps ks % P == q into its own partial.
-      // Every issuer walks every item: it reads the item's N, waits until the
-      // previous item's accumulator is released and adds one arrival to the
-      // item's accumulator barrier (the readers by tcgen05.commit). Within an
-      // item each activation slot (BS % 4 == 0) and each A slot has fixed
-      // readers, which alone free it: an activation slot by one commit, an A
-      // slot by two arrivals (a lone issuer adds a plain one to its commit).
-      // The release wait at every item start keeps an issuer that skipped
-      // slots from waiting on a phase two behind or ahead of the barrier.
+      // Blocks above 128 rows: an item of at most 128 rows is split along K,
+      // P = big_block_parts(N) issuers, issuer q taking the k steps
+      // ks % P == q into its own partial; an item above 128 rows along N, two
+      // issuers each taking half of the token columns (0..127, 128..N) of the
+      // one partial. Every issuer walks every item: it reads the item's N,
+      // waits until the previous item's accumulator is released and adds one
+      // arrival to the item's accumulator barrier (the issuers by
+      // tcgen05.commit). Within an item each activation slot (BS % 4 == 0)
+      // and each A slot has fixed readers, which alone free it, by two
+      // arrivals: two readers' commits, or one reader's commit and a plain
+      // arrive. The release wait at every item start keeps an issuer that
+      // skipped slots from waiting on a phase two behind or ahead of the
+      // barrier.
       if (lane == 0) {
         RingPos ip, ap, bp;
         uint32_t acc_phase = 0;  // one accumulator slot
@@ -742,47 +745,63 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int it = unit0; it < items && ok; it += units) {
           const ItemDesc d = decode_item<kRaster, kPair, kLayer>(args, it, num_blocks, bpe, rank);
           if (d.e < 0) continue;
-          if (!wait_phase(B.itf(ip.slot), ip.phase, abort_flag, status, kWhereMmaItem, tmo) ||
-              !wait_phase(B.acce(0), acc_phase ^ 1, abort_flag, status, kWhereMmaAcc, tmo)) {
+          W4A16_PROF_MARK(5);
+          if (!wait_phase(B.itf(ip.slot), ip.phase, abort_flag, status, kWhereMmaItem, tmo)) {
             ok = false;
             break;
           }
+          W4A16_PROF_MARK(0);
+          if (!wait_phase(B.acce(0), acc_phase ^ 1, abort_flag, status, kWhereMmaAcc, tmo)) {
+            ok = false;
+            break;
+          }
+          W4A16_PROF_MARK(1);
           const int n16 = sm.info_n16[ip.slot];
-          const int P = big_block_parts(n16);
+          const bool nsplit = n16 > 128;
+          const int P = nsplit ? 1 : big_block_parts(n16);
           const int nst_i = nstp_of(d);
-          if (q >= P) {
+          if (q >= (nsplit ? 2 : P)) {
             // no MMAs in this item: pass its slots
             mbar_arrive(B.accf(0));
             ap.skip(nst_i, kASlots);
             bp.skip(2 * nst_i, BS);
           } else {
             tc_fence_after();
-            const uint32_t idesc = idesc_bf16_m128(static_cast<uint32_t>(n16));
-            const uint32_t d_tmem = tmem + d_col_base + q * (kBigAccCols / P);
+            // an N split: issuer q takes token columns 128 q.., its rows of the
+            // activation slot start 128 q rows (16 KB) in
+            const uint32_t n_q = nsplit ? (q == 0 ? 128u : static_cast<uint32_t>(n16 - 128))
+                                        : static_cast<uint32_t>(n16);
+            const uint32_t idesc = idesc_bf16_m128(n_q);
+            const uint32_t d_tmem = tmem + d_col_base + (nsplit ? q * 128 : q * (kBigAccCols / P));
+            const uint64_t b_row_off = nsplit ? static_cast<uint64_t>(q) * (128u * 128u >> 4) : 0u;
             const int ks = ksteps_of(d);
             uint32_t acc = 0;
             for (int st = 0; st < nst_i && ok; ++st) {
-              const int r0 = (2 * st) & (P - 1), r1 = (2 * st + 1) & (P - 1);
+              const int r0 = nsplit ? q : (2 * st) & (P - 1);
+              const int r1 = nsplit ? q : (2 * st + 1) & (P - 1);
               if (r0 != q && r1 != q) {
                 ap.next(kASlots);
                 bp.skip(2, BS);
                 continue;
               }
+              W4A16_PROF_MARK(5);
               if (!wait_phase(B.af(ap.slot), ap.phase, abort_flag, status, kWhereMmaA, tmo)) {
                 ok = false;
                 break;
               }
+              W4A16_PROF_MARK(2);
               for (int j = 0; j < 2; ++j, bp.next(BS)) {
                 if ((j ? r1 : r0) != q) continue;
                 if (!wait_phase(B.bf(bp.slot), bp.phase, abort_flag, status, kWhereMmaB, tmo)) {
                   ok = false;
                   break;
                 }
+                W4A16_PROF_MARK(3);
                 tc_fence_after();
                 if (2 * st + j < ks) {
                   // slot offsets are multiples of 1024 bytes
                   const uint64_t b_desc =
-                      b_desc0 + ((static_cast<uint32_t>(bp.slot) * b_step_bytes) >> 4);
+                      b_desc0 + ((static_cast<uint32_t>(bp.slot) * b_step_bytes) >> 4) + b_row_off;
                   const uint32_t a_tmem = tmem + ap.slot * kAColsPerSlot + j * kAColsPerStep;
 #pragma unroll
                   for (int kk = 0; kk < 4; ++kk) {
@@ -790,12 +809,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     acc = 1;
                   }
                 }
+                W4A16_PROF_MARK(4);
+                // two arrivals per slot: a lone reader adds a plain one
+                if (!nsplit) mbar_arrive(B.be(bp.slot));
                 tc_commit(B.be(bp.slot));
+                W4A16_PROF_MARK(6);
               }
               if (!ok) break;
-              // the slot expects two arrivals: a lone issuer adds a plain one
-              if (P == 1) mbar_arrive(B.ae(ap.slot));
               tc_commit(B.ae(ap.slot));
+              W4A16_PROF_MARK(6);
               ap.next(kASlots);
             }
             if (!ok) break;
