@@ -27,7 +27,8 @@ def _fused_and_unfused(p, device, bm=None, cta_pair=0):
                           p.tok_e_hint())
     if bm:
         plan.block_m = bm
-        plan.stages, plan.b_stages = min(plan.stages, 8), 8   # fit larger token stages
+        # fit larger token stages (256 rows: four single-k-step slots)
+        plan.stages, plan.b_stages = min(plan.stages, 8), (4 if bm > 128 else 8)
     plan.cta_pair = cta_pair
     sid, eid, ntp = ops.w4a16_moe_align_block_size(dev(p.topk_ids, device), p.num_experts,
                                                    plan.block_m)
@@ -48,7 +49,7 @@ def _fused_and_unfused(p, device, bm=None, cta_pair=0):
     return bf16_bits(g), bf16_bits(act_ref), bf16_bits(act), routed
 
 
-@pytest.mark.parametrize("bm", [16, 32, 64])
+@pytest.mark.parametrize("bm", [16, 32, 64, 256])
 def test_fused_activation_tiny(cuda_dev, bm):
     p = wl.tiny(seed=51)
     g_bits, ref_bits, act_bits, routed = _fused_and_unfused(p, cuda_dev, bm)
@@ -71,6 +72,17 @@ def test_fused_activation_pair(cuda_dev, bm):
     # CTA pairs: the fused epilogue of each CTA's tile gives the unfused bits
     p = wl.tiny(seed=53)
     g_bits, ref_bits, act_bits, routed = _fused_and_unfused(p, cuda_dev, bm, cta_pair=1)
+    np.testing.assert_array_equal(act_bits[routed], ref_bits[routed])
+
+
+def test_fused_activation_256_row_blocks(cuda_dev):
+    # 256-row blocks with items of every kind: K split over 4 or 2 issuers
+    # (at most 64 / 128 rows) and N split over 2 (above 128 rows)
+    p = wl.uniform_problem(640, 1024, 256, 5, 2, seed=55)    # ~256 rows per expert
+    p.topk_ids[290:][p.topk_ids[290:] == 4] = -1             # expert 4: 65..128 rows
+    counts = np.bincount(p.topk_ids[p.topk_ids >= 0], minlength=5)
+    assert counts.max() > 256 and (counts % 256 <= 64).any() and 64 < counts[4] <= 128
+    g_bits, ref_bits, act_bits, routed = _fused_and_unfused(p, cuda_dev, 256)
     np.testing.assert_array_equal(act_bits[routed], ref_bits[routed])
 
 

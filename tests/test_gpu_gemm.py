@@ -233,6 +233,27 @@ def _down_det(p, packed, routing, plan, act_bits, device, out=None, accumulate=F
     return out
 
 
+def test_down_deterministic_256_row_blocks(cuda_dev):
+    # the deterministic pass on 256-row blocks (items of 1-4 issuers): the
+    # same bits for any grid, the oracle's values, 0 for a token without a
+    # local expert
+    p = wl.uniform_problem(512, 1024, 512, 6, 3, seed=66)   # ~256 rows per expert
+    p.topk_ids[200:][p.topk_ids[200:] == 5] = -1             # expert 5: 65..128 rows
+    p.topk_ids[7, :] = -1
+    counts = np.bincount(p.topk_ids[p.topk_ids >= 0], minlength=6)
+    assert counts.max() > 256 and 64 < counts[5] <= 128
+    pk = _pack(p.q_dn, p.s_dn, cuda_dev)
+    a_bits = wl.random_activations(np.random.default_rng(67), p.numel, p.inter)
+    a_bits[~_routed(p)] = 0
+    ref = oracle.indexed_down(a_bits, p.topk_ids, p.topk_weights, p.q_dn, p.s_dn)
+    routing = _routing(p.topk_ids, p.num_experts, 256, cuda_dev)
+    outs = [_down_det(p, pk, routing, _plan(256, p.hidden, p.inter, grid=g), a_bits,
+                      cuda_dev).cpu().numpy() for g in (0, 5)]
+    np.testing.assert_array_equal(outs[1].view(np.uint32), outs[0].view(np.uint32))
+    assert np.all(outs[0][7] == 0.0)
+    assert_close(outs[0], ref, "deterministic down, 256-row blocks")
+
+
 def test_down_deterministic(cuda_dev):
     # W4A16_FLAG_DETERMINISTIC: each weighted row goes to the workspace and a
     # second kernel adds every token's rows in top-k slot order. The output

@@ -1644,11 +1644,11 @@ void* pick_kernel(const GemmArgs& args) {
   const bool early = early_epilogue(args.block_m);
   if (!kPair && b_per_step(args.block_m)) {
     // blocks above 128 rows: no early release; the grouped item order when
-    // the call asks for it (the deterministic rows pass keeps tile-major)
+    // the call asks for it (every indexed call does; the fused activation
+    // exists only there, and the deterministic rows pass keeps tile-major)
     const bool raster = args.raster_rows != 0;
     auto big = rows ? w4a16_moe_gemm_kernel<false, false, false, true, false, false, true>
-               : glu ? (raster ? w4a16_moe_gemm_kernel<true, true, false, false, false, false, true>
-                               : w4a16_moe_gemm_kernel<true, false, false, false, false, false, true>)
+               : glu ? w4a16_moe_gemm_kernel<true, true, false, false, false, false, true>
                : raster ? w4a16_moe_gemm_kernel<false, true, false, false, false, false, true>
                         : w4a16_moe_gemm_kernel<false, false, false, false, false, false, true>;
     return reinterpret_cast<void*>(big);
