@@ -406,6 +406,17 @@ def test_grouped_contiguous_small(cuda_dev, bm):
     assert_close(got[valid], ref[valid], f"contiguous bm={bm}")
 
 
+@pytest.mark.parametrize("bm,n", [(128, 198), (64, 198), (128, 130)])
+def test_grouped_contiguous_width_not_multiple_of_4(cuda_dev, bm, n):
+    # output rows whose width is not a multiple of 4 take the scalar stores
+    # of the staged epilogue (128 rows: BF16 staging; 64 rows: FP32)
+    gp = wl.grouped_contiguous_problem([5, 128, 0, 77], num_experts=4, n=n, k=96, seed=n + bm)
+    got = _grouped(gp, cuda_dev, _plan(bm, gp.n, gp.k))
+    ref = oracle.grouped_contiguous(gp.a, gp.layout, gp.q, gp.s)
+    valid = gp.layout >= 0
+    assert_close(got[valid], ref[valid], f"contiguous bm={bm} n={n}")
+
+
 @pytest.mark.parametrize("bm", [16, 32])
 def test_grouped_masked_small(cuda_dev, bm):
     gp = wl.grouped_masked_problem(num_experts=6, max_m=32, n=256, k=160, seed=bm)

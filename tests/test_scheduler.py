@@ -48,7 +48,8 @@ def test_plan_ignores_total_tokens_given_tok_e():
 
 # the five workload families, as the bench runs them
 CASES = {
-    # name: (plan, k, expected block_m, issuers, accumulator slots, early epilogue)
+    # name: (plan, k, expected block_m, issuers, accumulator slots, early epilogue
+    # (for 65..128-row blocks: with a BF16 output, so not the down pass itself))
     "tiny": (lambda: _plan(64, 2, 8, 1024, 512, 16.0), 512, 32, 4, 2, 0),
     "ep8_decode gate_up": (lambda: _plan(576, 8, 48, 2 * I, H, 12.0), H, 32, 4, 2, 0),
     "ep8_decode down": (lambda: _plan(576, 8, 48, H, I, 12.0), I, 32, 4, 2, 0),
@@ -60,18 +61,18 @@ CASES = {
     # four times the EP8 prefill rows (tok_e 325): gate_up 256-row blocks,
     # four issuer threads of which an item uses 1, 2 or 4; down 128 rows
     "heavy prefill gate_up": (lambda: _plan(32768, 8, 48, 2 * I, H, 325.3), H, 256, 4, 1, 0),
-    "heavy prefill down": (lambda: _plan(32768, 8, 48, H, I, 325.3), I, 128, 1, 2, 0),
+    "heavy prefill down": (lambda: _plan(32768, 8, 48, H, I, 325.3), I, 128, 1, 2, 1),
     "grouped contiguous 128": (
         lambda: ops.w4a16_grouped_plan(ops.W4A16_GROUPED_CONTIGUOUS, 48 * 128, 2 * I, H, 128),
-        H, 128, 2, 1, 0),
+        H, 128, 2, 1, 1),
     # 128-row blocks: two issuers over k = 7168, one issuer and two slots over
     # the down projection's k = 2048 (the epilogue overlaps the next item)
     "grouped contiguous 1024 gate_up": (
         lambda: ops.w4a16_grouped_plan(ops.W4A16_GROUPED_CONTIGUOUS, 48 * 1024, 2 * I, H, 1024),
-        H, 128, 2, 1, 0),
+        H, 128, 2, 1, 1),
     "grouped contiguous 1024 down": (
         lambda: ops.w4a16_grouped_plan(ops.W4A16_GROUPED_CONTIGUOUS, 48 * 1024, H, I, 1024),
-        I, 128, 1, 2, 0),
+        I, 128, 1, 2, 1),
     "grouped masked 32": (
         lambda: ops.w4a16_grouped_plan(ops.W4A16_GROUPED_MASKED, 32, 2 * I, H, 16),
         H, 32, 4, 2, 0),

@@ -309,7 +309,8 @@ w4a16_status w4a16_plan_info(const w4a16_plan_t* plan, int k, w4a16_plan_info_t*
   out->mma_issuers = activation_slot_is_step(plan->block_m) ? 4 : pl.parts;
   out->acc_slots = pl.d_slots;
   out->acc_cols = pl.d_cols;
-  out->early_epilogue = early_epilogue(plan->block_m) ? 1 : 0;
+  // (blocks of 65..128 rows free it early for a BF16 output only)
+  out->early_epilogue = early_epilogue(plan->block_m, kOutBf16, plan->cta_pair != 0) ? 1 : 0;
   out->w_stages = pl.w_stages;
   out->b_stages = pl.b_stages;
   out->smem_bytes = pl.smem;

@@ -149,7 +149,8 @@ int max_pair_clusters(const GemmArgs& args);
 // issuers) and of accumulator slots.
 // False when even one accumulator does not fit.
 bool tmem_accumulators(int block_m, int k_steps, int* d_cols, int* parts, int* d_slots);
-bool early_epilogue(int block_m);
+// The epilogue frees the accumulator slot before its global stores.
+bool early_epilogue(int block_m, int out_mode, bool pair);
 // 2-D map of BF16 [rows, k] (box 64 x box_rows, 128-byte swizzle).
 bool encode_act_tmap(CUtensorMap* map, const void* act, long long rows, int k, int box_rows);
 // 3-D map of the permuted rows [rows, k_pad]: dims (64 columns, rows, k_pad /

@@ -103,6 +103,15 @@ __host__ __device__ constexpr int epi_stage_rows(int block_m) {
 __host__ __device__ constexpr int epi_tile_bytes(int block_m) {
   return 4 * epi_stage_rows(block_m) * 32 * 4;  // 4 epilogue warps x rows x 32 FP32
 }
+// Blocks of 65..128 rows with a BF16 output stage the whole block as BF16
+// (32 KB at 128 rows, a region of its own after the rest of the carve-up), so
+// that their accumulator slot, the only one, is freed before the stores too.
+__host__ __device__ constexpr bool epi_half_stage(int block_m) {
+  return block_m > 64 && block_m <= 128;
+}
+__host__ __device__ constexpr int epi_half_bytes(int block_m) {
+  return epi_half_stage(block_m) ? 4 * block_m * 32 * 2 : 0;  // 4 warps x rows x 32 BF16
+}
 // Blocks above 128 rows: one 64-k step of token rows is up to 32 KB, so the
 // activation ring holds single k steps (two stage-sized slots would leave
 // room for too few in flight), and the one MMA issuer waits on each k step.
@@ -148,6 +157,7 @@ struct Smem {
   uint64_t* bars;
   uint32_t* tmem_base;
   volatile int* abort_flag;
+  __nv_bfloat16* epi_half;  // (kEarly) [4 warps][block_m token rows][32]: BF16 staging
 };
 
 // mbarrier addresses (shared-window offsets, 8 bytes each)
@@ -482,12 +492,13 @@ __device__ __forceinline__ void dequant_group(const uint4 q, uint32_t scale_bits
 // slot before its stores (blocks of 48 or 64 rows, whose accumulators fill
 // TMEM's single slot), and kRows: the deterministic down pass (out_mode
 // kOutF32Rows), kPair: the CTA-pair kernel, kLayer: the single-launch
-// layer (gate_up items, then down items), and kBig: blocks above 128 rows
-// are compiled into their own instantiations so that they cannot change the
+// layer (gate_up items, then down items), kBig: blocks above 128 rows, and
+// kHalf: the BF16 staging of 65..128-row blocks are compiled into their own
+// instantiations so that they cannot change the
 // register allocation or the instruction footprint of the plain kernel
 // (compiled into it, the 256-row code made the TP8 down pass 18% slower).
 template <bool kGlu, bool kRaster, bool kEarly, bool kRows, bool kPair, bool kLayer = false,
-          bool kBig = false>
+          bool kBig = false, bool kHalf = false>
 __global__ void __launch_bounds__(kThreads, 1)
     w4a16_moe_gemm_kernel(const __grid_constant__ GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
@@ -542,6 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   sm.tmem_base = reinterpret_cast<uint32_t*>(base + off);
   off += 4;
   sm.abort_flag = reinterpret_cast<volatile int*>(base + off);
+  if constexpr (kHalf) sm.epi_half = reinterpret_cast<__nv_bfloat16*>(base + align_up(off + 4, 16));
 
   Bars B;
   {
@@ -1203,9 +1215,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // whole block fits (stage_rows), one pass first moves every partial sum
         // out of TMEM and frees the accumulator slot, so that the next item's
         // MMAs overlap this item's stores; otherwise each 16-row pass is staged
-        // and written, and the slot is freed at the end.
-        const bool early = rows <= stage_rows;  // (kEarly launches only)
-        const int pass_rows = early ? stage_rows : 16;
+        // and written, and the slot is freed at the end. A 65..128-row block
+        // with a BF16 output (half_stage) is staged whole as BF16 in tile_h.
+        constexpr bool half_stage = kHalf && !kGlu && !kRows;
+        __nv_bfloat16* tile_h = half_stage ? sm.epi_half + quarter * (bm * 32) : nullptr;
+        const int stage_rows_e = half_stage ? bm : stage_rows;
+        const bool early = rows <= stage_rows_e;  // (kEarly launches only)
+        const int pass_rows = early ? stage_rows_e : 16;
         for (int p0 = 0; p0 < rows; p0 += pass_rows) {
           const int p1 = min(rows, p0 + pass_rows);
           for (int j0 = p0; j0 < p1; j0 += 16) {
@@ -1248,6 +1264,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 slab[(2 * m + (hi_lane ? 1 : 0)) * 16 + (lane & 15)] =
                     __fdividef(g, 1.0f + __expf(-g)) * u;
               }
+            } else if (half_stage) {
+              // transposed and rounded to the BF16 the output holds
+              __nv_bfloat16* slab_h = tile_h + (j0 - p0) * 32;
+#pragma unroll
+              for (int jj = 0; jj < 16; ++jj)
+                slab_h[jj * 32 + lane] = __float2bfloat16_rn(__uint_as_float(v[jj]));
             } else {
               // transposed: slab[jj][lane] = value of token column j0 + jj for
               // weight row lane
@@ -1284,6 +1306,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int j = j0 + jr;
                 const int dr = idst[j];
                 if (dr < 0 || ng >= args.n) continue;
+                if (half_stage) {
+                  const uint2 pk =
+                      *reinterpret_cast<const uint2*>(tile_h + (j - p0) * 32 + 4 * c4);
+                  __nv_bfloat16* o = static_cast<__nv_bfloat16*>(args.out) +
+                                     static_cast<long long>(dr) * args.n + ng;
+                  if (vec4) {
+                    *reinterpret_cast<uint2*>(o) = pk;
+                  } else {
+                    const __nv_bfloat16* hv = reinterpret_cast<const __nv_bfloat16*>(&pk);
+                    o[0] = hv[0];
+                    if (ng + 1 < args.n) o[1] = hv[1];
+                    if (ng + 2 < args.n) o[2] = hv[2];
+                    if (ng + 3 < args.n) o[3] = hv[3];
+                  }
+                  continue;
+                }
                 const float4 x = *reinterpret_cast<const float4*>(slab + jr * 32 + 4 * c4);
                 if constexpr (kRows) {
                   // deterministic down pass: the weighted row at its routing position
@@ -1544,12 +1582,17 @@ size_t gemm_smem_bytes(int block_m, int w_stages, int b_stages, bool pair) {
   off = (off + 7) / 8 * 8;
   off += (2 * w_stages + 2 * b_stages + kNumBarsFixed) * 8;
   off += 8;
+  // the BF16 staging of 65..128-row blocks (unpaired), 16-byte aligned
+  if (!pair && epi_half_stage(block_m)) off = (off + 15) / 16 * 16 + epi_half_bytes(block_m);
   return off;
 }
 
 // The epilogue that frees the accumulator slot before its stores: exactly
-// the block sizes whose staging tile holds a whole block.
-bool early_epilogue(int block_m) { return epi_stage_rows(block_m) > 16; }
+// the launches whose staging tile holds a whole block (48..64 rows in FP32;
+// 65..128 rows in BF16 when the output is BF16, unpaired).
+bool early_epilogue(int block_m, int out_mode, bool pair) {
+  return epi_stage_rows(block_m) > 16 || (epi_half_stage(block_m) && out_mode == kOutBf16 && !pair);
+}
 
 bool tmem_accumulators(int block_m, int k_steps, int* d_cols, int* parts, int* d_slots) {
   const int dcols = (block_m + 31) / 32 * 32;
@@ -1641,7 +1684,14 @@ template <bool kPair>
 void* pick_kernel(const GemmArgs& args) {
   const bool glu = args.out_mode == kOutGluBf16;
   const bool rows = args.out_mode == kOutF32Rows;
-  const bool early = early_epilogue(args.block_m);
+  const bool early = early_epilogue(args.block_m, args.out_mode, kPair);
+  if (!kPair && early && epi_half_stage(args.block_m)) {
+    // 65..128-row blocks with a BF16 output: the BF16 staging tile
+    auto half = args.raster_rows
+                    ? w4a16_moe_gemm_kernel<false, true, true, false, false, false, false, true>
+                    : w4a16_moe_gemm_kernel<false, false, true, false, false, false, false, true>;
+    return reinterpret_cast<void*>(half);
+  }
   if (!kPair && b_per_step(args.block_m)) {
     // blocks above 128 rows: no early release; the grouped item order when
     // the call asks for it (every indexed call does; the fused activation
@@ -1676,7 +1726,7 @@ int max_pair_clusters(const GemmArgs& args) {
   // CTA pairs that can be resident at once (a pair needs two SMs of one GPC)
   static std::mutex mu;
   static int cache[8][2] = {};
-  const bool early = early_epilogue(args.block_m);
+  const bool early = early_epilogue(args.block_m, args.out_mode, true);
   const int key = (args.out_mode == kOutGluBf16 ? 4 : 0) + (args.raster_rows ? 2 : 0) + (early ? 1 : 0);
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
