@@ -564,13 +564,24 @@ w4a16_status w4a16_moe_grouped_gemm(int kind, const void* packed, int num_expert
   g.n_tiles = packed_tiles(n);
   g.k_steps = packed_ksteps(k);
   g.act = a;
-  g.gather_rows = 0;
   g.act_rows = static_cast<int>(rows_total);
   const bool pair = plan->cta_pair != 0 && g.n_tiles % 2 == 0;
-  if (!encode_act_tmap(&g.tmap, a, rows_total, k, activation_box_rows(bm, pair)) ||
-      (!pair && activation_slot_is_step(bm) &&
-       !encode_act_tmap(&g.tmap2, a, rows_total, k, kActivationBoxRowsSmall)))
+  const bool step_slots = !pair && activation_slot_is_step(bm);
+  // k a multiple of 64 (two-step slots): the rows seen as the 3-D array
+  // (64 columns, rows, k / 64), so that one tensor copy brings both k steps
+  // of a stage, as for the indexed family's permuted rows (grouped masked,
+  // budget 32: gate_up 236 -> 208 us, down 126 -> 113 us); else one 2-D copy
+  // per k step
+  const bool two_step_copies = !step_slots && k % kKStep == 0;
+  g.gather_rows = two_step_copies ? 1 : 0;
+  if (two_step_copies) {
+    if (!encode_permuted_tmap(&g.tmap, a, rows_total, k, activation_box_rows(bm, pair), 2))
+      return W4A16_ERR_CUDA;
+  } else if (!encode_act_tmap(&g.tmap, a, rows_total, k, activation_box_rows(bm, pair)) ||
+             (step_slots &&
+              !encode_act_tmap(&g.tmap2, a, rows_total, k, kActivationBoxRowsSmall))) {
     return W4A16_ERR_CUDA;
+  }
   g.family = kind == W4A16_GROUPED_CONTIGUOUS ? kContiguous : kMasked;
   g.out_mode = kOutBf16;
   g.layout = layout;

@@ -62,12 +62,13 @@ __host__ __device__ inline int packed_source_row(int n, int layout, int tile, in
 }
 
 struct GemmArgs {
-  // Activation tensor map: the permuted rows of the indexed family (3-D,
-  // two k steps per box) or the rows of the grouped families (2-D, one k step
-  // per box); box rows = block_m, 128-byte swizzle.
+  // Activation tensor map: the permuted rows of the indexed family, or the
+  // rows of a grouped family when k % 64 == 0, as a 3-D array (two k steps
+  // per box); else the rows of a grouped family (2-D, one k step per box);
+  // box rows = block_m, 128-byte swizzle.
   CUtensorMap tmap;
   int act_rows;
-  int gather_rows;  // 1: routed rows (indexed family), 0: consecutive rows
+  int gather_rows;  // 1: the 3-D map (two k steps per copy), 0: the 2-D map
   const uint8_t* wpack;
   long long expert_bytes;
   int num_experts, n, k, n_tiles, k_steps;
