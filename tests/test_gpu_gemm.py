@@ -428,6 +428,19 @@ def test_grouped_masked_small(cuda_dev, bm):
     assert_close(got[valid], ref[valid], f"masked bm={bm}")
 
 
+@pytest.mark.parametrize("k", [160, 192])
+def test_grouped_masked_256_row_blocks(cuda_dev, k):
+    # a 300-row budget on 256-row blocks: two blocks per expert, items of
+    # every issuer split (N <= 64, <= 128 and above), one k step per copy
+    # (k = 32 mod 64 gives a pad k step)
+    gp = wl.grouped_masked_problem(num_experts=5, max_m=300, n=256, k=k, seed=k)
+    gp.layout[:] = [300, 40, 0, 100, 257]
+    got = _grouped(gp, cuda_dev, _plan(256, gp.n, gp.k))
+    ref = oracle.grouped_masked(gp.a, gp.layout, gp.q, gp.s)
+    valid = ~np.isnan(ref[..., 0])
+    assert_close(got[valid], ref[valid], f"masked bm=256 k={k}")
+
+
 # ------------------------------------------------- full-size shard shapes --
 
 @functools.lru_cache(maxsize=1)
