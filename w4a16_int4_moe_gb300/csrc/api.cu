@@ -477,9 +477,11 @@ w4a16_status indexed_gemm(int mode, const void* packed, int num_experts, int n, 
   // tile pass would read them from DRAM again (EP8 prefill at four times the
   // rows: 5.7 GB of DRAM reads per gate_up launch); grouped in blocks of 8,
   // a group's rows stay in L2 across its tiles
-  // ... and 48/64-row blocks over a long reduction (the EP8 prefill gate_up:
-  // its 78 MB of routed rows are re-read per tile pass in tile-major order)
-  g.raster_rows = (step_slots || (!pair && bm > 32 && bm <= 64 && k > 2048)) ? 1 : 0;
+  // ... and blocks of 48..128 rows over a long reduction: the routed rows
+  // of a prefill gate_up (EP8 prefill: 78 MB) are re-read per tile pass in
+  // tile-major order (EP8 prefill gate_up 379 -> 368.5 us; 128-row blocks at
+  // tok_e 163: 652 -> 557 us)
+  g.raster_rows = (step_slots || (!pair && bm > 32 && k > 2048)) ? 1 : 0;
   g.timeout_cycles = wait_timeout_cycles();
   g.pair = pair ? 1 : 0;
   long long grid = plan->grid > 0 ? plan->grid : static_cast<long long>(sms) * plan->ctas_per_sm;
