@@ -126,10 +126,9 @@ typedef struct {
  * tok_e_hint > 0 overrides the expected rows per expert (default
  * tokens * topk / num_experts); it is known on the host without a sync.
  * block_m from tok_e: up to 80, roundup16(1.5 tok_e) within 16..64; then 64
- * below 120, 128, and 256 from 200 when k > 2048. The two GEMMs of a layer
- * may so get different block sizes (each call takes routing aligned to its
- * own plan's block_m). Host only. Errors: INVALID_ARG on non-positive sizes
- * or a NULL out.
+ * below 120, else 128 (256-row blocks are accepted in a plan the caller
+ * sets; each call takes routing aligned to its own plan's block_m). Host
+ * only. Errors: INVALID_ARG on non-positive sizes or a NULL out.
  */
 w4a16_status w4a16_plan(int tokens, int topk, int num_experts, int n, int k,
                         float tok_e_hint, w4a16_plan_t* out);

@@ -53,8 +53,8 @@ def test_plan_follows_tok_e(lib):
     assert ops.w4a16_plan(16, 8, 384, 512, 7168).block_m == 16
     # prefill above the ~80 rows/expert switch
     assert ops.w4a16_plan(8192, 8, 384, 4096, 7168, 81.3).block_m == 64
-    # heavy prefill: 256-row blocks for the long gate_up reduction, 128 for down
-    assert ops.w4a16_plan(8192, 8, 48, 4096, 7168, 600.0).block_m == 256
+    # heavy prefill: 128-row blocks for both GEMMs
+    assert ops.w4a16_plan(8192, 8, 48, 4096, 7168, 600.0).block_m == 128
     assert ops.w4a16_plan(8192, 8, 48, 7168, 2048, 600.0).block_m == 128
     for tok_e in (0.3, 5, 12, 40, 80, 81, 150, 400):
         p = ops.w4a16_plan(1024, 8, 48, 4096, 7168, float(tok_e))
@@ -81,7 +81,11 @@ def test_plan_ring_depths():
     heavy_dn = ops.w4a16_plan(8192, 8, 48, 7168, 2048, 300.0)
     assert (heavy_dn.block_m, heavy_dn.b_stages, heavy_dn.stages) == (128, 8, 4)
     heavy_gu = ops.w4a16_plan(8192, 8, 48, 4096, 7168, 300.0)
-    assert (heavy_gu.block_m, heavy_gu.b_stages, heavy_gu.stages) == (256, 4, 8)
+    assert (heavy_gu.block_m, heavy_gu.b_stages, heavy_gu.stages) == (128, 8, 4)
+    # a 256-row plan set by the caller: 4 single-step slots and 8 weight stages
+    big = ops.Plan.from_buffer_copy(heavy_gu)
+    big.block_m, big.b_stages, big.stages = 256, 4, 8
+    assert ops.w4a16_plan_info(big, 7168).smem_bytes <= 227 * 1024
 
 
 def test_plan_rejects_bad_sizes(lib):

@@ -350,11 +350,11 @@ def test_layer_forward_and_graph_capture(cuda_dev):
 
 
 @pytest.mark.parametrize("from_logits", [False, True])
-def test_layer_with_different_blocks_per_gemm(cuda_dev, from_logits):
-    # tok_e 256 over a long gate_up reduction (k = 4096) and a short down one
-    # (k = 256): gate_up takes 256-row blocks, down 128, each on its own
-    # routing; experts of a little under or over 256 rows give items of 1
-    # issuer and of 4 (a short second block); the result is the oracle layer's
+def test_layer_with_different_blocks_per_gemm(cuda_dev, from_logits, monkeypatch):
+    # gate_up (k = 4096) on 256-row blocks, down (k = 256) on 128, each on its
+    # own routing (the plan of the long reduction is set to 256 rows here);
+    # experts of a little under or over 256 rows give items of 1 issuer and of
+    # 4 (a short second block); the result is the oracle layer's
     rng = np.random.default_rng(23)
     tokens, hidden, inter, experts, topk = 512, 4096, 256, 8, 4
     logits = rng.standard_normal((tokens, experts)).astype(np.float32)
@@ -366,6 +366,15 @@ def test_layer_with_different_blocks_per_gemm(cuda_dev, from_logits):
                                                dev(p.s_gu.view(np.int16), cuda_dev))
     dn = moe_mod.PackedExperts.from_checkpoint(dev(p.q_dn, cuda_dev),
                                                dev(p.s_dn.view(np.int16), cuda_dev))
+    plan = ops.w4a16_plan
+
+    def gate_up_on_256_rows(tokens_, topk_, experts_, n_, k_, hint_=0.0):
+        p_ = plan(tokens_, topk_, experts_, n_, k_, hint_)
+        if k_ == hidden:
+            p_.block_m, p_.b_stages, p_.stages = 256, 4, 8
+        return p_
+
+    monkeypatch.setattr(ops, "w4a16_plan", gate_up_on_256_rows)
     layer = moe_mod.W4A16MoE(gu, dn, topk, tokens, tok_e_hint=256.0)
     assert (layer.block_m, layer.block_m_dn) == (256, 128)
     x = bf16_tensor(p.x, cuda_dev)
@@ -481,16 +490,19 @@ def test_ep8_prefill_full_size(cuda_dev):
 
 
 @pytest.mark.slow
-def test_ep8_prefill_heavy_full_size(cuda_dev):
-    # four times the prefill rows (tok_e 80 .. 2400): gate_up on 256-row
-    # blocks (items of 1, 2 or 4 issuers by their rows), down on 128
+@pytest.mark.parametrize("bm", [128, 256])
+def test_ep8_prefill_heavy_full_size(cuda_dev, bm):
+    # four times the prefill rows (tok_e 80 .. 2400): the scheduler's 128-row
+    # blocks, and gate_up on 256-row blocks (items of 1, 2 or 4 issuers by
+    # their rows; a plan the caller sets) with down on 128
     p = wl.ep8_prefill(scale=4)
     hint = p.tok_e_hint()
-    bm = ops.w4a16_plan(p.tokens, p.topk, p.num_experts, 2 * p.inter, p.hidden, hint).block_m
-    bm_dn = ops.w4a16_plan(p.tokens, p.topk, p.num_experts, p.hidden, p.inter, hint).block_m
-    assert (bm, bm_dn) == (256, 128)
+    assert ops.w4a16_plan(p.tokens, p.topk, p.num_experts, 2 * p.inter, p.hidden,
+                          hint).block_m == 128
+    assert ops.w4a16_plan(p.tokens, p.topk, p.num_experts, p.hidden, p.inter,
+                          hint).block_m == 128
     _check_pair(p, cuda_dev, bm, cols_gu=_sample_cols(4096, 96, 7),
-                cols_dn=_sample_cols(7168, 96, 8), what="EP8 prefill x4", bm_dn=bm_dn)
+                cols_dn=_sample_cols(7168, 96, 8), what=f"EP8 prefill x4 bm={bm}", bm_dn=128)
 
 
 @pytest.mark.slow

@@ -18,6 +18,13 @@ def _plan(tokens, topk, experts, n, k, hint=0.0):
     return ops.w4a16_plan(tokens, topk, experts, n, k, hint)
 
 
+def _with(plan, **fields):
+    p = ops.Plan.from_buffer_copy(plan)
+    for f, v in fields.items():
+        setattr(p, f, v)
+    return p
+
+
 @pytest.mark.parametrize("tok_e,block_m", [
     (0.3, 16), (5.3, 16), (10.0, 16), (10.66, 16),  # 1.5 tok_e <= 16
     (10.7, 32),
@@ -25,8 +32,7 @@ def _plan(tokens, topk, experts, n, k, hint=0.0):
     (22.0, 48), (32.0, 48),
     (33.0, 64), (80.0, 64),                         # capped at 64
     (80.1, 64), (119.0, 64),                        # above the switch (EP8 prefill: 81)
-    (120.0, 128), (199.0, 128),
-    (200.0, 256), (600.0, 256),                     # long reduction (k = 7168)
+    (120.0, 128), (199.0, 128), (200.0, 128), (600.0, 128),
 ])
 def test_block_m_follows_tok_e(tok_e, block_m):
     assert _plan(1, 1, 1, 4096, H, tok_e).block_m == block_m
@@ -34,8 +40,8 @@ def test_block_m_follows_tok_e(tok_e, block_m):
 
 @pytest.mark.parametrize("tok_e,block_m", [(100.0, 64), (150.0, 128), (200.0, 128),
                                            (600.0, 128)])
-def test_short_reductions_stop_at_128(tok_e, block_m):
-    # the down projection (k = 2048) keeps 128-row blocks at any tok_e
+def test_both_projections_get_the_same_blocks(tok_e, block_m):
+    # the down projection (k = 2048) follows the same rule
     assert _plan(1, 1, 1, H, I, tok_e).block_m == block_m
 
 
@@ -58,10 +64,13 @@ CASES = {
     "tp8 T=256 gate_up": (lambda: _plan(256, 8, 384, 512, H), H, 16, 4, 2, 0),
     "ep8_prefill gate_up": (lambda: _plan(8192, 8, 48, 2 * I, H, 81.33), H, 64, 4, 1, 1),
     "ep8_prefill down": (lambda: _plan(8192, 8, 48, H, I, 81.33), I, 64, 4, 1, 1),
-    # four times the EP8 prefill rows (tok_e 325): gate_up 256-row blocks,
-    # four issuer threads of which an item uses 1, 2 or 4; down 128 rows
-    "heavy prefill gate_up": (lambda: _plan(32768, 8, 48, 2 * I, H, 325.3), H, 256, 4, 1, 0),
+    # four times the EP8 prefill rows (tok_e 325): 128-row blocks for both
+    "heavy prefill gate_up": (lambda: _plan(32768, 8, 48, 2 * I, H, 325.3), H, 128, 2, 1, 1),
     "heavy prefill down": (lambda: _plan(32768, 8, 48, H, I, 325.3), I, 128, 1, 2, 1),
+    # a 256-row plan the caller sets: four issuer threads, of which an item
+    # uses 1, 2 or 4, over one 256-column accumulator slot
+    "256-row plan": (lambda: _with(_plan(32768, 8, 48, 2 * I, H, 325.3), block_m=256,
+                                   b_stages=4, stages=8), H, 256, 4, 1, 0),
     "grouped contiguous 128": (
         lambda: ops.w4a16_grouped_plan(ops.W4A16_GROUPED_CONTIGUOUS, 48 * 128, 2 * I, H, 128),
         H, 128, 2, 1, 1),

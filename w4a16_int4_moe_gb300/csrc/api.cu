@@ -173,22 +173,21 @@ w4a16_status w4a16_plan(int tokens, int topk, int num_experts, int n, int k, flo
   // above it the block is sized by padded expert rows. The MMA N of a block
   // is its real row count rounded to 16, so padding costs no tensor time.
   // Above the switch (GB300 measurements, 48 local experts): 64-row blocks
-  // up to tok_e 120 (the skewed EP8 prefill shard, tok_e 81: 64 -> 634 us per
-  // layer, 128 -> 776, 256 -> 1037); 128-row blocks from 120 (uniform tok_e
-  // 128: gate_up 410 vs 461 us at 64); from 200, for long reductions (k >
-  // 2048), 256-row blocks, whose items of more than 128 rows issue M = 128,
-  // N up to 256 MMAs from one thread (uniform tok_e 256: gate_up 742 vs 859
-  // us at 128; tok_e 512: 1601 vs 2064). Short reductions keep 128: their
-  // items are too short to hide the epilogue behind a single 256-column
-  // accumulator (down at tok_e 512: 1099 us at 256, 875 at 128).
+  // up to tok_e 120 (the skewed EP8 prefill shard, tok_e 81: layer 624 us at
+  // 64, 697 at 128; uniform tok_e 128: 686 at 64, 576 at 128), then 128-row
+  // blocks, whose BF16-staged
+  // epilogue frees the accumulator before the stores and whose long
+  // reductions take the grouped item order. They also beat 256-row blocks
+  // (one 256-column accumulator slot, single-k-step activation slots) at
+  // every heavier shape measured: gate_up at uniform tok_e 256 657 vs 708
+  // us, at four times the EP8 prefill rows 967 vs 1132, at uniform tok_e 512
+  // 1269 vs 1334. 256-row blocks stay available to an explicit plan.
   int block_m;
   if (tok_e <= 80.0) {
     block_m = round_up(std::max(16, static_cast<int>(std::ceil(1.5 * tok_e))), 16);
     block_m = std::min(block_m, 64);
   } else if (tok_e < 120.0) {
     block_m = 64;
-  } else if (tok_e >= 200.0 && k > 2048) {
-    block_m = 256;
   } else {
     block_m = 128;
   }
