@@ -102,9 +102,9 @@ class W4A16MoE:
         self.sorted_ids = torch.empty(self.capacity, dtype=torch.int32, device=dev)
         self.expert_ids = torch.empty(self.capacity // self.block_m, dtype=torch.int32, device=dev)
         self.ntp = torch.empty(1, dtype=torch.int32, device=dev)
-        # The down GEMM may take other blocks than gate_up (at large tok_e the
-        # long gate_up reduction takes 256-row blocks, down 128): gate_up
-        # writes its rows in token order, so each GEMM reads its own routing.
+        # The down GEMM may take other blocks than gate_up (when the plans
+        # differ, e.g. a 256-row gate_up plan): gate_up writes its rows in
+        # token order, so each GEMM reads its own routing.
         self.block_m_dn = self.plan_dn.block_m
         if self.block_m_dn != self.block_m:
             self.capacity_dn = ops.w4a16_align_capacity(numel, self.num_experts, self.block_m_dn)
