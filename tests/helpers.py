@@ -35,3 +35,33 @@ def bf16_bits(t: torch.Tensor) -> np.ndarray:
 
 def dev(a: np.ndarray, device) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+
+GUARD = 4096      # guard bytes on each side: a multiple of 256 keeps every view aligned
+PATTERN = 0xA5
+
+
+class Guarded:
+    """A buffer of `shape` and `dtype` in the middle of a larger allocation
+    whose first and last GUARD bytes hold PATTERN; ``t`` is the view a call
+    writes into, ``check`` asserts that both guards are intact."""
+
+    def __init__(self, shape, dtype, device, fill=None):
+        shape = tuple(shape) if isinstance(shape, (tuple, list)) else (shape,)
+        numel = int(np.prod(shape)) if shape else 1
+        self.nbytes = numel * torch.empty((), dtype=dtype).element_size()
+        self.raw = torch.full((GUARD + self.nbytes + GUARD,), PATTERN, dtype=torch.uint8,
+                              device=device)
+        self.t = self.raw[GUARD:GUARD + self.nbytes].view(dtype).view(shape)
+        if fill is not None:
+            self.t.fill_(fill)
+
+    def check(self, what):
+        if self.raw.is_cuda:
+            torch.cuda.synchronize()
+        b = self.raw.cpu().numpy()
+        head = np.flatnonzero(b[:GUARD] != PATTERN)
+        tail = np.flatnonzero(b[GUARD + self.nbytes:] != PATTERN)
+        assert head.size == 0 and tail.size == 0, (
+            f"{what}: guard bytes changed (head offsets {head[:8] - GUARD}, "
+            f"tail offsets past the end {tail[:8]})")
