@@ -81,60 +81,90 @@ def test_prepack_writes_only_its_blob(cuda_dev, layout):
     assert torch.equal(out.t, ops.w4a16_prepack(q, sc, layout=layout))
 
 
-@pytest.mark.parametrize("bm", [16, 32, 64, 128, 256])
-def test_indexed_gemms_write_only_their_outputs(cuda_dev, bm):
-    p = _problem()
-    pk_gu = ops.w4a16_prepack(dev(p.q_gu, cuda_dev), dev(p.s_gu.view(np.int16), cuda_dev))
-    pk_dn = ops.w4a16_prepack(dev(p.q_dn, cuda_dev), dev(p.s_dn.view(np.int16), cuda_dev))
-    ids = dev(p.topk_ids, cuda_dev)
-    cap = ops.w4a16_align_capacity(p.numel, p.num_experts, bm)
-    sid, eid, ntp = ops.w4a16_moe_align_block_size(ids, p.num_experts, bm, cap)
-    x = bf16_tensor(p.x, cuda_dev)
-    w = dev(p.topk_weights, cuda_dev)
+def _indexed_pair(p, plan_gu, plan_dn, device, what, deterministic=True):
+    """gate_up, then down on silu_and_mul of it, into guarded outputs and
+    workspaces; each against the same call on plain tensors."""
+    pk_gu = ops.w4a16_prepack(dev(p.q_gu, device), dev(p.s_gu.view(np.int16), device))
+    pk_dn = ops.w4a16_prepack(dev(p.q_dn, device), dev(p.s_dn.view(np.int16), device))
+    ids = dev(p.topk_ids, device)
+    x = bf16_tensor(p.x, device)
+    w = dev(p.topk_weights, device)
     n_gu, k_gu, n_dn, k_dn = 2 * p.inter, p.hidden, p.hidden, p.inter
 
     # gate_up: BF16 rows at their routing positions
-    plan = _plan(bm, n_gu, k_gu)
-    ws = _ws(ops.w4a16_workspace_size(plan, cap, k_gu), cuda_dev)
-    out = Guarded((p.numel, n_gu), torch.bfloat16, cuda_dev, fill=0.0)
+    cap = ops.w4a16_align_capacity(p.numel, p.num_experts, plan_gu.block_m)
+    sid, eid, ntp = ops.w4a16_moe_align_block_size(ids, p.num_experts, plan_gu.block_m, cap)
+    ws = _ws(ops.w4a16_workspace_size(plan_gu, cap, k_gu), device)
+    out = Guarded((p.numel, n_gu), torch.bfloat16, device, fill=0.0)
     ops.w4a16_moe_indexed_gemm(ops.W4A16_GATE_UP, pk_gu, p.num_experts, n_gu, k_gu, x,
-                               p.tokens, p.topk, sid, eid, ntp, plan, ws.t, out=out.t)
-    out.check(f"gate_up output bm={bm}")
-    ws.check(f"gate_up workspace bm={bm}")
+                               p.tokens, p.topk, sid, eid, ntp, plan_gu, ws.t, out=out.t)
+    out.check(f"{what}: gate_up output")
+    ws.check(f"{what}: gate_up workspace")
     assert ops.w4a16_read_device_status(ws.t)[0] == ops.W4A16_OK
-    ref = torch.zeros((p.numel, n_gu), dtype=torch.bfloat16, device=cuda_dev)
+    ref = torch.zeros((p.numel, n_gu), dtype=torch.bfloat16, device=device)
     ops.w4a16_moe_indexed_gemm(ops.W4A16_GATE_UP, pk_gu, p.num_experts, n_gu, k_gu, x,
-                               p.tokens, p.topk, sid, eid, ntp, plan,
-                               ops.new_workspace(plan, cuda_dev, cap, k_gu), out=ref)
+                               p.tokens, p.topk, sid, eid, ntp, plan_gu,
+                               ops.new_workspace(plan_gu, device, cap, k_gu), out=ref)
     assert torch.equal(out.t.view(torch.int16), ref.view(torch.int16))
+    del out, ws
 
     # down: the top-k weighted FP32 adds into the token rows
     act = ops.w4a16_silu_and_mul(ref)
-    plan = _plan(bm, n_dn, k_dn)
-    ws = _ws(ops.w4a16_workspace_size(plan, cap, k_dn), cuda_dev)
-    out = Guarded((p.tokens, n_dn), torch.float32, cuda_dev, fill=float("nan"))
+    del ref
+    cap = ops.w4a16_align_capacity(p.numel, p.num_experts, plan_dn.block_m)
+    sid, eid, ntp = ops.w4a16_moe_align_block_size(ids, p.num_experts, plan_dn.block_m, cap)
+    ws = _ws(ops.w4a16_workspace_size(plan_dn, cap, k_dn), device)
+    out = Guarded((p.tokens, n_dn), torch.float32, device, fill=float("nan"))
     ops.w4a16_moe_indexed_gemm(ops.W4A16_DOWN, pk_dn, p.num_experts, n_dn, k_dn, act,
-                               p.tokens, p.topk, sid, eid, ntp, plan, ws.t, topk_weights=w,
+                               p.tokens, p.topk, sid, eid, ntp, plan_dn, ws.t, topk_weights=w,
                                out=out.t)
-    out.check(f"down output bm={bm}")
-    ws.check(f"down workspace bm={bm}")
+    out.check(f"{what}: down output")
+    ws.check(f"{what}: down workspace")
     assert ops.w4a16_read_device_status(ws.t)[0] == ops.W4A16_OK
     y = ops.w4a16_moe_indexed_gemm(ops.W4A16_DOWN, pk_dn, p.num_experts, n_dn, k_dn, act,
-                                   p.tokens, p.topk, sid, eid, ntp, plan,
-                                   ops.new_workspace(plan, cuda_dev, cap, k_dn), topk_weights=w)
-    torch.testing.assert_close(out.t, y, rtol=1e-6, atol=1e-6)
+                                   p.tokens, p.topk, sid, eid, ntp, plan_dn,
+                                   ops.new_workspace(plan_dn, device, cap, k_dn), topk_weights=w)
+    torch.testing.assert_close(out.t, y, rtol=1e-5, atol=1e-5)
+    if not deterministic:
+        return
 
     # the deterministic down pass: rows parked in the workspace, then summed
-    size = (ops.w4a16_workspace_size(plan, cap, k_dn)
+    size = (ops.w4a16_workspace_size(plan_dn, cap, k_dn)
             + ops.w4a16_deterministic_bytes(cap, n_dn, p.numel))
-    ws = _ws(size, cuda_dev)
-    out = Guarded((p.tokens, n_dn), torch.float32, cuda_dev, fill=float("nan"))
+    ws = _ws(size, device)
+    out = Guarded((p.tokens, n_dn), torch.float32, device, fill=float("nan"))
     ops.w4a16_moe_indexed_gemm(ops.W4A16_DOWN, pk_dn, p.num_experts, n_dn, k_dn, act,
-                               p.tokens, p.topk, sid, eid, ntp, plan, ws.t, topk_weights=w,
+                               p.tokens, p.topk, sid, eid, ntp, plan_dn, ws.t, topk_weights=w,
                                out=out.t, flags=ops.W4A16_FLAG_DETERMINISTIC)
-    out.check(f"deterministic down output bm={bm}")
-    ws.check(f"deterministic down workspace bm={bm}")
-    torch.testing.assert_close(out.t, y, rtol=1e-5, atol=1e-6)
+    out.check(f"{what}: deterministic down output")
+    ws.check(f"{what}: deterministic down workspace")
+    torch.testing.assert_close(out.t, y, rtol=1e-5, atol=1e-5)
+
+
+@pytest.mark.parametrize("bm", [16, 32, 64, 128, 256])
+def test_indexed_gemms_write_only_their_outputs(cuda_dev, bm):
+    p = _problem()
+    _indexed_pair(p, _plan(bm, 2 * p.inter, p.hidden), _plan(bm, p.hidden, p.inter), cuda_dev,
+                  f"bm={bm}")
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["ep8_decode", "tp8_64", "ep8_prefill", "ep8_prefill_x4"])
+def test_full_size_shards_write_only_their_outputs(cuda_dev, name):
+    # the shard shapes in the plans the scheduler gives them (block_m 32, 16,
+    # 64 and 128; the long gate_up reductions of the prefill shards take the
+    # rastered item order, the four-times shard's gate_up the BF16 staging)
+    if name == "ep8_decode":
+        p = wl.ep8_decode()
+    elif name == "tp8_64":
+        p = wl.tp8(64)
+    else:
+        p = wl.ep8_prefill(scale=4 if name.endswith("x4") else 1)
+    hint = p.tok_e_hint()
+    plan_gu = ops.w4a16_plan(p.tokens, p.topk, p.num_experts, 2 * p.inter, p.hidden, hint)
+    plan_dn = ops.w4a16_plan(p.tokens, p.topk, p.num_experts, p.hidden, p.inter, hint)
+    _indexed_pair(p, plan_gu, plan_dn, cuda_dev, name, deterministic=False)
+    torch.cuda.empty_cache()
 
 
 @pytest.mark.parametrize("bm", [32, 128])
