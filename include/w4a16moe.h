@@ -20,6 +20,11 @@
  *   enqueued. Unless a flag says otherwise no call synchronises, so calls can
  *   be captured in a CUDA graph (the over-allocated routing buffers make the
  *   grid independent of the routing, [P-lens] "ランタイムの考慮事項").
+ * - A pointer to an array of zero elements may be NULL: the activation,
+ *   the output and the top-k weights when there are no tokens (m = 0 for
+ *   the grouped calls), sorted_ids and expert_ids when the capacity is 0.
+ *   num_tokens_padded, the packed weights and the plan are never NULL.
+ *   An empty call enqueues nothing that touches them.
  * - Every call validates its arguments on the host before it enqueues
  *   anything and returns a w4a16_status; nothing is enqueued on error.
  *   A failed launch returns W4A16_ERR_CUDA.

@@ -181,6 +181,45 @@ def test_gemm_argument_checks_before_any_launch(lib):
         == ops.W4A16_ERR_INVALID_ARG
 
 
+def test_empty_calls_accept_null_arrays_and_enqueue_nothing(lib):
+    # no tokens, capacity 0: the zero-element arrays may be NULL and the calls
+    # return before any CUDA call (so this runs without a GPU); a NULL array
+    # that has elements is refused
+    fake = ctypes.c_void_p(1 << 20)
+    plan = ops.w4a16_plan(64, 2, 8, 1024, 512, 0.0)
+    for mode in (ops.W4A16_GATE_UP, ops.W4A16_DOWN):
+        assert lib.w4a16_moe_indexed_gemm(mode, fake, 8, 1024, 512, None, 0, 2, None, None, fake,
+                                          0, None, None, 0, ctypes.byref(plan), fake, 1 << 20,
+                                          None) == ops.W4A16_OK
+    assert lib.w4a16_moe_indexed_gemm(ops.W4A16_GATE_UP, fake, 8, 1024, 512, fake, 64, 2, fake,
+                                      fake, fake, 256, None, None, 0, ctypes.byref(plan), fake,
+                                      1 << 30, None) == ops.W4A16_ERR_INVALID_ARG   # no output
+    assert lib.w4a16_moe_indexed_gemm(ops.W4A16_GATE_UP, fake, 8, 1024, 512, fake, 64, 2, None,
+                                      fake, fake, 256, None, fake, 0, ctypes.byref(plan), fake,
+                                      1 << 30, None) == ops.W4A16_ERR_INVALID_ARG   # no sorted_ids
+    assert lib.w4a16_moe_indexed_gemm(ops.W4A16_GATE_UP, fake, 8, 1024, 512, None, 0, 2, None,
+                                      None, None, 0, None, None, 0, ctypes.byref(plan), fake,
+                                      1 << 20, None) == ops.W4A16_ERR_INVALID_ARG   # ntp NULL
+    gplan = ops.w4a16_grouped_plan(ops.W4A16_GROUPED_CONTIGUOUS, 128, 1024, 512)
+    assert lib.w4a16_moe_grouped_gemm(ops.W4A16_GROUPED_CONTIGUOUS, fake, 8, 1024, 512, None, 0,
+                                      None, 0, None, 0, ctypes.byref(gplan), fake, 256,
+                                      None) == ops.W4A16_OK
+    assert lib.w4a16_moe_grouped_gemm(ops.W4A16_GROUPED_MASKED, fake, 8, 1024, 512, None, 0,
+                                      fake, 0, None, 0, ctypes.byref(gplan), fake, 256,
+                                      None) == ops.W4A16_OK
+    assert lib.w4a16_moe_grouped_gemm(ops.W4A16_GROUPED_MASKED, fake, 8, 1024, 512, None, 0,
+                                      None, 0, None, 0, ctypes.byref(gplan), fake, 256,
+                                      None) == ops.W4A16_ERR_INVALID_ARG   # masked_m [E] NULL
+    glu = ops.w4a16_plan(64, 2, 8, 1024, 512, 0.0)
+    glu.layout = ops.W4A16_LAYOUT_KTILE64_GLU16
+    assert lib.w4a16_moe_layer(fake, fake, 8, 512, 512, None, 0, 2, None, None, fake, 0, None,
+                               None, 0, ctypes.byref(glu), fake, 256, None) == ops.W4A16_OK
+    assert lib.w4a16_moe_layer(fake, fake, 8, 512, 512, fake, 64, 2, fake, fake, fake, 256, fake,
+                               None, 0, ctypes.byref(glu), fake, 1 << 30,
+                               None) == ops.W4A16_ERR_INVALID_ARG   # no output
+    assert lib.w4a16_silu_and_mul(None, 0, 512, None, None) == ops.W4A16_OK
+
+
 def test_grouped_and_align_argument_checks(lib):
     fake = ctypes.c_void_p(1 << 20)
     plan = ops.w4a16_plan(32, 1, 1, 256, 256, 32.0)

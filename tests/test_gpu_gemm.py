@@ -170,6 +170,41 @@ def test_no_routed_rows_leaves_output_untouched(cuda_dev):
     assert torch.all(torch.isnan(g))
 
 
+@pytest.mark.parametrize("single_launch", [False, True])
+def test_empty_batch(cuda_dev, single_launch):
+    # no tokens at all: align writes a padded total of 0 (its zero-element
+    # arrays passed as NULL), and the layer returns an empty output, through
+    # two launches or one
+    p = wl.tiny(seed=12)
+    ids = torch.empty((0, p.topk), dtype=torch.int32, device=cuda_dev)
+    assert ops.w4a16_align_capacity(0, p.num_experts, 32) == 0
+    ntp = torch.full((1,), -5, dtype=torch.int32, device=cuda_dev)
+    empty = torch.empty(0, dtype=torch.int32, device=cuda_dev)
+    ops.w4a16_moe_align_block_size(ids, p.num_experts, 32, 0, out=(empty, empty, ntp))
+    assert int(ntp.item()) == 0
+    layout = ops.W4A16_LAYOUT_KTILE64_GLU16 if single_launch else ops.W4A16_LAYOUT_KTILE64
+    gu = moe_mod.PackedExperts.from_checkpoint(dev(p.q_gu, cuda_dev),
+                                               dev(p.s_gu.view(np.int16), cuda_dev), layout=layout)
+    dn = moe_mod.PackedExperts.from_checkpoint(dev(p.q_dn, cuda_dev),
+                                               dev(p.s_dn.view(np.int16), cuda_dev))
+    layer = moe_mod.W4A16MoE(gu, dn, p.topk, p.tokens, device=cuda_dev,
+                             single_launch=single_launch)
+    x = torch.empty((0, p.hidden), dtype=torch.bfloat16, device=cuda_dev)
+    w = torch.empty((0, p.topk), dtype=torch.float32, device=cuda_dev)
+    y = layer.forward(x, ids, w)
+    torch.cuda.synchronize()
+    assert y.shape == (0, p.hidden)
+    assert int(layer.ntp.item()) == 0
+    ws = layer.layer_workspace if single_launch else layer.workspace
+    assert ops.w4a16_read_device_status(ws)[0] == ops.W4A16_OK
+    # the same layer on a real batch afterwards
+    y = layer.forward(bf16_tensor(p.x, cuda_dev), dev(p.topk_ids, cuda_dev),
+                      dev(p.topk_weights, cuda_dev))
+    _, _, _, y_ref = oracle.moe_layer(p.x, p.topk_ids, p.topk_weights, p.q_gu, p.s_gu,
+                                      p.q_dn, p.s_dn)
+    assert_close(y.cpu().numpy(), y_ref, "layer after an empty batch")
+
+
 def test_schedules_are_bitwise_identical(cuda_dev):
     # Pipelining and scheduling choices do not change any gate_up output bit
     # (every row's K reduction runs in the same order): block size, ring

@@ -219,7 +219,9 @@ w4a16_status w4a16_moe_align_block_size(const int32_t* topk_ids, int tokens, int
                                         int32_t* num_tokens_padded, void* stream) {
   if (tokens < 0 || topk <= 0 || num_experts <= 0 || block_m <= 0 || capacity < 0)
     return W4A16_ERR_INVALID_ARG;
-  if (sorted_ids == nullptr || expert_ids == nullptr || num_tokens_padded == nullptr)
+  // arrays of zero elements may be NULL (num_tokens_padded always has one)
+  if (num_tokens_padded == nullptr ||
+      (capacity > 0 && (sorted_ids == nullptr || expert_ids == nullptr)))
     return W4A16_ERR_INVALID_ARG;
   const long long numel = static_cast<long long>(tokens) * topk;
   if (numel > 0 && topk_ids == nullptr) return W4A16_ERR_INVALID_ARG;
@@ -349,10 +351,13 @@ w4a16_status indexed_gemm(int mode, const void* packed, int num_experts, int n, 
   if (num_experts <= 0 || n <= 0 || k <= 0 || tokens < 0 || topk <= 0 || capacity < 0)
     return W4A16_ERR_INVALID_ARG;
   if (k % kGroup != 0) return W4A16_ERR_UNSUPPORTED;
-  if (plan == nullptr || packed == nullptr || out == nullptr || sorted_ids == nullptr ||
-      expert_ids == nullptr || num_tokens_padded == nullptr)
+  // arrays of zero elements may be NULL: the output and the activation when
+  // there are no tokens, the routing arrays when the capacity is 0
+  if (plan == nullptr || packed == nullptr || num_tokens_padded == nullptr)
     return W4A16_ERR_INVALID_ARG;
-  if (tokens > 0 && a == nullptr) return W4A16_ERR_INVALID_ARG;
+  if (tokens > 0 && (a == nullptr || out == nullptr)) return W4A16_ERR_INVALID_ARG;
+  if (capacity > 0 && (sorted_ids == nullptr || expert_ids == nullptr))
+    return W4A16_ERR_INVALID_ARG;
   if (mode == W4A16_DOWN && tokens > 0 && topk_weights == nullptr) return W4A16_ERR_INVALID_ARG;
   if ((flags & ~(W4A16_FLAG_VALIDATE_ROUTING | W4A16_FLAG_ACCUMULATE |
                  W4A16_FLAG_DETERMINISTIC)) != 0)
@@ -512,8 +517,11 @@ w4a16_status w4a16_moe_grouped_gemm(int kind, const void* packed, int num_expert
     return W4A16_ERR_INVALID_ARG;
   if (num_experts <= 0 || n <= 0 || k <= 0 || m < 0) return W4A16_ERR_INVALID_ARG;
   if (k % kGroup != 0) return W4A16_ERR_UNSUPPORTED;
-  if (packed == nullptr || out == nullptr || layout == nullptr) return W4A16_ERR_INVALID_ARG;
-  if (m > 0 && a == nullptr) return W4A16_ERR_INVALID_ARG;
+  // arrays of zero elements may be NULL: a, out and the contiguous layout
+  // when m is 0 (the masked layout always has num_experts entries)
+  if (packed == nullptr) return W4A16_ERR_INVALID_ARG;
+  if (m > 0 && (a == nullptr || out == nullptr || layout == nullptr)) return W4A16_ERR_INVALID_ARG;
+  if (kind == W4A16_GROUPED_MASKED && layout == nullptr) return W4A16_ERR_INVALID_ARG;
   if ((flags & ~W4A16_FLAG_VALIDATE_ROUTING) != 0) return W4A16_ERR_INVALID_ARG;
   if (!aligned16(packed) || !aligned16(out) || (a != nullptr && !aligned16(a)))
     return W4A16_ERR_INVALID_ARG;
@@ -646,8 +654,9 @@ w4a16_status w4a16_moe_route_align(const void* logits, int logits_dtype, int tok
   if (num_local_experts > 1024 || block_m > 1024) return W4A16_ERR_UNSUPPORTED;
   const long long numel = static_cast<long long>(tokens) * topk;
   if (numel >= (1LL << 30)) return W4A16_ERR_UNSUPPORTED;
-  if (sorted_ids == nullptr || expert_ids == nullptr || num_tokens_padded == nullptr ||
-      arrivals == nullptr)
+  // arrays of zero elements may be NULL (the routing arrays at capacity 0)
+  if (num_tokens_padded == nullptr || arrivals == nullptr ||
+      (capacity > 0 && (sorted_ids == nullptr || expert_ids == nullptr)))
     return W4A16_ERR_INVALID_ARG;
   if (tokens > 0 && (logits == nullptr || topk_ids == nullptr || topk_weights == nullptr))
     return W4A16_ERR_INVALID_ARG;
@@ -689,10 +698,15 @@ w4a16_status w4a16_moe_layer(const void* packed_gate_up, const void* packed_down
   if (num_experts <= 0 || hidden <= 0 || inter <= 0 || tokens < 0 || topk <= 0 || capacity < 0)
     return W4A16_ERR_INVALID_ARG;
   if (hidden % kGroup != 0 || inter % 64 != 0 || hidden % 4 != 0) return W4A16_ERR_UNSUPPORTED;
-  if (plan == nullptr || packed_gate_up == nullptr || packed_down == nullptr || out == nullptr ||
-      sorted_ids == nullptr || expert_ids == nullptr || num_tokens_padded == nullptr)
+  // arrays of zero elements may be NULL: x, the weights and the output when
+  // there are no tokens, the routing arrays when the capacity is 0
+  if (plan == nullptr || packed_gate_up == nullptr || packed_down == nullptr ||
+      num_tokens_padded == nullptr)
     return W4A16_ERR_INVALID_ARG;
-  if (tokens > 0 && (x == nullptr || topk_weights == nullptr)) return W4A16_ERR_INVALID_ARG;
+  if (tokens > 0 && (x == nullptr || topk_weights == nullptr || out == nullptr))
+    return W4A16_ERR_INVALID_ARG;
+  if (capacity > 0 && (sorted_ids == nullptr || expert_ids == nullptr))
+    return W4A16_ERR_INVALID_ARG;
   if ((flags & ~(W4A16_FLAG_VALIDATE_ROUTING | W4A16_FLAG_ACCUMULATE)) != 0)
     return W4A16_ERR_INVALID_ARG;
   if (!aligned16(packed_gate_up) || !aligned16(packed_down) || !aligned16(out) ||
