@@ -220,6 +220,20 @@ def test_empty_calls_accept_null_arrays_and_enqueue_nothing(lib):
     assert lib.w4a16_silu_and_mul(None, 0, 512, None, None) == ops.W4A16_OK
 
 
+def test_row_counts_of_2_pow_30_are_refused(lib):
+    # flattened routed rows (tokens x topk) index the routing as int32 with
+    # room for the sentinel: 2^30 rows and above are refused before any
+    # CUDA call
+    fake = ctypes.c_void_p(1 << 20)
+    plan = ops.w4a16_plan(64, 2, 8, 1024, 512, 0.0)
+    big = 1 << 27   # x 8 = 2^30
+    assert lib.w4a16_moe_indexed_gemm(ops.W4A16_GATE_UP, fake, 8, 1024, 512, fake, big, 8, fake,
+                                      fake, fake, 256, None, fake, 0, ctypes.byref(plan), fake,
+                                      1 << 40, None) == ops.W4A16_ERR_UNSUPPORTED
+    assert lib.w4a16_moe_align_block_size(fake, big, 8, 8, 16, 1 << 30, fake, fake, fake,
+                                          None) == ops.W4A16_ERR_UNSUPPORTED
+
+
 def test_grouped_and_align_argument_checks(lib):
     fake = ctypes.c_void_p(1 << 20)
     plan = ops.w4a16_plan(32, 1, 1, 256, 256, 32.0)

@@ -381,8 +381,7 @@ w4a16_status indexed_gemm(int mode, const void* packed, int num_experts, int n, 
   if (glu && n % kTileRows != 0) return W4A16_ERR_UNSUPPORTED;
   const int bm = plan->block_m;
   if (capacity % bm != 0) return W4A16_ERR_INVALID_ARG;
-  const long long numel = static_cast<long long>(tokens) * topk;
-  if (numel >= (1LL << 30)) return W4A16_ERR_UNSUPPORTED;
+  const long long numel = numel_all;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   if (flags & W4A16_FLAG_VALIDATE_ROUTING) {
