@@ -59,9 +59,8 @@ class Guarded:
     def check(self, what):
         if self.raw.is_cuda:
             torch.cuda.synchronize()
-        b = self.raw.cpu().numpy()
-        head = np.flatnonzero(b[:GUARD] != PATTERN)
-        tail = np.flatnonzero(b[GUARD + self.nbytes:] != PATTERN)
+        head = np.flatnonzero(self.raw[:GUARD].cpu().numpy() != PATTERN)
+        tail = np.flatnonzero(self.raw[GUARD + self.nbytes:].cpu().numpy() != PATTERN)
         assert head.size == 0 and tail.size == 0, (
             f"{what}: guard bytes changed (head offsets {head[:8] - GUARD}, "
             f"tail offsets past the end {tail[:8]})")
