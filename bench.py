@@ -535,6 +535,16 @@ def grouped_inputs(name, device, packed):
     return calls, label, rows, active
 
 
+def grouped_work(rows, active):
+    """Algorithmic bytes and flops of one grouped step on the EP8 shard: the
+    weights of the experts with rows, each valid BF16 input row read once and
+    each valid BF16 output row written once, 2 * rows * n * k flops per GEMM."""
+    gu_bytes = active * 4096 * 7168 * WEIGHT_BYTES + rows * 7168 * 2 + rows * 4096 * 2
+    dn_bytes = active * 7168 * 2048 * WEIGHT_BYTES + rows * 2048 * 2 + rows * 7168 * 2
+    return {"gate_up": {"bytes": gu_bytes, "flops": 2.0 * rows * 4096 * 7168},
+            "down": {"bytes": dn_bytes, "flops": 2.0 * rows * 7168 * 2048}}
+
+
 def grouped_config(name, packed, device, flush, steps, warmup, peaks):
     """One step = the grouped gate_up GEMM then the grouped down GEMM (the
     activation between them untimed), L2 flushed before each step."""
@@ -570,9 +580,9 @@ def grouped_config(name, packed, device, flush, steps, warmup, peaks):
         raise SystemExit(f"device status {word:#x} in configuration {name}")
     gu_us = statistics.mean(e[0].elapsed_time(e[1]) * 1e3 for e in ev)
     dn_us = statistics.mean(e[1].elapsed_time(e[2]) * 1e3 for e in ev)
-    gu_bytes = active * 4096 * 7168 * WEIGHT_BYTES + rows * 7168 * 2 + rows * 4096 * 2
-    dn_bytes = active * 7168 * 2048 * WEIGHT_BYTES + rows * 2048 * 2 + rows * 7168 * 2
-    flops = 2.0 * rows * 4096 * 7168 + 2.0 * rows * 7168 * 2048
+    work = grouped_work(rows, active)
+    gu_bytes, dn_bytes = work["gate_up"]["bytes"], work["down"]["bytes"]
+    flops = work["gate_up"]["flops"] + work["down"]["flops"]
     layer_us = gu_us + dn_us
     hbm, tf, src = peaks
     if name.startswith("grouped_contig_"):

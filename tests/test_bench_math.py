@@ -51,6 +51,21 @@ def test_tp8_work_counts_only_experts_with_rows():
     assert w["rows"] == 16 * 8
 
 
+def test_grouped_work():
+    # contiguous, 128 rows for each of 48 experts: 6144 rows
+    w = bench.grouped_work(6144, 48)
+    assert w["gate_up"]["flops"] + w["down"]["flops"] == 2 * 6144 * 44040192   # 4096*7168 + 7168*2048
+    assert (w["gate_up"]["flops"] + w["down"]["flops"]) / 1e9 == pytest.approx(541.17, abs=0.01)
+    # masked, budget 32: all 48 experts' weights (1.189 GB) plus the rows in and out
+    counts = wl.masked_counts(48, 32, seed=1)
+    rows = int(counts.sum())
+    w = bench.grouped_work(rows, 48)
+    weights = 48 * (4096 * 7168 + 7168 * 2048) * B_W
+    assert weights / 1e9 == pytest.approx(1.189, abs=0.001)
+    assert w["gate_up"]["bytes"] + w["down"]["bytes"] == pytest.approx(
+        weights + rows * (7168 + 4096) * 2 + rows * (2048 + 7168) * 2)
+
+
 def test_roofline_entry_fractions():
     r = bench.roofline_entry("hbm", "k", 3400.0, 6800.0, 8000.0, "measured hbm_gbs",
                              {"traffic": None})
